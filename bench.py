@@ -1,0 +1,600 @@
+#!/usr/bin/env python3
+"""Benchmark of the SFI decode-attention path on one GB300 (replicas on N GPUs).
+
+Workload (the paper's Table 1 setting with Qwen3-0.6B attention shapes): 16 query
+heads / 8 KV heads, head_dim 128, 28 layers, bf16 paged KV (page 16), KV length
+16384, batch 16, sink 64 + selected + recent 256. Seeded N(0,1) Q/K/V on the device
+with heavy-hitter keys on 2% of the candidates.
+
+One bench step = one SFI refresh cycle of 16 decode steps over all 28 layers: a slow
+step (append, dense attention + masked group-summed scores on the main stream,
+Selector + compaction on the aux stream overlapped with the next layers), then 15
+fast steps (append, sparse attention over sink + selected + recent) at 6.25%
+retention (k = 704). The whole cycle is one CUDA graph replay. `value` is the
+decode-attention time per decode step (cycle time / 16, all 28 layers).
+
+Also reported: the fast-step retention sweep of Table 1 against the dense decode
+kernel, the end-to-end time through the public API with host buffers (per decode
+step: H2D of q/k/v, D2H of the outputs), the roofline of the dominant kernel, and
+the CPU oracle timed on a bounded sample (the reference arm: --impl reference).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode-attn µs/step & achieved HBM GB/s vs ~8 TB/s; sparse/dense speedup at 16K"
+UNIT = "us/step"
+WL = dict(workload="qwen3-0.6b-attn kv16k b16 sfi-cycle", num_q_heads=16, num_kv_heads=8, head_dim=128,
+          page_size=16, layers=28, batch=16, kv_len=16384, sink=64, recent=256, retention=0.0625,
+          refresh_interval=16, heavy_hitter_frac=0.02, heavy_hitter_beta=3.0)
+# Table 1 retention points at 16K: n/64 of the KV length (n = 1 is below sink + recent: recent 192, k = 0)
+SWEEP_N = [1, 4, 8, 16, 24, 32, 48, 63, 64]
+TABLE1 = {1: 10.67, 4: 9.56, 8: 7.15, 16: 3.96, 24: 2.75, 32: 2.10, 48: 1.43, 63: 1.10, 64: 1.00}
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["sfi", "reference"], default="sfi")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the retention sweep")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
+    ap.add_argument("--layers", type=int, default=WL["layers"])
+    ap.add_argument("--batch", type=int, default=WL["batch"])
+    ap.add_argument("--kv-len", type=int, default=WL["kv_len"])
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# ranks
+# ---------------------------------------------------------------------------
+def rank_info():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+class Ranks:
+    def __init__(self):
+        self.rank, self.world, self.local = rank_info()
+        self.pg = None
+        if self.world > 1:
+            import torch.distributed as dist
+            dist.init_process_group("gloo")
+            self.dist = dist
+
+    def barrier(self):
+        if self.world > 1:
+            self.dist.barrier()
+
+    def max(self, x: float) -> float:
+        if self.world == 1:
+            return x
+        import torch
+        t = torch.tensor([x], dtype=torch.float64)
+        self.dist.all_reduce(t, op=self.dist.ReduceOp.MAX)
+        return float(t.item())
+
+    def close(self):
+        if self.world > 1:
+            self.dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.thread.join(timeout=2)
+        sm, smax, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            f = [x.strip() for x in l.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax = float(f[2])
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# algorithmic bytes
+# ---------------------------------------------------------------------------
+def fast_bytes(B, Hq, Hkv, D, P, n_ret, W):
+    """K/V rows of sink + selected + recent, q in, o out (fp32) and lse, recent page ids."""
+    return B * Hkv * n_ret * 4 * D + B * Hq * D * (2 + 4) + B * Hq * 4 + B * (math.ceil(W / P) + 1) * 4
+
+
+def dense_bytes(B, Hq, Hkv, D, P, L, scores):
+    b = B * Hkv * L * 4 * D + B * math.ceil(L / P) * 4 + B * Hq * D * (2 + 4) + B * Hq * 4
+    if scores:
+        b += B * Hkv * L * 4
+    return b
+
+
+def select_bytes(B, Hkv, nC, k):
+    return B * Hkv * nC * 4 + B * Hkv * k * 4
+
+
+def compact_bytes(B, Hkv, D, S, k):
+    return 2 * B * Hkv * (S + k) * 4 * D + B * Hkv * k * 4
+
+
+def append_bytes(B, Hkv, D):
+    return 2 * 2 * B * Hkv * D * 2
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            j = json.load(f)
+        return float(j["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_gpu(args, ranks: Ranks):
+    import numpy as np
+    import torch
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    dev = torch.device("cuda", ranks.local)
+    torch.cuda.set_device(dev)
+    Hq, Hkv, D, P = WL["num_q_heads"], WL["num_kv_heads"], WL["head_dim"], WL["page_size"]
+    NL, B, L0 = args.layers, args.batch, args.kv_len
+    S, W, cyc = WL["sink"], WL["recent"], WL["refresh_interval"]
+    shape = sfi.AttnShape(Hq, Hkv, D, P)
+    k_main = syn.retention_budget(WL["retention"], L0, S, W)
+    k_cap = max(k_main, L0 - S - W)  # room for the 100% sweep point
+    seed0 = 1000 + 97 * ranks.rank
+
+    # ---- requests: shuffled page table with room for the cycle's appends ----
+    g = syn.rng(seed0, 1)
+    table, num_pages = syn.make_page_table(g, [L0 + cyc] * B, P, shuffle=True)
+    page_table = torch.as_tensor(table).to(dev)
+    off, cap = sfi.compact_layout(shape, S, [k_cap] * B, device=dev)
+    batch = sfi.DecodeBatch(page_table, off, cap, torch.full((B,), k_main, dtype=torch.int32, device=dev), k_cap,
+                            score_stride=L0 + cyc)
+    seq_steps = torch.tensor([[L0 + t] * B for t in range(cyc)], dtype=torch.int32, device=dev)  # [cyc][B]
+
+    # ---- per-step inputs (all layers) ----
+    q_all = torch.empty((cyc, NL, B, Hq, D), dtype=torch.bfloat16, device=dev)
+    kn_all = torch.empty((cyc, NL, B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vn_all = torch.empty_like(kn_all)
+    syn.device_normal_bf16_(q_all, syn.stream_seed(seed0, 2))
+    syn.device_normal_bf16_(kn_all, syn.stream_seed(seed0, 3))
+    syn.device_normal_bf16_(vn_all, syn.stream_seed(seed0, 4))
+    out = torch.zeros((NL, B, Hq, D), dtype=torch.float32, device=dev)
+
+    def pool_init(i, kp, vp):
+        syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 10, i))
+        syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 11, i))
+        syn.device_plant_heavy_hitters_(kp, page_table, q_all[0, i], seq_steps[0], S, W, WL["heavy_hitter_frac"],
+                                        WL["heavy_hitter_beta"], syn.stream_seed(seed0, 12, i))
+
+    t_alloc = time.time()
+    layers = sfi.allocate_layers(shape, NL, num_pages, batch, S, device=dev, pool_init=pool_init)
+    torch.cuda.synchronize()
+    t_alloc = time.time() - t_alloc
+    dec = sfi.SFIDecoder(shape, layers, batch, S, W, max_len=L0 + cyc, device=dev)
+    ios = [sfi.StepIO(q_all[t], kn_all[t], vn_all[t], out) for t in range(cyc)]
+
+    def cycle():
+        dec.slow_step(ios[0], seq_steps[0])
+        for t in range(1, cyc):
+            dec.fast_step(ios[t], seq_steps[t])
+        dec.join()
+
+    # ---- timing events captured as graph nodes around every attention launch ----
+    marks = {"slow": [], "fast": []}
+    open_ev = {}
+
+    def timer(kind, phase, stream):
+        ev = torch.cuda.Event(enable_timing=True, external=True)
+        ev.record(stream)
+        if phase == "start":
+            open_ev[kind] = ev
+        else:
+            marks[kind].append((open_ev.pop(kind), ev))
+
+    # eager warm-up (sets kernel attributes; checks status) then capture
+    with torch.cuda.stream(dec.main):
+        cycle()
+    torch.cuda.synchronize()
+    assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
+
+    g_cycle = torch.cuda.CUDAGraph()
+    dec.timer = timer
+    with torch.cuda.graph(g_cycle, stream=dec.main):
+        cycle()
+    dec.timer = None
+    launches_per_cycle = NL * 4 + (cyc - 1) * NL * 2
+
+    with torch.cuda.stream(dec.main):
+        for _ in range(args.warmup):
+            g_cycle.replay()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(dev.index)
+    clocks.start()
+    time.sleep(0.3)
+    ranks.barrier()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(dec.main):
+        e0.record(dec.main)
+        for _ in range(args.steps):
+            g_cycle.replay()
+        e1.record(dec.main)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    clk = clocks.stop()
+    ms_cycle = ranks.max(e0.elapsed_time(e1) / args.steps)
+    assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
+
+    # the same cycle captured without the timing event nodes, for their overhead
+    g_plain = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_plain, stream=dec.main):
+        cycle()
+    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(dec.main):
+        for _ in range(args.warmup):
+            g_plain.replay()
+        p0.record(dec.main)
+        for _ in range(args.steps):
+            g_plain.replay()
+        p1.record(dec.main)
+    torch.cuda.synchronize()
+    ms_plain = ranks.max(p0.elapsed_time(p1) / args.steps)
+
+    # per-kernel durations from the events of the last replay of the timed region
+    try:
+        dur = {k: [a.elapsed_time(b) * 1e3 for a, b in v] for k, v in marks.items()}
+        timing_method = "graph event nodes around each launch, last timed replay"
+    except RuntimeError as exc:  # event timing inside graphs unavailable
+        dur = None
+        timing_method = f"unavailable: {exc}"
+
+    # ---- algorithmic bytes of one cycle ----
+    n_ret_fast = S + k_main + W  # per (request, KV head) at L > S + W
+    by_fast = fast_bytes(B, Hq, Hkv, D, P, n_ret_fast, W)
+    by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True)
+    nC = L0 - S - W
+    by_cycle = (NL * (by_slow + select_bytes(B, Hkv, nC, k_main) + compact_bytes(B, Hkv, D, S, k_main)) +
+                (cyc - 1) * NL * by_fast + cyc * NL * append_bytes(B, Hkv, D))
+    us_step = ms_cycle * 1e3 / cyc
+    peak, peak_kind = measured_peaks()
+
+    roofline = None
+    if dur:
+        t_fast = statistics.mean(dur["fast"]) if dur["fast"] else 0.0
+        t_slow = statistics.mean(dur["slow"]) if dur["slow"] else 0.0
+        share_fast = t_fast * len(dur["fast"]) / (ms_cycle * 1e3)
+        share_slow = t_slow * len(dur["slow"]) / (ms_cycle * 1e3)
+        if share_slow >= share_fast:
+            name, per, tl, sh = "attn_decode_kernel<128,dense,scores> (slow step)", by_slow, t_slow, share_slow
+        else:
+            name, per, tl, sh = "attn_decode_kernel<128,fast> (fast step)", by_fast, t_fast, share_fast
+        ach = per / (tl * 1e-6) / 1e9
+        roofline = {"bound": "hbm", "kernel": name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
+                    "frac": round(ach / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
+                    "traffic": None, "bytes_per_launch": per, "avg_launch_us": round(tl, 3),
+                    "time_share": round(sh, 4), "timing": timing_method,
+                    "other": {"fast_avg_us": round(t_fast, 3), "fast_GBps": round(by_fast / (t_fast * 1e-6) / 1e9, 1)
+                              if t_fast else None, "fast_share": round(share_fast, 4),
+                              "slow_avg_us": round(t_slow, 3), "slow_GBps": round(by_slow / (t_slow * 1e-6) / 1e9, 1)
+                              if t_slow else None, "slow_share": round(share_slow, 4)}}
+
+    result = {
+        "metric": METRIC, "value": round(us_step, 3), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_cycle, 4), "higher_is_better": False, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {**WL, "layers": NL, "batch": B, "kv_len": L0, "k": k_main,
+                   "step": f"1 slow + {cyc - 1} fast decode steps x {NL} layers (one CUDA graph)",
+                   "l2": f"inputs larger than L2: {NL} distinct layers, {by_cycle / cyc / 1e9:.2f} GB per decode step",
+                   "parallelism": f"replicas x{ranks.world}"},
+        "us_per_step_without_timing_nodes": round(ms_plain * 1e3 / cyc, 3),
+        "tokens_per_s": round(ranks.world * B * cyc / (ms_cycle * 1e-3), 1),
+        "hbm_GBps_cycle": round(by_cycle / (ms_cycle * 1e-3) / 1e9, 1),
+        "bytes_per_cycle": by_cycle,
+        "gpu_launches": launches_per_cycle * args.steps,
+        "clocks": clk,
+        "roofline": roofline,
+        "alloc_s": round(t_alloc, 1),
+    }
+
+    # ---- end to end through the public API with host buffers ----
+    result["e2e"] = e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks)
+
+    # ---- retention sweep vs dense (Table 1) ----
+    if not args.no_sweep:
+        result["retention_sweep"] = retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps,
+                                                    NL, B, Hq, Hkv, D, P, L0, S, dev, peak)
+    return result
+
+
+def e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks):
+    """The same cycle with every decode step's q/k_new/v_new copied in from pinned
+    host memory and its outputs copied back, all inside one captured graph."""
+    import torch
+    h_q = [io.q.cpu().pin_memory() for io in ios]
+    h_k = [io.k_new.cpu().pin_memory() for io in ios]
+    h_v = [io.v_new.cpu().pin_memory() for io in ios]
+    h_out = [torch.empty(ios[0].out.shape, dtype=torch.float32, pin_memory=True) for _ in range(cyc)]
+
+    def step_io(t):
+        io = ios[t]
+        io.q.copy_(h_q[t], non_blocking=True)
+        io.k_new.copy_(h_k[t], non_blocking=True)
+        io.v_new.copy_(h_v[t], non_blocking=True)
+
+    def cycle():
+        step_io(0)
+        dec.slow_step(ios[0], seq_steps[0])
+        h_out[0].copy_(ios[0].out, non_blocking=True)
+        for t in range(1, cyc):
+            step_io(t)
+            dec.fast_step(ios[t], seq_steps[t])
+            h_out[t].copy_(ios[t].out, non_blocking=True)
+        dec.join()
+
+    with torch.cuda.stream(dec.main):
+        cycle()
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=dec.main):
+        cycle()
+    with torch.cuda.stream(dec.main):
+        for _ in range(max(1, args.warmup)):
+            g.replay()
+    torch.cuda.synchronize()
+    n = max(3, args.steps // 2)
+    ranks.barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with torch.cuda.stream(dec.main):
+        e0.record(dec.main)
+        for _ in range(n):
+            g.replay()
+        e1.record(dec.main)
+    torch.cuda.synchronize()
+    ranks.barrier()
+    ms = ranks.max(e0.elapsed_time(e1) / n)
+    h2d = sum(x.numel() * x.element_size() for x in h_q + h_k + h_v)
+    d2h = sum(x.numel() * x.element_size() for x in h_out)
+    return {"value": round(ms * 1e3 / cyc, 3), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "steps": n, "path": "SFIDecoder (libsfi C ABI) with pinned host inputs/outputs, one graph per cycle"}
+
+
+def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps, NL, B, Hq, Hkv, D, P, L0, S,
+                    dev, peak):
+    """Fast decode steps (all layers) at Table 1's retention points vs the dense decode kernel."""
+    import torch
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    reps = 20
+    L1 = L0 + 1
+    seq = seq_steps[1]
+
+    def time_graph(fn):
+        with torch.cuda.stream(dec.main):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=dec.main):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(dec.main):
+            for _ in range(3):
+                g.replay()
+            e0.record(dec.main)
+            for _ in range(reps):
+                g.replay()
+            e1.record(dec.main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    ws_dense = dec.ws_dense
+
+    def dense_step():
+        for i, Lb in enumerate(layers):
+            kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
+            sfi.sfi_paged_kv_append(shape, kv, kn_all[1, i], vn_all[1, i], stream=dec.main)
+            sfi.sfi_slow_dense_attn_with_scores(shape, kv, S, 0, q_all[1, i], out[i], None, None,
+                                                max_tokens=L1 + P, workspace=ws_dense, stream=dec.main)
+
+    us_dense = time_graph(dense_step)
+    by_dense = dense_bytes(B, Hq, Hkv, D, P, L1, scores=False) + append_bytes(B, Hkv, D)
+    rows = []
+    for n in SWEEP_N:
+        W = 192 if n == 1 else 256
+        k = max(0, n * 256 - S - W) if n < 64 else L0 - S - W
+        kreq = torch.full((B,), k, dtype=torch.int32, device=dev)
+        # slow step at L0 fills the compact buffers for this retention
+        for i, Lb in enumerate(layers):
+            kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq_steps[0])
+            sfi.sfi_slow_dense_attn_with_scores(shape, kv, S, W, q_all[0, i], out[i], None, Lb.scores,
+                                                max_tokens=L0 + P, workspace=ws_dense, stream=dec.main)
+            sfi.sfi_select_topk(Lb.scores, Hkv, seq_steps[0], S, W, kreq, Lb.idx, Lb.compact.count, stream=dec.main)
+            sfi.sfi_compact_gather(shape, kv, Lb.idx, Lb.compact.count, S, Lb.compact, stream=dec.main)
+        max_tok = S + k + W + 2 * P
+        ws_fast = sfi.alloc_workspace(shape, B, max_tok, device=dev)
+
+        def fast_step():
+            for i, Lb in enumerate(layers):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
+                sfi.sfi_paged_kv_append(shape, kv, kn_all[1, i], vn_all[1, i], stream=dec.main)
+                sfi.sfi_fast_decode_attn(shape, kv, Lb.compact, S, W, q_all[1, i], out[i], None, max_tokens=max_tok,
+                                         workspace=ws_fast, stream=dec.main)
+
+        us = time_graph(fast_step)
+        n_ret = S + k + W
+        by = NL * (fast_bytes(B, Hq, Hkv, D, P, n_ret, W) + append_bytes(B, Hkv, D))
+        rows.append({"retention_pct": round(100 * n_ret / L1, 2), "n_over_64": n, "sink": S, "k": k, "recent": W,
+                     "us_per_step": round(us, 2), "GBps": round(by / (us * 1e-6) / 1e9, 1),
+                     "frac_of_peak": round(by / (us * 1e-6) / 1e9 / peak, 3),
+                     "speedup_vs_dense": round(us_dense / us, 3), "table1_speedup_context": TABLE1[n]})
+    # restore the main cycle's selection state
+    dec.pending = [False] * len(layers)
+    return {"dense_us_per_step": round(us_dense, 2),
+            "dense_GBps": round(NL * by_dense / (us_dense * 1e-6) / 1e9, 1),
+            "dense_frac_of_peak": round(NL * by_dense / (us_dense * 1e-6) / 1e9 / peak, 3),
+            "points": rows, "note": "fast and dense steps include the paged append; 28 layers per step; "
+                                    "Table 1 speedups are the paper's (hardware unstated), context only"}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (reference arm and cpu_baseline)
+# ---------------------------------------------------------------------------
+_SAMPLE = {}
+
+
+def oracle_sample_us_per_step(min_seconds: float, layers: int, batch: int, kv_len: int):
+    """Time the CPU oracle on a bounded sample of the workload and scale it.
+
+    Sample: one request, one layer, 2 of the 8 KV heads (4 of the 16 query heads; the
+    heads are independent and cost the same), one refresh cycle's work: a slow step
+    (dense attention + masked scores + Selector + compaction) and a fast step. Scaled
+    by 4 for the heads, by batch x layers, and to a decode step as
+    (slow + (cycle - 1) * fast) / cycle."""
+    import numpy as np
+    import oracle
+    import sfi_synth as syn
+
+    Hq_all, Hkv_all = WL["num_q_heads"], WL["num_kv_heads"]
+    Hq, Hkv, D, P = 4, 2, WL["head_dim"], WL["page_size"]
+    S, W, cyc = WL["sink"], WL["recent"], WL["refresh_interval"]
+    L0 = kv_len
+    k = syn.retention_budget(WL["retention"], L0, S, W)
+    key = (L0,)
+    if key not in _SAMPLE:
+        oracle.build()
+        g = syn.rng(7000, 1)
+        _SAMPLE[key] = (syn.make_paged_kv(g, [L0], Hkv, D, P), syn.normal_bf16(g, (Hq, D)))
+    kvh, q = _SAMPLE[key]
+    pr = kvh.page_table[0]
+    t_slow, t_fast, n = 0.0, 0.0, 0
+    t_begin = time.perf_counter()
+    while True:
+        t0 = time.perf_counter()
+        oracle.dense_attn(q, kvh.k_pool, kvh.v_pool, pr, L0, Hq, Hkv, D, P)
+        sc = oracle.group_scores(q, kvh.k_pool, pr, L0, S, W, Hq, Hkv, D, P)
+        idx = np.stack([oracle.select_topk(sc[h], L0, S, W, k) for h in range(Hkv)])
+        ck, cv = oracle.compact(kvh.k_pool, kvh.v_pool, pr, L0, S, idx, k, Hkv, D, P, S + k)
+        t1 = time.perf_counter()
+        oracle.fast_attn(q, ck, cv, k, kvh.k_pool, kvh.v_pool, pr, L0, S, W, Hq, Hkv, D, P)
+        t2 = time.perf_counter()
+        t_slow += t1 - t0
+        t_fast += t2 - t1
+        n += 1
+        if time.perf_counter() - t_begin >= min_seconds:
+            break
+    head_scale = Hkv_all / Hkv
+    per_req_layer_cycle = (t_slow + (cyc - 1) * t_fast) / n * head_scale
+    us_step = per_req_layer_cycle / cyc * batch * layers * 1e6
+    sample = (f"{n} x (one slow step: dense + scores + Selector + compaction, and one fast step) of one request, "
+              f"one layer, {Hkv} of {Hkv_all} KV heads ({Hq} of {Hq_all} query heads), L={L0}; scaled x{head_scale:g} "
+              f"heads x{batch} requests x{layers} layers, (slow + {cyc - 1} fast)/{cyc} per decode step")
+    return us_step, sample, time.perf_counter() - t_begin
+
+
+def run_reference(args, ranks: Ranks):
+    if ranks.rank != 0:
+        return None
+    times = []
+    sample = ""
+    for _ in range(args.warmup):
+        oracle_sample_us_per_step(0.0, args.layers, args.batch, args.kv_len)
+    t_all = time.perf_counter()
+    for _ in range(args.steps):
+        us, sample, _ = oracle_sample_us_per_step(0.0, args.layers, args.batch, args.kv_len)
+        times.append(us)
+    wall = time.perf_counter() - t_all
+    us = statistics.mean(times)
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": ranks.world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * WL["refresh_interval"] / 1e3, 3),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {**WL, "layers": args.layers, "batch": args.batch, "kv_len": args.kv_len,
+                   "parallelism": "rank 0 only"},
+        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": sample + f"; one sample per step, {wall:.1f} s wall for {args.steps} steps"},
+        "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    args = parse_args()
+    ranks = Ranks()
+    try:
+        if args.impl == "reference":
+            res = run_reference(args, ranks)
+        else:
+            res = run_gpu(args, ranks)
+            if res is not None and ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
+                us, sample, secs = oracle_sample_us_per_step(12.0, args.layers, args.batch, args.kv_len)
+                res["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+                                       "sample": sample + f"; {secs:.1f} s of CPU time"}
+        if res is not None and ranks.rank == 0:
+            print(json.dumps(res), flush=True)
+    finally:
+        ranks.close()
+
+
+if __name__ == "__main__":
+    main()

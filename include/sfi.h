@@ -1,0 +1,238 @@
+/*
+ * sfi.h - C ABI of libsfi: Slow-Fast Inference (SFI) decode attention over a
+ * sparse, recallable KV memory, for NVIDIA GB300 (sm_103a).
+ *
+ * Method: "Slow-Fast Inference: Training-Free Inference Acceleration via
+ * Within-Sentence Support Stability" (Xie et al., 2026).
+ *   Figure 2 caption: fast steps attend to a managed sparse state
+ *     (sink + selected + recent); a slow step performs dense attention, collects
+ *     masked attention logits over the allowed candidate set and invokes the
+ *     Selector to refresh the selected memory for the next segment.
+ *   Figure 3 caption: (A) the Selector and cache reorganisation of layer i run on
+ *     an aux stream while the main stream computes layer i+1's attention;
+ *     (B) sink and selected tokens are packed into a contiguous compact buffer and
+ *     recent tokens are read in place from paged KV.
+ *   Table 1: kernel-level sparse/dense speedup at KV length 16K, batch 16, bf16.
+ * The same per-KV-head logit statistics are what "A Sparse Glimpse of the Whole:
+ * Train-Free Self-Speculative Decoding" (SparseSpec-L, abstract) recycles as its
+ * importance signal.
+ *
+ * Notation: B requests, Hq query heads, Hkv KV heads, G = Hq / Hkv, D head_dim,
+ * P page size, L the current length of a request (the current token included),
+ * S sink size, W recent-window size, k selected tokens per KV head.
+ * Query head h reads KV head h / G. Softmax scale defaults to 1/sqrt(D).
+ *
+ * Sparse state of a request at length L (the fast step attends to exactly this):
+ *   sink     positions [0, min(S, L))              compact rows [0, min(S, L))
+ *   selected positions idx[0 .. count)             compact rows [S, S + count)
+ *   recent   positions [max(S, L - W), L)          read in place from the pages
+ * Candidates of a slow step at length L: C = [S, L - W) (empty when L <= S + W).
+ *
+ * Conventions for every entry point:
+ *   - The caller owns every buffer. The library allocates nothing, frees nothing,
+ *     never synchronises and never changes the current device. Device pointers
+ *     must belong to the current device.
+ *   - Work is enqueued on `stream` (a cudaStream_t; NULL = legacy default stream)
+ *     and runs asynchronously.
+ *   - Host-side errors (a NULL pointer, an unsupported shape, a short workspace)
+ *     are returned before anything is launched. A failed launch returns
+ *     SFI_ERR_CUDA.
+ *   - Device-side errors never trap: the kernel ORs an SFI_DEV_* bit into
+ *     *dev_status (optional; may be NULL) and skips the offending unit's writes.
+ *   - Per-request arrays (q, out, lse, scores, seq_lens, page_table rows,
+ *     k_per_req, counts, compact rows) are indexed by the request id r. An entry
+ *     point processes `batch` requests: r = req_ids[b] when req_ids is non-NULL
+ *     (a subset of a larger batch, e.g. the slow subset of a mixed step), else
+ *     r = b. req_ids must not repeat an id within one call.
+ *   - Supported: head_dim 64 or 128, page_size 16, G in {1, 2, 4, 8}. Q/K/V are
+ *     bf16; outputs, LSE and scores are fp32; positions are int32.
+ *   - LSE is the natural log of sum_j exp(scale * q . k_j) over the attended
+ *     positions.
+ */
+#ifndef SFI_H
+#define SFI_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SFI_VERSION 1
+
+#if defined(__GNUC__)
+#define SFI_API __attribute__((visibility("default")))
+#else
+#define SFI_API
+#endif
+
+typedef enum {
+    SFI_OK = 0,
+    SFI_ERR_INVALID_ARG = 1, /* NULL pointer, negative size, inconsistent shape */
+    SFI_ERR_UNSUPPORTED = 2, /* head_dim, page_size or group size not supported */
+    SFI_ERR_WORKSPACE = 3,   /* workspace missing or smaller than sfi_workspace_size() */
+    SFI_ERR_CUDA = 4         /* a CUDA call or launch failed */
+} sfi_status;
+
+/* Bits ORed into *dev_status by the kernels (0 = no error). */
+#define SFI_DEV_BAD_PAGE 1u     /* a page-table entry outside [0, num_pages) */
+#define SFI_DEV_BAD_LEN 2u      /* seq_len < 1 or beyond the page table */
+#define SFI_DEV_K_OVERFLOW 4u   /* k_r < 0, k_r > k_cap, or sink + count > capacity */
+#define SFI_DEV_BAD_INDEX 8u    /* a selected position outside [0, L) */
+#define SFI_DEV_TIMEOUT 16u     /* an in-kernel pipeline wait ran past its bound */
+#define SFI_DEV_BAD_COMPACT 32u /* compact rows of a request fall outside the buffer */
+
+/* Attention geometry shared by all calls. */
+typedef struct {
+    int32_t num_q_heads;  /* Hq */
+    int32_t num_kv_heads; /* Hkv */
+    int32_t head_dim;     /* D: 64 or 128 */
+    int32_t page_size;    /* P: 16 */
+    float softmax_scale;  /* <= 0 selects 1/sqrt(D) */
+} sfi_attn_shape;
+
+/* Paged bf16 KV cache (Figure 3: the dense KV is kept in pages and never discarded). */
+typedef struct {
+    void *k_pool;               /* bf16 [num_pages][Hkv][P][D], 16-byte aligned */
+    void *v_pool;               /* bf16 [num_pages][Hkv][P][D], 16-byte aligned */
+    int32_t num_pages;          /* pages in each pool */
+    int32_t max_pages_per_req;  /* row stride of page_table */
+    const int32_t *page_table;  /* int32 [B][max_pages_per_req]: page of positions [16p, 16p+16) */
+    const int32_t *seq_lens;    /* int32 [B]: L of each request, current token included */
+} sfi_paged_kv;
+
+/* Compact buffer (Figure 3B: sink + selected packed contiguously), one per layer.
+ * Row i of KV head h of request r is buffer row  row_offset[r] + h * capacity[r] + i,
+ * each row D bf16 values. Rows [0, min(S, L)) hold the sink, rows [S, S + count[r])
+ * the selection in ascending position order. */
+typedef struct {
+    void *k;                   /* bf16 [total_rows][D], 16-byte aligned */
+    void *v;                   /* bf16 [total_rows][D], 16-byte aligned */
+    int64_t total_rows;        /* rows in each of k and v */
+    const int64_t *row_offset; /* int64 [B] */
+    const int32_t *capacity;   /* int32 [B] rows per KV head, >= S + k_r */
+    const int32_t *count;      /* int32 [B] selected rows per KV head (written by sfi_select_topk) */
+} sfi_compact_kv;
+
+/*
+ * sfi_paged_kv_append - write the current token's K and V into the paged cache.
+ * Figure 3 caption (paged KV). For each request r, position L_r - 1 (L_r =
+ * seq_lens[r], which already counts the new token) receives k_new[r] and v_new[r]:
+ * slot (L_r - 1) % P of page page_table[r][(L_r - 1) / P].
+ *   k_new, v_new : bf16 [B][Hkv][D], indexed by request id like q
+ * Device errors: SFI_DEV_BAD_LEN, SFI_DEV_BAD_PAGE (that request is skipped).
+ */
+SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
+                               const void *v_new, const int32_t *req_ids, int32_t batch, int32_t *dev_status,
+                               void *stream);
+
+/*
+ * sfi_fast_decode_attn - the fast step (Figure 2: attention over sink + selected +
+ * recent; Figure 3B: the compact segment is streamed contiguously, the recent
+ * segment is gathered page by page in place).
+ * Each query head h of request r attends, with one softmax, to compact rows
+ * [0, min(S, L) + count[r]) of KV head h / G followed by paged positions
+ * [max(S, L - W), L). The compact buffer must have been filled by
+ * sfi_compact_gather at a length >= min(S, L) (the sink is complete).
+ *   q       : bf16 [B][Hq][D]
+ *   out     : fp32 [B][Hq][D]
+ *   lse     : fp32 [B][Hq] or NULL
+ *   max_tokens : an upper bound on S + max count + W + P over the batch, used to
+ *                plan split-KV; 0 lets the library assume the compact capacity
+ *                is small. It affects speed only, never results.
+ *   num_splits : 0 = automatic; otherwise the number of KV splits per
+ *                (request, KV head) (clamped to the plan's maximum).
+ *   workspace  : at least sfi_workspace_size(shape, batch, max_tokens, num_splits)
+ *                bytes of device memory, zero-filled before its first use. The
+ *                kernels leave it zero-filled again when they finish without a
+ *                device error; after SFI_DEV_TIMEOUT zero it again. Launches
+ *                that share one workspace must not overlap in time.
+ * Device errors: SFI_DEV_BAD_LEN, SFI_DEV_BAD_PAGE, SFI_DEV_K_OVERFLOW,
+ * SFI_DEV_BAD_COMPACT, SFI_DEV_TIMEOUT.
+ */
+SFI_API sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
+                                int32_t sink, int32_t recent, const void *q, float *out, float *lse,
+                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * sfi_slow_dense_attn_with_scores - the slow step (Figure 2 caption: dense
+ * attention plus the masked attention logits over the candidate set).
+ * Each query head attends to all positions [0, L) of its KV head through the page
+ * table. When scores is non-NULL it also writes, for every KV head kv,
+ *   scores[r][kv][j] = sum_{g < G} scale * q_{kv*G+g} . k_{kv,j}   for j in [S, L - W)
+ *   scores[r][kv][j] = -inf                                        for other j < L
+ * in fp32; entries j >= L are not written. With scores == NULL this is the dense
+ * full-KV decode attention (the denominator of Table 1).
+ *   scores       : fp32 [B][Hkv][score_stride], score_stride >= max L, or NULL
+ *   max_tokens   : an upper bound on L + P over the batch (split planning only)
+ *   num_splits, workspace, workspace_bytes : as for sfi_fast_decode_attn
+ * Device errors: SFI_DEV_BAD_LEN (also when L > score_stride: the scores of that
+ * request are then not written), SFI_DEV_BAD_PAGE, SFI_DEV_TIMEOUT.
+ */
+SFI_API sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
+                                           int32_t recent, const void *q, float *out, float *lse, float *scores,
+                                           int64_t score_stride, const int32_t *req_ids, int32_t batch,
+                                           int32_t max_tokens, int32_t num_splits, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * sfi_select_topk - the Selector (Figure 2 caption): for every (request r, KV
+ * head kv) keep the k_eff = min(k_per_req[r], |C|) candidates of C = [S, L - W)
+ * with the largest score; equal scores go to the lower position; -0 equals +0;
+ * NaN ranks below every number. The result is written in ascending position
+ * order, and k_eff to count_out[r].
+ *   scores    : fp32 [B][Hkv][score_stride] (as written by the slow step)
+ *   seq_lens  : int32 [B] (L at the slow step)
+ *   k_per_req : int32 [B], 0 <= k_r <= k_cap
+ *   idx_out   : int32 [B][Hkv][k_cap]; entries past k_eff are not written
+ *   count_out : int32 [B]
+ * Device errors: SFI_DEV_K_OVERFLOW, SFI_DEV_BAD_LEN (L > score_stride); that
+ * request's outputs are not written.
+ */
+SFI_API sfi_status sfi_select_topk(const float *scores, int64_t score_stride, int32_t num_kv_heads, const int32_t *seq_lens,
+                           int32_t sink, int32_t recent, const int32_t *k_per_req, int32_t k_cap, int32_t *idx_out,
+                           int32_t *count_out, const int32_t *req_ids, int32_t batch, int32_t *dev_status,
+                           void *stream);
+
+/*
+ * sfi_compact_gather - cache reorganisation (Figure 3: sink and selected tokens
+ * packed into the contiguous compact buffer). For every (request, KV head):
+ *   compact row i          <- paged position i          for i < min(S, L)
+ *   compact row S + t      <- paged position idx[t]     for t < count[r]
+ * for both K and V, copied bit for bit. `count` is the Selector's count_out and
+ * normally the same array as compact->count.
+ *   idx   : int32 [B][Hkv][k_cap] ascending positions (from sfi_select_topk)
+ *   count : int32 [B]
+ * Device errors: SFI_DEV_BAD_LEN, SFI_DEV_BAD_PAGE, SFI_DEV_BAD_INDEX,
+ * SFI_DEV_K_OVERFLOW, SFI_DEV_BAD_COMPACT (offending rows are skipped).
+ */
+SFI_API sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const int32_t *idx,
+                              const int32_t *count, int32_t k_cap, int32_t sink, const sfi_compact_kv *compact,
+                              const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream);
+
+/*
+ * sfi_workspace_size - bytes of workspace the attention entry points need for this
+ * batch, token bound and split request on the current device (split-KV partial
+ * states plus one counter per (request, KV head)). Returns 0 on invalid input.
+ */
+SFI_API size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
+
+/*
+ * sfi_plan_splits - the split count the attention entry points will use for these
+ * arguments on the current device (for reports and tests). 0 on invalid input.
+ */
+SFI_API int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
+
+/* Human-readable name of a status code (static string). */
+SFI_API const char *sfi_status_string(sfi_status status);
+
+/* SFI_VERSION of the built library. */
+SFI_API int32_t sfi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SFI_H */

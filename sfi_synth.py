@@ -228,3 +228,34 @@ def device_normal_bf16_(t, seed: int):
         e = min(flat.numel(), s + chunk)
         flat[s:e].copy_(torch.randn(e - s, generator=gen, device=t.device, dtype=torch.float32))
     return t
+
+
+def device_plant_heavy_hitters_(k_pool, page_table, q, seq_lens, sink: int, recent: int, frac: float, beta: float,
+                                seed: int):
+    """Heavy-hitter keys on the device: for each (request, KV head), a seeded 'frac'
+    share of the candidate positions [sink, L - recent) gets K += beta * u, u the unit
+    vector along the group-summed query q (bf16 [B][Hq][D]). In place on k_pool
+    (bf16 [pages][Hkv][P][D]); page_table int32 [B][max_pages] and seq_lens are
+    device tensors."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv, P = k_pool.shape[1], k_pool.shape[2]
+    G = Hq // Hkv
+    gen = torch.Generator(device=q.device)
+    gen.manual_seed(int(seed))
+    qbar = q.float().view(B, Hkv, G, D).sum(2)
+    u = qbar / qbar.norm(dim=-1, keepdim=True).clamp_min(1e-12)          # [B][Hkv][D]
+    flat = k_pool.view(-1, D)
+    lens = seq_lens.cpu().tolist()
+    for r in range(B):
+        n = lens[r] - sink - recent
+        m = int(round(frac * n))
+        if m <= 0:
+            continue
+        pos = sink + torch.stack([torch.randperm(n, generator=gen, device=q.device)[:m] for _ in range(Hkv)])
+        pages = page_table[r].long()[pos // P]                              # [Hkv][m]
+        kvh = torch.arange(Hkv, device=q.device).view(Hkv, 1)
+        rows = (pages * Hkv + kvh) * P + pos % P
+        vals = flat[rows.view(-1)].float().view(Hkv, m, D) + beta * u[r].view(Hkv, 1, D)
+        flat[rows.view(-1)] = vals.view(-1, D).to(k_pool.dtype)
+    return k_pool

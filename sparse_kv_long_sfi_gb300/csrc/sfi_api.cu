@@ -1,0 +1,333 @@
+// C ABI of libsfi (declared in include/sfi.h): argument validation, TMA descriptor
+// encoding, split-KV planning and kernel dispatch. Stateless apart from per-device
+// caches of the SM count and of kernel attributes; allocates nothing.
+#include <algorithm>
+#include <atomic>
+#include <cmath>
+#include <mutex>
+
+#include "sfi_internal.h"
+
+namespace {
+
+using sfi::AttnMaps;
+using sfi::AttnParams;
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn tensor_map_encoder() {
+    static EncodeTiledFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    });
+    return fn;
+}
+
+// 2-D view [rows][D] of a bf16 buffer, boxes of [16 rows][64 elements] with the
+// 128-byte swizzle (one box row = one 128-byte line).
+bool encode_rows(CUtensorMap *map, void *base, int64_t rows, int head_dim) {
+    EncodeTiledFn enc = tensor_map_encoder();
+    if (!enc) return false;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * 2};
+    cuuint32_t box[2] = {64, (cuuint32_t)sfi::kSubTokens};
+    cuuint32_t estr[2] = {1, 1};
+    return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, base, dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int sm_count_current_device() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) {
+        int v = cache[dev].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+sfi_status check_shape(const sfi_attn_shape *s) {
+    if (!s) return SFI_ERR_INVALID_ARG;
+    if (s->num_q_heads <= 0 || s->num_kv_heads <= 0 || s->num_q_heads % s->num_kv_heads != 0)
+        return SFI_ERR_INVALID_ARG;
+    const int g = s->num_q_heads / s->num_kv_heads;
+    if (g != 1 && g != 2 && g != 4 && g != 8) return SFI_ERR_UNSUPPORTED;
+    if (s->head_dim != 64 && s->head_dim != 128) return SFI_ERR_UNSUPPORTED;
+    if (s->page_size != sfi::kSubTokens) return SFI_ERR_UNSUPPORTED;
+    return SFI_OK;
+}
+
+sfi_status check_paged(const sfi_attn_shape *s, const sfi_paged_kv *kv) {
+    if (!kv || !kv->k_pool || !kv->v_pool || !kv->page_table || !kv->seq_lens) return SFI_ERR_INVALID_ARG;
+    if (kv->num_pages <= 0 || kv->max_pages_per_req <= 0) return SFI_ERR_INVALID_ARG;
+    if (!aligned16(kv->k_pool) || !aligned16(kv->v_pool)) return SFI_ERR_INVALID_ARG;
+    // TMA row coordinates are int32
+    if ((int64_t)kv->num_pages * s->num_kv_heads * s->page_size >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
+    if ((int64_t)kv->max_pages_per_req * s->page_size >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
+    return SFI_OK;
+}
+
+int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_count) {
+    constexpr int kMaxSplits = 256;
+    if (units <= 0) return 1;
+    int by_tokens = kMaxSplits;
+    if (max_tokens > 0) {
+        // at least two full stages of sub-blocks per split
+        const int nb = (max_tokens + sfi::kSubTokens - 1) / sfi::kSubTokens + 1;
+        by_tokens = std::max(1, nb / (2 * sfi::kConsumerWarps));
+    }
+    int s;
+    if (requested > 0) {
+        s = requested;
+    } else if (max_tokens <= 0) {
+        s = 1;
+    } else {
+        // one wave of resident CTAs: every split of every unit is on an SM at once
+        s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm / units);
+    }
+    return std::max(1, std::min({s, by_tokens, kMaxSplits}));
+}
+
+float resolve_scale(const sfi_attn_shape *s) {
+    return s->softmax_scale > 0.f ? s->softmax_scale : 1.0f / std::sqrt((float)s->head_dim);
+}
+
+void fill_common(AttnParams &p, const sfi_attn_shape *s, const sfi_paged_kv *kv, const void *q, float *out,
+                 float *lse, const int32_t *req_ids, int32_t sink, int32_t recent, int32_t *dev_status) {
+    p.q = static_cast<const __nv_bfloat16 *>(q);
+    p.out = out;
+    p.lse = lse;
+    p.scores = nullptr;
+    p.score_stride = 0;
+    p.page_table = kv->page_table;
+    p.max_pages = kv->max_pages_per_req;
+    p.num_pages = kv->num_pages;
+    p.seq_lens = kv->seq_lens;
+    p.c_row_offset = nullptr;
+    p.c_capacity = nullptr;
+    p.c_count = nullptr;
+    p.c_total_rows = 0;
+    p.req_ids = req_ids;
+    p.hq = s->num_q_heads;
+    p.hkv = s->num_kv_heads;
+    p.group = s->num_q_heads / s->num_kv_heads;
+    p.sink = sink;
+    p.recent = recent;
+    p.scale = resolve_scale(s);
+    p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.dev_status = dev_status;
+}
+
+sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, size_t ws_bytes) {
+    p.ws_count = nullptr;
+    p.ws_ml = nullptr;
+    p.ws_part = nullptr;
+    if (p.splits <= 1) return SFI_OK;
+    const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim);
+    if (!ws || ws_bytes < l.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SFI_ERR_WORKSPACE;
+    char *base = static_cast<char *>(ws);
+    p.ws_count = reinterpret_cast<int32_t *>(base + l.count_off);
+    p.ws_ml = reinterpret_cast<float *>(base + l.ml_off);
+    p.ws_part = reinterpret_cast<float *>(base + l.part_off);
+    return SFI_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int32_t sfi_version(void) { return SFI_VERSION; }
+
+const char *sfi_status_string(sfi_status status) {
+    switch (status) {
+        case SFI_OK: return "SFI_OK";
+        case SFI_ERR_INVALID_ARG: return "SFI_ERR_INVALID_ARG";
+        case SFI_ERR_UNSUPPORTED: return "SFI_ERR_UNSUPPORTED";
+        case SFI_ERR_WORKSPACE: return "SFI_ERR_WORKSPACE";
+        case SFI_ERR_CUDA: return "SFI_ERR_CUDA";
+    }
+    return "SFI_ERR_UNKNOWN";
+}
+
+int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits) {
+    if (check_shape(shape) != SFI_OK || batch < 0 || num_splits < 0) return 0;
+    return plan_splits((int64_t)batch * shape->num_kv_heads, max_tokens, num_splits, sm_count_current_device());
+}
+
+size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits) {
+    const int32_t s = sfi_plan_splits(shape, batch, max_tokens, num_splits);
+    if (s <= 1) return 0;
+    return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, s, shape->head_dim).total;
+}
+
+sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
+                               const void *v_new, const int32_t *req_ids, int32_t batch, int32_t *dev_status,
+                               void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    sfi::CopyParams p{};
+    p.k_pool_dst = static_cast<__nv_bfloat16 *>(kv->k_pool);
+    p.v_pool_dst = static_cast<__nv_bfloat16 *>(kv->v_pool);
+    p.num_pages = kv->num_pages;
+    p.max_pages = kv->max_pages_per_req;
+    p.page_table = kv->page_table;
+    p.seq_lens = kv->seq_lens;
+    p.hkv = shape->num_kv_heads;
+    p.head_dim = shape->head_dim;
+    p.req_ids = req_ids;
+    p.dev_status = dev_status;
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    return sfi::launch_paged_append(p, batch, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFI_OK
+                                                                                                : SFI_ERR_CUDA;
+}
+
+sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
+                                int32_t sink, int32_t recent, const void *q, float *out, float *lse,
+                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out) return SFI_ERR_INVALID_ARG;
+    if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity || !compact->count)
+        return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v) || !aligned16(q))
+        return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
+    if (batch == 0) return SFI_OK;
+    AttnParams p{};
+    fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.c_row_offset = compact->row_offset;
+    p.c_capacity = compact->capacity;
+    p.c_count = compact->count;
+    p.c_total_rows = compact->total_rows;
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
+    AttnMaps maps;
+    const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
+    if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.pool_v, kv->v_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.comp_k, compact->k, compact->total_rows, shape->head_dim) ||
+        !encode_rows(&maps.comp_v, compact->v, compact->total_rows, shape->head_dim))
+        return SFI_ERR_CUDA;
+    return sfi::launch_attention(shape->head_dim, sfi::kModeFast, false, maps, p, batch,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
+                                           int32_t recent, const void *q, float *out, float *lse, float *scores,
+                                           int64_t score_stride, const int32_t *req_ids, int32_t batch,
+                                           int32_t max_tokens, int32_t num_splits, void *workspace,
+                                           size_t workspace_bytes, int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned16(q))
+        return SFI_ERR_INVALID_ARG;
+    if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    AttnParams p{};
+    fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.scores = scores;
+    p.score_stride = score_stride;
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
+    AttnMaps maps;
+    const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
+    if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.pool_v, kv->v_pool, pool_rows, shape->head_dim))
+        return SFI_ERR_CUDA;
+    maps.comp_k = maps.pool_k;  // unused in dense mode
+    maps.comp_v = maps.pool_v;
+    return sfi::launch_attention(shape->head_dim, sfi::kModeDense, scores != nullptr, maps, p, batch,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+sfi_status sfi_select_topk(const float *scores, int64_t score_stride, int32_t num_kv_heads, const int32_t *seq_lens,
+                           int32_t sink, int32_t recent, const int32_t *k_per_req, int32_t k_cap, int32_t *idx_out,
+                           int32_t *count_out, const int32_t *req_ids, int32_t batch, int32_t *dev_status,
+                           void *stream) {
+    if (!scores || !seq_lens || !k_per_req || !idx_out || !count_out) return SFI_ERR_INVALID_ARG;
+    if (score_stride <= 0 || num_kv_heads <= 0 || sink < 0 || recent < 0 || k_cap < 0 || batch < 0)
+        return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    sfi::TopkParams p{};
+    p.scores = scores;
+    p.score_stride = score_stride;
+    p.hkv = num_kv_heads;
+    p.seq_lens = seq_lens;
+    p.sink = sink;
+    p.recent = recent;
+    p.k_per_req = k_per_req;
+    p.k_cap = k_cap;
+    p.idx_out = idx_out;
+    p.count_out = count_out;
+    p.req_ids = req_ids;
+    p.dev_status = dev_status;
+    return sfi::launch_select_topk(p, batch, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFI_OK
+                                                                                               : SFI_ERR_CUDA;
+}
+
+sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const int32_t *idx,
+                              const int32_t *count, int32_t k_cap, int32_t sink, const sfi_compact_kv *compact,
+                              const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (!idx || !count || k_cap < 0 || sink < 0 || batch < 0) return SFI_ERR_INVALID_ARG;
+    if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity)
+        return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v)) return SFI_ERR_INVALID_ARG;
+    if (batch == 0 || (int64_t)sink + k_cap == 0) return SFI_OK;
+    if ((int64_t)sink + k_cap >= (int64_t(1) << 31)) return SFI_ERR_INVALID_ARG;
+    sfi::CopyParams p{};
+    p.k_pool_src = static_cast<const __nv_bfloat16 *>(kv->k_pool);
+    p.v_pool_src = static_cast<const __nv_bfloat16 *>(kv->v_pool);
+    p.num_pages = kv->num_pages;
+    p.max_pages = kv->max_pages_per_req;
+    p.page_table = kv->page_table;
+    p.seq_lens = kv->seq_lens;
+    p.hkv = shape->num_kv_heads;
+    p.head_dim = shape->head_dim;
+    p.req_ids = req_ids;
+    p.dev_status = dev_status;
+    p.idx = idx;
+    p.count = count;
+    p.k_cap = k_cap;
+    p.sink = sink;
+    p.ck = static_cast<__nv_bfloat16 *>(compact->k);
+    p.cv = static_cast<__nv_bfloat16 *>(compact->v);
+    p.c_total_rows = compact->total_rows;
+    p.c_row_offset = compact->row_offset;
+    p.c_capacity = compact->capacity;
+    return sfi::launch_compact_gather(p, batch, sink + k_cap, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+}  // extern "C"

@@ -1,0 +1,107 @@
+// Internal interface between the C ABI layer (sfi_api.cu) and the kernel files.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/sfi.h"
+
+namespace sfi {
+
+// Tokens per sub-block: one page of the paged pool, one unit of TMA work, one
+// mma.sync n-extent pair for a consumer warp.
+constexpr int kSubTokens = 16;
+// Consumer warps per attention CTA (each owns one sub-block of every stage).
+constexpr int kConsumerWarps = 4;
+// Rows of the query tile handled per (request, KV head): G <= 8 query heads share a KV head.
+constexpr int kMaxGroup = 8;
+// Attention CTAs resident per SM (shared memory sized for this).
+constexpr int kAttnCtasPerSm = 2;
+
+enum AttnMode : int { kModeFast = 0, kModeDense = 1 };
+
+struct AttnParams {
+    const __nv_bfloat16 *q;  // [B][Hq][D]
+    float *out;              // [B][Hq][D]
+    float *lse;              // [B][Hq] or null
+    float *scores;           // [B][Hkv][score_stride] or null
+    int64_t score_stride;
+    const int32_t *page_table;
+    int32_t max_pages;
+    int32_t num_pages;
+    const int32_t *seq_lens;
+    const int64_t *c_row_offset;
+    const int32_t *c_capacity;
+    const int32_t *c_count;
+    int64_t c_total_rows;
+    const int32_t *req_ids;
+    int32_t hq, hkv, group;
+    int32_t sink, recent;
+    float scale;       // softmax scale
+    float scale_log2;  // scale * log2(e)
+    int32_t splits;
+    int32_t *ws_count;  // [units]
+    float *ws_ml;       // [units][splits][8][2]
+    float *ws_part;     // [units][splits][8][D]
+    int32_t *dev_status;
+};
+
+struct AttnMaps {
+    CUtensorMap pool_k, pool_v;  // rows = (page * Hkv + kv) * P + slot
+    CUtensorMap comp_k, comp_v;  // rows = compact buffer rows (dummy copies of pool maps in dense mode)
+};
+
+// Workspace layout for `units` (request, KV head) pairs and `splits` splits.
+struct WorkspaceLayout {
+    size_t count_off, ml_off, part_off, total;
+};
+WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim);
+
+cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
+                             int batch, cudaStream_t stream);
+
+struct TopkParams {
+    const float *scores;
+    int64_t score_stride;
+    int32_t hkv;
+    const int32_t *seq_lens;
+    int32_t sink, recent;
+    const int32_t *k_per_req;
+    int32_t k_cap;
+    int32_t *idx_out;
+    int32_t *count_out;
+    const int32_t *req_ids;
+    int32_t *dev_status;
+};
+cudaError_t launch_select_topk(const TopkParams &p, int batch, cudaStream_t stream);
+
+struct CopyParams {
+    const __nv_bfloat16 *k_pool_src;
+    const __nv_bfloat16 *v_pool_src;
+    __nv_bfloat16 *k_pool_dst;
+    __nv_bfloat16 *v_pool_dst;
+    int32_t num_pages, max_pages;
+    const int32_t *page_table;
+    const int32_t *seq_lens;
+    int32_t hkv, head_dim;
+    const int32_t *req_ids;
+    int32_t *dev_status;
+    // append
+    const __nv_bfloat16 *k_new;
+    const __nv_bfloat16 *v_new;
+    // compaction
+    const int32_t *idx;
+    const int32_t *count;
+    int32_t k_cap, sink;
+    __nv_bfloat16 *ck;
+    __nv_bfloat16 *cv;
+    int64_t c_total_rows;
+    const int64_t *c_row_offset;
+    const int32_t *c_capacity;
+};
+cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t stream);
+cudaError_t launch_compact_gather(const CopyParams &p, int batch, int max_rows, cudaStream_t stream);
+
+}  // namespace sfi

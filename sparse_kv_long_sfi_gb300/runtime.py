@@ -1,0 +1,239 @@
+"""Host runtime of the SFI decode path: per-layer buffers, the slow/fast schedule and
+the two-stream pipeline.
+
+Slow-Fast Inference (Xie et al., 2026):
+  * Figure 2 caption: a slow step is triggered by a boundary token or when a fixed
+    refresh interval is reached; otherwise the step is fast.
+  * Figure 3 caption (A): while the main stream computes attention for layer i+1,
+    an aux stream runs the Selector and the cache reorganisation of layer i.
+Every device operation of a step is one of libsfi's kernels; this module only
+orders them on streams with events and keeps the per-request counters.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional
+
+import numpy as np
+import torch
+
+from .api import (AttnShape, CompactKV, PagedKV, alloc_workspace, sfi_compact_gather, sfi_fast_decode_attn,
+                  sfi_paged_kv_append, sfi_select_topk, sfi_slow_dense_attn_with_scores)
+
+
+class SlowFastSchedule:
+    """Per-request slow/fast decisions (host counters).
+
+    Step t of request b is slow if it is the request's first step, if a boundary event
+    fired, or if `interval` steps have passed since its last slow step.
+    """
+
+    def __init__(self, batch: int, interval: int):
+        self.interval = int(interval)
+        self.last_slow = np.full(batch, -1, np.int64)
+        self.t = 0
+
+    def next(self, boundary: Optional[np.ndarray] = None) -> np.ndarray:
+        b = np.zeros_like(self.last_slow, dtype=bool) if boundary is None else np.asarray(boundary, bool)
+        slow = (self.last_slow < 0) | b | (self.t - self.last_slow >= self.interval)
+        self.last_slow[slow] = self.t
+        self.t += 1
+        return slow.astype(np.uint8)
+
+
+@dataclass
+class LayerBuffers:
+    """Device state of one attention layer."""
+    k_pool: torch.Tensor      # bf16 [num_pages][Hkv][P][D]
+    v_pool: torch.Tensor
+    compact: CompactKV        # sink + selected rows
+    scores: torch.Tensor      # fp32 [B][Hkv][score_stride]
+    idx: torch.Tensor         # int32 [B][Hkv][k_cap]
+
+
+@dataclass
+class DecodeBatch:
+    """Requests shared by all layers: page table, capacities, per-request k."""
+    page_table: torch.Tensor  # int32 [B][max_pages]
+    row_offset: torch.Tensor  # int64 [B]
+    capacity: torch.Tensor    # int32 [B]
+    k_per_req: torch.Tensor   # int32 [B]
+    k_cap: int
+    score_stride: int
+
+
+def allocate_layers(shape: AttnShape, num_layers: int, num_pages: int, batch: DecodeBatch, sink: int,
+                    device="cuda", pool_init=None) -> List[LayerBuffers]:
+    """Allocate per-layer pools, compact buffers, score and index arrays.
+
+    pool_init(layer, k_pool, v_pool) fills the pools (e.g. seeded synthetic KV).
+    """
+    B = batch.page_table.shape[0]
+    total_rows = int((batch.row_offset[-1] + shape.num_kv_heads * batch.capacity[-1]).item()) if B else 1
+    layers = []
+    for i in range(num_layers):
+        kp = torch.empty((num_pages, shape.num_kv_heads, shape.page_size, shape.head_dim), dtype=torch.bfloat16,
+                         device=device)
+        vp = torch.empty_like(kp)
+        if pool_init is not None:
+            pool_init(i, kp, vp)
+        ck = torch.zeros((max(total_rows, 1), shape.head_dim), dtype=torch.bfloat16, device=device)
+        cv = torch.zeros_like(ck)
+        comp = CompactKV(ck, cv, batch.row_offset, batch.capacity,
+                         torch.zeros(B, dtype=torch.int32, device=device))
+        scores = torch.empty((B, shape.num_kv_heads, batch.score_stride), dtype=torch.float32, device=device)
+        idx = torch.zeros((B, shape.num_kv_heads, max(batch.k_cap, 1)), dtype=torch.int32, device=device)
+        layers.append(LayerBuffers(kp, vp, comp, scores, idx))
+    return layers
+
+
+def compact_layout(shape: AttnShape, sink: int, k_per_req, device="cuda"):
+    """Row offsets and capacities of a packed compact buffer (capacity = sink + k_r per KV head)."""
+    k = np.asarray(k_per_req, np.int64)
+    cap = sink + k
+    off = np.concatenate([[0], np.cumsum(cap * shape.num_kv_heads)[:-1]]).astype(np.int64)
+    return (torch.tensor(off, dtype=torch.int64, device=device), torch.tensor(cap, dtype=torch.int32, device=device))
+
+
+@dataclass
+class StepIO:
+    """Per-step inputs/outputs of all layers (leading dim = layer)."""
+    q: torch.Tensor           # bf16 [NL][B][Hq][D]
+    k_new: torch.Tensor       # bf16 [NL][B][Hkv][D]
+    v_new: torch.Tensor
+    out: torch.Tensor         # fp32 [NL][B][Hq][D]
+    lse: Optional[torch.Tensor] = None  # fp32 [NL][B][Hq]
+
+
+class SFIDecoder:
+    """Runs decode steps over all layers with a main and an aux stream.
+
+    Slow step, per layer i (main stream): append, dense attention + masked scores,
+    record e_i. Aux stream: wait e_i, Selector, compaction, record a_i. The main
+    stream moves on to layer i + 1 at once (Figure 3A); the next use of layer i's
+    compact buffer (a later step) waits a_i.
+    """
+
+    def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
+                 max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
+                 main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None):
+        self.shape, self.layers, self.batch = shape, layers, batch
+        self.sink, self.recent = int(sink), int(recent)
+        self.max_len = int(max_len)
+        B = batch.page_table.shape[0]
+        self.max_fast_tokens = self.sink + int(batch.k_cap) + self.recent + 2 * shape.page_size
+        self.max_dense_tokens = self.max_len + shape.page_size
+        self.ws_fast = alloc_workspace(shape, B, self.max_fast_tokens, device=device)
+        self.ws_dense = alloc_workspace(shape, B, self.max_dense_tokens, device=device)
+        self.dev_status = dev_status if dev_status is not None else torch.zeros(1, dtype=torch.int32, device=device)
+        lo, hi = torch.cuda.Stream.priority_range()
+        self.main = main_stream or torch.cuda.Stream(device=device, priority=hi)
+        self.aux = aux_stream or torch.cuda.Stream(device=device, priority=lo)
+        self.e_attn = [torch.cuda.Event() for _ in layers]
+        self.e_aux = [torch.cuda.Event() for _ in layers]
+        self.pending = [False] * len(layers)
+        # Optional instrumentation: called as timer(kind, "start"|"end", stream) around
+        # each attention launch (kind "slow", "fast" or "dense"), e.g. to record events.
+        self.timer = None
+
+    def _mark(self, kind: str, phase: str):
+        if self.timer is not None:
+            self.timer(kind, phase, self.main)
+
+    def kv(self, i: int, seq_lens: torch.Tensor) -> PagedKV:
+        L = self.layers[i]
+        return PagedKV(L.k_pool, L.v_pool, self.batch.page_table, seq_lens)
+
+    def _wait_aux(self, i: int):
+        if self.pending[i]:
+            self.main.wait_event(self.e_aux[i])
+            self.pending[i] = False
+
+    def slow_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
+                  append: bool = True):
+        n = None if req_ids is None else req_ids.numel()
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            self._wait_aux(i)
+            if append:
+                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], req_ids=req_ids, batch=n,
+                                    dev_status=self.dev_status, stream=self.main)
+            self._mark("slow", "start")
+            sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
+                                            None if io.lse is None else io.lse[i], L.scores, req_ids=req_ids,
+                                            batch=n, max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
+                                            dev_status=self.dev_status, stream=self.main)
+            self._mark("slow", "end")
+            self.e_attn[i].record(self.main)
+            self.aux.wait_event(self.e_attn[i])
+            sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,
+                            self.batch.k_per_req, L.idx, L.compact.count, req_ids=req_ids, batch=n,
+                            dev_status=self.dev_status, stream=self.aux)
+            sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact, req_ids=req_ids,
+                               batch=n, dev_status=self.dev_status, stream=self.aux)
+            self.e_aux[i].record(self.aux)
+            self.pending[i] = True
+
+    def fast_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
+                  append: bool = True):
+        n = None if req_ids is None else req_ids.numel()
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            self._wait_aux(i)
+            if append:
+                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], req_ids=req_ids, batch=n,
+                                    dev_status=self.dev_status, stream=self.main)
+            self._mark("fast", "start")
+            sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
+                                 None if io.lse is None else io.lse[i], req_ids=req_ids, batch=n,
+                                 max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
+                                 dev_status=self.dev_status, stream=self.main)
+            self._mark("fast", "end")
+
+    def mixed_step(self, io: StepIO, seq_lens: torch.Tensor, slow_ids: torch.Tensor, fast_ids: torch.Tensor):
+        """One step where each request is slow or fast (ASPIRE-style mixed batch, two launches per layer)."""
+        ns, nf = slow_ids.numel(), fast_ids.numel()
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            self._wait_aux(i)
+            sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], dev_status=self.dev_status,
+                                stream=self.main)
+            if nf:
+                sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
+                                     None if io.lse is None else io.lse[i], req_ids=fast_ids, batch=nf,
+                                     max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
+                                     dev_status=self.dev_status, stream=self.main)
+            if ns:
+                sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
+                                                None if io.lse is None else io.lse[i], L.scores, req_ids=slow_ids,
+                                                batch=ns, max_tokens=self.max_dense_tokens,
+                                                workspace=self.ws_dense, dev_status=self.dev_status,
+                                                stream=self.main)
+                self.e_attn[i].record(self.main)
+                self.aux.wait_event(self.e_attn[i])
+                sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,
+                                self.batch.k_per_req, L.idx, L.compact.count, req_ids=slow_ids, batch=ns,
+                                dev_status=self.dev_status, stream=self.aux)
+                sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact,
+                                   req_ids=slow_ids, batch=ns, dev_status=self.dev_status, stream=self.aux)
+                self.e_aux[i].record(self.aux)
+                self.pending[i] = True
+
+    def dense_step(self, io: StepIO, seq_lens: torch.Tensor, append: bool = True):
+        """Full-KV decode step (the baseline of the paper's Table 1)."""
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            if append:
+                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], dev_status=self.dev_status,
+                                    stream=self.main)
+            self._mark("dense", "start")
+            sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
+                                            None if io.lse is None else io.lse[i], None,
+                                            max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
+                                            dev_status=self.dev_status, stream=self.main)
+            self._mark("dense", "end")
+
+    def join(self):
+        """Make the main stream wait for all outstanding aux work."""
+        for i in range(len(self.layers)):
+            self._wait_aux(i)

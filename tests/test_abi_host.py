@@ -1,0 +1,113 @@
+"""The C-ABI library builds, loads and exports every entry point include/sfi.h
+declares; host-side argument validation answers without touching a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "sfi.h")
+
+
+@pytest.fixture(scope="module")
+def libsfi():
+    from sparse_kv_long_sfi_gb300 import _abi, build
+    build.build()
+    return _abi.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return re.findall(r"^SFI_API\s+[\w\s\*]+?\b(sfi_\w+)\s*\(", text, flags=re.M)
+
+
+def test_header_declares_the_five_hot_path_calls():
+    names = declared_functions()
+    for n in ["sfi_paged_kv_append", "sfi_fast_decode_attn", "sfi_slow_dense_attn_with_scores", "sfi_select_topk",
+              "sfi_compact_gather"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libsfi):
+    from sparse_kv_long_sfi_gb300 import _abi
+    names = declared_functions()
+    assert set(names) == set(_abi.PROTOTYPES)
+    for n in names:
+        assert hasattr(libsfi, n), n
+
+
+def test_library_exports_nothing_else(libsfi):
+    import subprocess
+    from sparse_kv_long_sfi_gb300 import build
+    out = subprocess.run(["nm", "-D", "--defined-only", build.LIB], capture_output=True, text=True).stdout
+    exported = {l.split()[-1] for l in out.splitlines() if l.strip()}
+    assert exported == set(declared_functions())
+
+
+def test_version_and_status_strings(libsfi):
+    assert libsfi.sfi_version() == 1
+    assert libsfi.sfi_status_string(0) == b"SFI_OK"
+    assert libsfi.sfi_status_string(3) == b"SFI_ERR_WORKSPACE"
+    assert libsfi.sfi_status_string(99) == b"SFI_ERR_UNKNOWN"
+
+
+def _shape(hq=16, hkv=8, d=128, p=16):
+    from sparse_kv_long_sfi_gb300 import _abi
+    return _abi.sfi_attn_shape(hq, hkv, d, p, 0.0)
+
+
+def _paged(npages=4, maxp=4):
+    from sparse_kv_long_sfi_gb300 import _abi
+    # dummy, 16-byte aligned host addresses: validation never dereferences them
+    return _abi.sfi_paged_kv(4096, 8192, npages, maxp, 12288, 16384)
+
+
+@pytest.mark.parametrize("shape_args,expect", [
+    ((16, 8, 96, 16), 2),    # head_dim 96 unsupported
+    ((16, 8, 128, 32), 2),   # page size 32 unsupported
+    ((48, 4, 128, 16), 2),   # G = 12 unsupported
+    ((16, 5, 128, 16), 1),   # Hq not a multiple of Hkv
+    ((0, 8, 128, 16), 1),
+])
+def test_shape_validation_before_launch(libsfi, shape_args, expect):
+    sh = _shape(*shape_args)
+    kv = _paged()
+    st = libsfi.sfi_slow_dense_attn_with_scores(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, 8192, None, None,
+                                                0, None, 1, 0, 0, None, 0, None, None)
+    assert st == expect
+
+
+def test_null_and_negative_arguments(libsfi):
+    from sparse_kv_long_sfi_gb300 import _abi
+    sh, kv = _shape(), _paged()
+    assert libsfi.sfi_paged_kv_append(None, ctypes.byref(kv), 4096, 4096, None, 1, None, None) == 1
+    assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), None, 4096, 4096, None, 1, None, None) == 1
+    assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(kv), None, 4096, None, 1, None, None) == 1
+    assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(kv), 4097, 4096, None, 1, None, None) == 1
+    comp = _abi.sfi_compact_kv(4096, 4096, 100, 4096, 4096, 4096)
+    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), ctypes.byref(comp), -1, 32, 4096, 4096,
+                                       None, None, 1, 0, 0, None, 0, None, None) == 1
+    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), None, 4, 32, 4096, 4096,
+                                       None, None, 1, 0, 0, None, 0, None, None) == 1
+    assert libsfi.sfi_select_topk(None, 16, 8, 4096, 4, 32, 4096, 8, 4096, 4096, None, 1, None, None) == 1
+    assert libsfi.sfi_select_topk(4096, 0, 8, 4096, 4, 32, 4096, 8, 4096, 4096, None, 1, None, None) == 1
+    assert libsfi.sfi_compact_gather(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, -1, 4, ctypes.byref(comp),
+                                     None, 1, None, None) == 1
+    bad_pages = _abi.sfi_paged_kv(4096, 8192, 0, 4, 12288, 16384)
+    assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(bad_pages), 4096, 4096, None, 1, None,
+                                      None) == 1
+
+
+def test_empty_batch_is_a_no_op(libsfi):
+    sh, kv = _shape(), _paged()
+    assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, None, 0, None, None) == 0
+    assert libsfi.sfi_select_topk(4096, 16, 8, 4096, 4, 32, 4096, 8, 4096, 4096, None, 0, None, None) == 0
+
+
+def test_workspace_size_rejects_bad_shapes(libsfi):
+    sh = _shape(16, 8, 96)
+    assert libsfi.sfi_workspace_size(ctypes.byref(sh), 4, 1024, 0) == 0
+    assert libsfi.sfi_plan_splits(ctypes.byref(sh), 4, 1024, 0) == 0
+    assert libsfi.sfi_plan_splits(ctypes.byref(_shape()), 4, 0, 0) == 1  # no token bound: one split
+    assert libsfi.sfi_plan_splits(ctypes.byref(_shape()), 4, 4096, 3) == 3  # explicit request honoured

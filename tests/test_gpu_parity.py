@@ -1,0 +1,391 @@
+"""GPU parity: every CUDA entry point, called through the C ABI, against the CPU oracle
+on the same seeded inputs. Attention within |gpu - oracle| <= 2e-3 + 1e-2 |oracle|;
+scores within the fp32 dot-product bound; selection, compaction and append bit-exact
+(selection is checked by running the oracle's Selector on the GPU-written fp32
+scores, the same bytes the kernel ranked)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sfi_synth as syn
+from tests.gpu_harness import (Problem, assert_close, dev_bf16, dev_i32, host_bf16, oracle_compact_request,
+                               run_oracle_selection)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a CUDA GPU")
+    from sparse_kv_long_sfi_gb300 import build
+    build.build()
+    oracle.build()
+
+
+def _sfi():
+    import sparse_kv_long_sfi_gb300 as sfi
+    return sfi
+
+
+def _status():
+    return torch.zeros(1, dtype=torch.int32, device="cuda")
+
+
+def counters_zero(ws, units):
+    """The split-merge counters (one int32 per (request, KV head) at the start of the
+    workspace) are back to zero after a launch."""
+    return not ws[:4 * units].any()
+
+
+def _dense(prob, num_splits=0, scores=None, req_ids=None):
+    sfi = _sfi()
+    B = prob.B
+    out = torch.full((B, prob.Hq, prob.D), float("nan"), device="cuda")
+    lse = torch.full((B, prob.Hq), float("nan"), device="cuda")
+    maxL = int(prob.lens.max()) + 16
+    ws = sfi.alloc_workspace(prob.shape, B, maxL, num_splits)
+    st = _status()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, lse, scores,
+                                        req_ids=req_ids, max_tokens=maxL, num_splits=num_splits, workspace=ws,
+                                        dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert counters_zero(ws, B * prob.Hkv), "split counters must be left zeroed"
+    return out.cpu().numpy(), lse.cpu().numpy()
+
+
+# ---------------------------------------------------------------------------
+# Dense / slow-step attention
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 8), (128, 32, 8), (128, 64, 8), (64, 8, 2), (128, 8, 8)])
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_dense_attention_matches_oracle(D, Hq, Hkv, splits):
+    lens = [1, 2, 15, 16, 17, 100, 777, 1500]
+    prob = Problem(seed=D * 1000 + Hq + splits, lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=4, W=32).to_device()
+    out, lse = _dense(prob, num_splits=splits)
+    for r in range(prob.B):
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(out[r], o_ref, f"out r={r}")
+        assert_close(lse[r], l_ref, f"lse r={r}")
+
+
+def test_slow_step_scores_match_oracle_within_fp32_bound():
+    prob = Problem(seed=7, lens=[37, 300, 1024, 1031], Hq=8, Hkv=2, D=64, S=4, W=32, heavy_frac=0.04).to_device()
+    stride = 1040
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    out, lse = _dense(prob, scores=scores)
+    sc = scores.cpu().numpy()
+    for r in range(prob.B):
+        L = prob.lens[r]
+        ref = prob.oracle_scores(r, stride)
+        bound = prob.score_bound(r, stride)
+        assert np.isnan(sc[r, :, L:]).all(), "entries at j >= L must not be written"
+        masked = np.isneginf(ref[:, :L])
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+        err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
+        assert (err <= bound[:, :L][~masked]).all(), err.max()
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(out[r], o_ref, f"out r={r}")
+
+
+# ---------------------------------------------------------------------------
+# Selector
+# ---------------------------------------------------------------------------
+def _select(scores_np, lens, S, W, k_per_req, k_cap, Hkv, req_ids=None):
+    sfi = _sfi()
+    B = len(lens)
+    scores = torch.as_tensor(scores_np).cuda()
+    idx = torch.full((B, Hkv, max(k_cap, 1)), -7, dtype=torch.int32, device="cuda")
+    count = torch.full((B,), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_topk(scores, Hkv, dev_i32(lens), S, W, dev_i32(k_per_req), idx, count,
+                        req_ids=None if req_ids is None else dev_i32(req_ids), dev_status=st)
+    torch.cuda.synchronize()
+    return idx.cpu().numpy(), count.cpu().numpy(), st.item()
+
+
+def _check_selection(scores_np, lens, S, W, k_per_req, k_cap, Hkv):
+    idx, count, st = _select(scores_np, lens, S, W, k_per_req, k_cap, Hkv)
+    assert st == 0
+    for r in range(len(lens)):
+        for kvh in range(Hkv):
+            want = oracle.select_topk(scores_np[r, kvh], lens[r], S, W, k_per_req[r])
+            assert count[r] == len(want)
+            np.testing.assert_array_equal(idx[r, kvh, :len(want)], want, err_msg=f"r={r} kv={kvh}")
+            assert (idx[r, kvh, len(want):] == -7).all(), "entries past k_eff must not be written"
+
+
+def test_selector_planted_zipf_ties():
+    S, W, Hkv = 64, 256, 2
+    lens = [64 + 256 + 5000, 64 + 256 + 9000]
+    ks = [400, 4096]
+    stride = max(lens)
+    sc = np.full((2, Hkv, stride), np.nan, np.float32)
+    for r in range(2):
+        for kvh in range(Hkv):
+            n = lens[r] - S - W
+            sc[r, kvh, :lens[r]] = -np.inf
+            sc[r, kvh, S:S + n] = syn.zipf_scores_with_ties(syn.rng(200, r, kvh), n, ks[r])
+    _check_selection(sc, lens, S, W, ks, 4096, Hkv)
+
+
+SELECTOR_CASES = ["all_equal", "neg_inf_except_k", "nan_and_signed_zero", "k_zero", "k_all", "k_over_n", "short",
+                  "gaussian"]
+
+
+@pytest.mark.parametrize("case", SELECTOR_CASES)
+def test_selector_edge_cases(case):
+    S, W, Hkv = 4, 32, 2
+    g = syn.rng(201, SELECTOR_CASES.index(case))
+    lens = [1000, 1000, 30]
+    k = [50, 50, 5]
+    sc = np.zeros((3, Hkv, 1000), np.float32)
+    if case == "neg_inf_except_k":
+        sc[:] = -np.inf
+        for r in range(3):
+            n = lens[r] - S - W
+            for kvh in range(Hkv):
+                if n > 0:
+                    sc[r, kvh, S + g.choice(n, size=min(3, n), replace=False)] = 1.0
+    elif case == "nan_and_signed_zero":
+        pal = np.array([0.0, -0.0, np.nan, -np.inf, 1.0], np.float32)
+        sc[:] = pal[g.integers(0, 5, size=sc.shape)]
+    elif case == "k_zero":
+        k = [0, 0, 0]
+        sc[:] = g.standard_normal(sc.shape)
+    elif case == "k_all":
+        k = [1000 - S - W, 1000 - S - W, 0]
+        sc[:] = g.standard_normal(sc.shape)
+    elif case == "k_over_n":
+        k = [2000, 964, 100]
+        sc[:] = g.standard_normal(sc.shape)
+    elif case == "short":
+        lens = [3, 36, 37]
+        k = [10, 10, 10]
+        sc[:] = g.standard_normal(sc.shape)
+    elif case == "gaussian":
+        sc[:] = g.standard_normal(sc.shape).astype(np.float32)
+    _check_selection(sc, lens, S, W, k, 2000, Hkv)
+
+
+def test_selector_rejects_k_over_cap():
+    sc = np.zeros((2, 1, 500), np.float32)
+    idx, count, st = _select(sc, [500, 500], 4, 32, [10, 99], 50, 1)
+    assert st & 4  # SFI_DEV_K_OVERFLOW
+    assert count[0] == 10 and count[1] == -7
+
+
+# ---------------------------------------------------------------------------
+# Compaction, append
+# ---------------------------------------------------------------------------
+def _compact_buffers(prob, k_per_req):
+    sfi = _sfi()
+    off, cap = sfi.compact_layout(prob.shape, prob.S, k_per_req)
+    rows = int((off[-1] + prob.Hkv * cap[-1]).item())
+    ck = torch.zeros((rows, prob.D), dtype=torch.bfloat16, device="cuda")
+    cv = torch.zeros_like(ck)
+    count = torch.zeros(prob.B, dtype=torch.int32, device="cuda")
+    return sfi.CompactKV(ck, cv, off, cap, count)
+
+
+def test_slow_step_selection_and_compaction_bit_exact():
+    """Dense + scores -> Selector -> compaction on the GPU; the oracle ranks the GPU's score bytes."""
+    sfi = _sfi()
+    S, W = 4, 32
+    lens = [1024, 777, 36, 3, 40]
+    prob = Problem(seed=11, lens=lens, Hq=8, Hkv=2, D=64, S=S, W=W, heavy_frac=0.04).to_device()
+    k_per_req = [64, 100, 64, 8, 64]
+    k_cap = 128
+    stride = 1024
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    sc = scores.cpu().numpy()
+    comp = _compact_buffers(prob, k_per_req)
+    idx = torch.full((prob.B, prob.Hkv, k_cap), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_topk(scores, prob.Hkv, prob.d_kv.seq_lens, S, W, dev_i32(k_per_req), idx, comp.count,
+                        dev_status=st)
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    ref_idx, ref_count = run_oracle_selection(prob, sc, k_per_req, k_cap)
+    got_idx, got_count = idx.cpu().numpy(), comp.count.cpu().numpy()
+    np.testing.assert_array_equal(got_count, ref_count)
+    ck, cv = host_bf16(comp.k), host_bf16(comp.v)
+    off, cap = comp.row_offset.cpu().numpy(), comp.capacity.cpu().numpy()
+    for r in range(prob.B):
+        keff = ref_count[r]
+        np.testing.assert_array_equal(got_idx[r, :, :keff], ref_idx[r, :, :keff])
+        rk, rv = oracle_compact_request(prob, r, ref_idx[r], keff, cap[r])
+        ns = min(S, lens[r])
+        for kvh in range(prob.Hkv):
+            base = off[r] + kvh * cap[r]
+            for lo, hi in ((0, ns), (S, S + keff)):
+                np.testing.assert_array_equal(ck[base + lo:base + hi], rk[kvh, lo:hi])
+                np.testing.assert_array_equal(cv[base + lo:base + hi], rv[kvh, lo:hi])
+    # planted heavy hitters dominate the selection of the long request
+    assert got_count[0] == 64
+
+
+def test_append_bit_exact_and_only_the_last_slot():
+    sfi = _sfi()
+    prob = Problem(seed=12, lens=[40, 16, 1], Hq=8, Hkv=2, D=128, S=4, W=32, extra_tokens=20).to_device()
+    g = syn.rng(300, 1)
+    kn, vn = syn.normal_bf16(g, (3, 2, 128)), syn.normal_bf16(g, (3, 2, 128))
+    new_lens = prob.lens + 1
+    prob.set_lens(new_lens)
+    st = _status()
+    sfi.sfi_paged_kv_append(prob.shape, prob.d_kv, dev_bf16(kn), dev_bf16(vn), dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    kp, vp = prob.kv.k_pool.copy(), prob.kv.v_pool.copy()
+    for r in range(3):
+        oracle.paged_append(kp, vp, prob.kv.page_table[r], new_lens[r], kn[r], vn[r], 2, 128, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), kp)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.v_pool), vp)
+
+
+# ---------------------------------------------------------------------------
+# Fast step
+# ---------------------------------------------------------------------------
+def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids=None, heavy=0.02):
+    """Slow step + Selector + compaction on the GPU, then the fast step at the same length."""
+    sfi = _sfi()
+    prob = Problem(seed=seed, lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, heavy_frac=heavy).to_device()
+    stride = int(max(lens))
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    comp = _compact_buffers(prob, k_per_req)
+    idx = torch.zeros((prob.B, prob.Hkv, k_cap), dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_topk(scores, prob.Hkv, prob.d_kv.seq_lens, S, W, dev_i32(k_per_req), idx, comp.count,
+                        dev_status=st)
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
+    out = torch.full((prob.B, Hq, D), float("nan"), device="cuda")
+    lse = torch.full((prob.B, Hq), float("nan"), device="cuda")
+    max_tokens = S + k_cap + W + 32
+    ws = sfi.alloc_workspace(prob.shape, prob.B, max_tokens, splits)
+    rid = None if req_ids is None else dev_i32(req_ids)
+    sfi.sfi_fast_decode_attn(prob.shape, prob.d_kv, comp, S, W, prob.d_q, out, lse, req_ids=rid,
+                             max_tokens=max_tokens, num_splits=splits, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert counters_zero(ws, prob.B * Hkv)
+    sc = scores.cpu().numpy()
+    ref_idx, ref_count = run_oracle_selection(prob, sc, k_per_req, k_cap)
+    cap = comp.capacity.cpu().numpy()
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    for r in (range(prob.B) if req_ids is None else req_ids):
+        rk, rv = oracle_compact_request(prob, r, ref_idx[r], ref_count[r], cap[r])
+        o_ref, l_ref = oracle.fast_attn(prob.q[r], rk, rv, ref_count[r], prob.kv.k_pool, prob.kv.v_pool,
+                                        prob.kv.page_table[r], prob.lens[r], S, W, Hq, Hkv, D, 16)
+        assert_close(o[r], o_ref, f"fast out r={r}")
+        assert_close(l[r], l_ref, f"fast lse r={r}")
+    if req_ids is not None:
+        untouched = sorted(set(range(prob.B)) - set(req_ids))
+        assert np.isnan(o[untouched]).all()
+    return prob
+
+
+@pytest.mark.parametrize("splits", [1, 2, 5, 0])
+def test_fast_step_matches_oracle(splits):
+    lens = [1024, 1031, 530, 36, 30, 3, 17]
+    _fast_case(21 + splits, lens, 16, 8, 128, 4, 32, [64, 64, 100, 5, 5, 5, 5], 128, splits=splits)
+
+
+def test_fast_step_d64_g4_and_subset():
+    lens = [1024, 600, 1100, 900]
+    _fast_case(31, lens, 8, 2, 64, 4, 32, [64, 64, 64, 64], 64, req_ids=[2, 0])
+
+
+def test_fast_step_full_retention_equals_dense():
+    """Table 1: at 100% retention the fast step is the dense computation."""
+    S, W = 64, 256
+    lens = [2000, 1500]
+    k = [l - S - W for l in lens]
+    prob = _fast_case(41, lens, 32, 8, 128, S, W, k, max(k), heavy=0.0)
+    out_d, lse_d = _dense(prob)
+    for r in range(prob.B):
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(out_d[r], o_ref, "dense")
+
+
+def test_config1_slow_then_eight_fast_steps():
+    """Single request, GQA 8/2, D 64, context 1024, sink 4 + top-64 + recent 32: one slow
+    step at L = 1024, then 8 fast steps at L = 1025..1032, each appending its token."""
+    sfi = _sfi()
+    S, W, k = 4, 32, 64
+    prob = Problem(seed=1, lens=[1024], Hq=8, Hkv=2, D=64, S=S, W=W, extra_tokens=8, heavy_frac=40 / 988,
+                   heavy_beta=3.0).to_device()
+    g = syn.rng(1, 99)
+    st = _status()
+    scores = torch.full((1, 2, 1040), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    comp = _compact_buffers(prob, [k])
+    idx = torch.zeros((1, 2, k), dtype=torch.int32, device="cuda")
+    sfi.sfi_select_topk(scores, 2, prob.d_kv.seq_lens, S, W, dev_i32([k]), idx, comp.count, dev_status=st)
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
+    torch.cuda.synchronize()
+    sc = scores.cpu().numpy()
+    ref_idx, ref_count = run_oracle_selection(prob, sc, [k], k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), ref_idx)
+    rk, rv = oracle_compact_request(prob, 0, ref_idx[0], ref_count[0], S + k)
+    ws = sfi.alloc_workspace(prob.shape, 1, S + k + W + 32)
+    kp, vp = prob.kv.k_pool.copy(), prob.kv.v_pool.copy()
+    for step in range(8):
+        L = 1025 + step
+        q = syn.normal_bf16(g, (1, 8, 64))
+        kn, vn = syn.normal_bf16(g, (1, 2, 64)), syn.normal_bf16(g, (1, 2, 64))
+        prob.set_lens([L])
+        sfi.sfi_paged_kv_append(prob.shape, prob.d_kv, dev_bf16(kn), dev_bf16(vn), dev_status=st)
+        out = torch.empty((1, 8, 64), device="cuda")
+        lse = torch.empty((1, 8), device="cuda")
+        sfi.sfi_fast_decode_attn(prob.shape, prob.d_kv, comp, S, W, dev_bf16(q), out, lse,
+                                 max_tokens=S + k + W + 32, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        oracle.paged_append(kp, vp, prob.kv.page_table[0], L, kn[0], vn[0], 2, 64, 16)
+        o_ref, l_ref = oracle.fast_attn(q[0], rk, rv, ref_count[0], kp, vp, prob.kv.page_table[0], L, S, W,
+                                        8, 2, 64, 16)
+        assert_close(out.cpu().numpy()[0], o_ref, f"step {step}")
+        assert_close(lse.cpu().numpy()[0], l_ref, f"lse step {step}")
+
+
+# ---------------------------------------------------------------------------
+# Device-side error reporting (host-made bad inputs the kernels check; nothing faults)
+# ---------------------------------------------------------------------------
+def test_bad_page_and_length_are_reported_not_faulted():
+    sfi = _sfi()
+    prob = Problem(seed=51, lens=[100, 100], Hq=8, Hkv=2, D=64, S=4, W=32, extra_tokens=16).to_device()
+    pt = prob.d_kv.page_table.clone()
+    pt[1, 2] = 10_000_000  # page id outside the pool
+    bad = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, pt, prob.d_kv.seq_lens)
+    out = torch.zeros((2, 8, 64), device="cuda")
+    st = _status()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, bad, 4, 32, prob.d_q, out, None, None, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 1
+    o_ref, _ = prob.oracle_dense(0)
+    assert_close(out.cpu().numpy()[0], o_ref, "the healthy request is unaffected")
+    st.zero_()
+    lens_bad = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, prob.d_kv.page_table, dev_i32([100, 0]))
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, lens_bad, 4, 32, prob.d_q, out, None, None, dev_status=st)
+    kn = torch.zeros((2, 2, 64), dtype=torch.bfloat16, device="cuda")
+    sfi.sfi_paged_kv_append(prob.shape, bad, kn, kn, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 2
+
+
+def test_bad_selected_index_is_reported():
+    sfi = _sfi()
+    prob = Problem(seed=52, lens=[200], Hq=8, Hkv=2, D=64, S=4, W=32).to_device()
+    comp = _compact_buffers(prob, [8])
+    idx = torch.tensor([[[5, 6, 7, 8, 9, 10, 11, 5000], [5, 6, 7, 8, 9, 10, 11, 12]]], dtype=torch.int32,
+                       device="cuda")
+    comp.count.fill_(8)
+    st = _status()
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, 4, comp, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() & 8
