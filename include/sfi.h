@@ -213,6 +213,37 @@ SFI_API sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_pag
                               const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream);
 
 /*
+ * sfi_fast_decode_attn_noalloc - the fast step of sfi_fast_decode_attn for callers
+ * that cannot allocate device memory. The paper has no counterpart to this call; it
+ * exists for users of this library.
+ * Who needs it: sfi_fast_decode_attn wants a caller-provided device workspace for
+ * its split-KV partial results. A plugin running inside a host application that owns
+ * every device allocation, or a latency-critical path that must not call cudaMalloc
+ * (which can synchronise the whole device), has no way to provide one. This call
+ * takes the same inputs and outputs, minus the workspace, and uses instead a fixed
+ * array of SFI_NOALLOC_SCRATCH_BYTES inside the library's device memory. Every GPU
+ * that loads the library holds that array until the process exits.
+ *   - It calls no cudaMalloc, cudaFree or other allocating routine.
+ *   - Its first call on a device looks up the array's device address on that device
+ *     (cudaGetSymbolAddress, with that device current); make that first call before
+ *     any stream capture.
+ *   - Returns SFI_ERR_WORKSPACE when the split plan for these arguments needs more
+ *     than SFI_NOALLOC_SCRATCH_BYTES (sfi_workspace_size tells the need); reduce
+ *     num_splits or the batch per call.
+ *   - All calls on a device share the one array, which keeps what the last call left
+ *     in it; each call zeroes the split counters it needs (an async memset on
+ *     `stream`) before its kernel. Calls whose work can overlap on the GPU (for
+ *     example on two streams) race on the array: order them on one stream.
+ * Arguments, results and device errors are those of sfi_fast_decode_attn.
+ */
+#define SFI_NOALLOC_SCRATCH_BYTES (4u << 20)
+SFI_API sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
+                                                const sfi_compact_kv *compact, int32_t sink, int32_t recent,
+                                                const void *q, float *out, float *lse, const int32_t *req_ids,
+                                                int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                                int32_t *dev_status, void *stream);
+
+/*
  * sfi_workspace_size - bytes of workspace the attention entry points need for this
  * batch, token bound and split request on the current device (split-KV partial
  * states plus one counter per (request, KV head)). Returns 0 on invalid input.

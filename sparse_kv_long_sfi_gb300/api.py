@@ -181,6 +181,23 @@ def sfi_compact_gather(shape: AttnShape, kv: PagedKV, idx: torch.Tensor, count: 
     _check(st, "sfi_compact_gather")
 
 
+def sfi_fast_decode_attn_noalloc(shape: AttnShape, kv: PagedKV, compact: CompactKV, sink: int, recent: int,
+                                 q: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                                 req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None,
+                                 max_tokens: int = 0, num_splits: int = 0,
+                                 dev_status: Optional[torch.Tensor] = None, stream=None):
+    """sfi_fast_decode_attn without a workspace argument, for callers that cannot
+    allocate device memory: the split-KV scratch is a fixed array inside the library
+    (SFI_NOALLOC_SCRATCH_BYTES per GPU). Calls that may overlap on the GPU share that
+    array and race; order them on one stream."""
+    st = _abi.lib().sfi_fast_decode_attn_noalloc(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), ctypes.byref(compact.c()), int(sink), int(recent),
+        _ptr(q, torch.bfloat16, "q"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens), int(max_tokens),
+        int(num_splits), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_fast_decode_attn_noalloc")
+
+
 def sfi_workspace_size(shape: AttnShape, batch: int, max_tokens: int, num_splits: int = 0) -> int:
     return int(_abi.lib().sfi_workspace_size(ctypes.byref(shape.c()), int(batch), int(max_tokens), int(num_splits)))
 
