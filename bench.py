@@ -240,31 +240,17 @@ def run_gpu(args, ranks: Ranks):
             dec.fast_step(ios[t], seq_steps[t])
         dec.join()
 
-    # ---- timing events captured as graph nodes around every attention launch ----
-    marks = {"slow": [], "fast": []}
-    open_ev = {}
-
-    def timer(kind, phase, stream):
-        ev = torch.cuda.Event(enable_timing=True, external=True)
-        ev.record(stream)
-        if phase == "start":
-            open_ev[kind] = ev
-        else:
-            marks[kind].append((open_ev.pop(kind), ev))
-
-    # eager warm-up (sets kernel attributes; checks status) then capture
+    # eager warm-up (sets kernel attributes; checks status)
     with torch.cuda.stream(dec.main):
         cycle()
     torch.cuda.synchronize()
     assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
+    launches_per_cycle = NL * 3 + (cyc - 1) * NL  # slow + Selector + compaction, then fast (append fused)
 
+    # headline graph: the cycle with no timing nodes
     g_cycle = torch.cuda.CUDAGraph()
-    dec.timer = timer
     with torch.cuda.graph(g_cycle, stream=dec.main):
         cycle()
-    dec.timer = None
-    launches_per_cycle = NL * 4 + (cyc - 1) * NL * 2
-
     with torch.cuda.stream(dec.main):
         for _ in range(args.warmup):
             g_cycle.replay()
@@ -287,36 +273,58 @@ def run_gpu(args, ranks: Ranks):
     ms_cycle = ranks.max(e0.elapsed_time(e1) / args.steps)
     assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
 
-    # the same cycle captured without the timing event nodes, for their overhead
-    g_plain = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_plain, stream=dec.main):
-        cycle()
-    p0, p1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # per-kernel averages: the same cycle with timing events (graph nodes) at the step
+    # boundaries only; each step's main stream is NL back-to-back attention launches
+    step_marks = []
+
+    def cycle_marked():
+        def mark():
+            ev = torch.cuda.Event(enable_timing=True, external=True)
+            ev.record(dec.main)
+            return ev
+        a = mark()
+        dec.slow_step(ios[0], seq_steps[0])
+        b = mark()
+        step_marks.append(("slow", a, b))
+        for t in range(1, cyc):
+            a = mark()
+            dec.fast_step(ios[t], seq_steps[t])
+            b = mark()
+            step_marks.append(("fast", a, b))
+        dec.join()
+
+    g_marked = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_marked, stream=dec.main):
+        cycle_marked()
+    reps = max(3, min(args.steps, 10))
+    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     with torch.cuda.stream(dec.main):
         for _ in range(args.warmup):
-            g_plain.replay()
-        p0.record(dec.main)
-        for _ in range(args.steps):
-            g_plain.replay()
-        p1.record(dec.main)
+            g_marked.replay()
+        m0.record(dec.main)
+        for _ in range(reps):
+            g_marked.replay()
+        m1.record(dec.main)
     torch.cuda.synchronize()
-    ms_plain = ranks.max(p0.elapsed_time(p1) / args.steps)
-
-    # per-kernel durations from the events of the last replay of the timed region
-    try:
-        dur = {k: [a.elapsed_time(b) * 1e3 for a, b in v] for k, v in marks.items()}
-        timing_method = "graph event nodes around each launch, last timed replay"
-    except RuntimeError as exc:  # event timing inside graphs unavailable
+    ms_marked = m0.elapsed_time(m1) / reps
+    try:  # durations of the last replay
+        dur = {"slow": [], "fast": []}
+        for kind, a, b in step_marks:
+            dur[kind].append(a.elapsed_time(b) * 1e3 / NL)
+        timing_method = (f"events at decode-step boundaries (graph nodes), {NL} back-to-back launches per step, "
+                         f"last of {reps} replays after the headline region")
+    except RuntimeError as exc:
         dur = None
         timing_method = f"unavailable: {exc}"
 
     # ---- algorithmic bytes of one cycle ----
     n_ret_fast = S + k_main + W  # per (request, KV head) at L > S + W
-    by_fast = fast_bytes(B, Hq, Hkv, D, P, n_ret_fast, W)
-    by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True)
+    # per attention launch, the fused append included (read k_new/v_new, write the page slot)
+    by_fast = fast_bytes(B, Hq, Hkv, D, P, n_ret_fast, W) + append_bytes(B, Hkv, D)
+    by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True) + append_bytes(B, Hkv, D)
     nC = L0 - S - W
     by_cycle = (NL * (by_slow + select_bytes(B, Hkv, nC, k_main) + compact_bytes(B, Hkv, D, S, k_main)) +
-                (cyc - 1) * NL * by_fast + cyc * NL * append_bytes(B, Hkv, D))
+                (cyc - 1) * NL * by_fast)
     us_step = ms_cycle * 1e3 / cyc
     peak, peak_kind = measured_peaks()
 
@@ -324,8 +332,8 @@ def run_gpu(args, ranks: Ranks):
     if dur:
         t_fast = statistics.mean(dur["fast"]) if dur["fast"] else 0.0
         t_slow = statistics.mean(dur["slow"]) if dur["slow"] else 0.0
-        share_fast = t_fast * len(dur["fast"]) / (ms_cycle * 1e3)
-        share_slow = t_slow * len(dur["slow"]) / (ms_cycle * 1e3)
+        share_fast = t_fast * (cyc - 1) * NL / (ms_marked * 1e3)
+        share_slow = t_slow * NL / (ms_marked * 1e3)
         if share_slow >= share_fast:
             name, per, tl, sh = "attn_decode_kernel<128,dense,scores> (slow step)", by_slow, t_slow, share_slow
         else:
@@ -348,7 +356,7 @@ def run_gpu(args, ranks: Ranks):
                    "step": f"1 slow + {cyc - 1} fast decode steps x {NL} layers (one CUDA graph)",
                    "l2": f"inputs larger than L2: {NL} distinct layers, {by_cycle / cyc / 1e9:.2f} GB per decode step",
                    "parallelism": f"replicas x{ranks.world}"},
-        "us_per_step_without_timing_nodes": round(ms_plain * 1e3 / cyc, 3),
+        "us_per_step_with_step_timing_nodes": round(ms_marked * 1e3 / cyc, 3),
         "tokens_per_s": round(ranks.world * B * cyc / (ms_cycle * 1e-3), 1),
         "hbm_GBps_cycle": round(by_cycle / (ms_cycle * 1e-3) / 1e9, 1),
         "bytes_per_cycle": by_cycle,
@@ -454,9 +462,9 @@ def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_s
     def dense_step():
         for i, Lb in enumerate(layers):
             kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
-            sfi.sfi_paged_kv_append(shape, kv, kn_all[1, i], vn_all[1, i], stream=dec.main)
             sfi.sfi_slow_dense_attn_with_scores(shape, kv, S, 0, q_all[1, i], out[i], None, None,
-                                                max_tokens=L1 + P, workspace=ws_dense, stream=dec.main)
+                                                k_new=kn_all[1, i], v_new=vn_all[1, i], max_tokens=L1 + P,
+                                                workspace=ws_dense, stream=dec.main, flags=dec.attn_flags)
 
     us_dense = time_graph(dense_step)
     by_dense = dense_bytes(B, Hq, Hkv, D, P, L1, scores=False) + append_bytes(B, Hkv, D)
@@ -478,9 +486,9 @@ def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_s
         def fast_step():
             for i, Lb in enumerate(layers):
                 kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
-                sfi.sfi_paged_kv_append(shape, kv, kn_all[1, i], vn_all[1, i], stream=dec.main)
-                sfi.sfi_fast_decode_attn(shape, kv, Lb.compact, S, W, q_all[1, i], out[i], None, max_tokens=max_tok,
-                                         workspace=ws_fast, stream=dec.main)
+                sfi.sfi_fast_decode_attn(shape, kv, Lb.compact, S, W, q_all[1, i], out[i], None,
+                                         k_new=kn_all[1, i], v_new=vn_all[1, i], max_tokens=max_tok,
+                                         workspace=ws_fast, stream=dec.main, flags=dec.attn_flags)
 
         us = time_graph(fast_step)
         n_ret = S + k + W
@@ -494,7 +502,7 @@ def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_s
     return {"dense_us_per_step": round(us_dense, 2),
             "dense_GBps": round(NL * by_dense / (us_dense * 1e-6) / 1e9, 1),
             "dense_frac_of_peak": round(NL * by_dense / (us_dense * 1e-6) / 1e9 / peak, 3),
-            "points": rows, "note": "fast and dense steps include the paged append; 28 layers per step; "
+            "points": rows, "note": "fast and dense steps include the (fused) paged append; 28 layers per step; "
                                     "Table 1 speedups are the paper's (hardware unstated), context only"}
 
 

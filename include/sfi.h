@@ -83,6 +83,15 @@ typedef enum {
 #define SFI_DEV_TIMEOUT 16u     /* an in-kernel pipeline wait ran past its bound */
 #define SFI_DEV_BAD_COMPACT 32u /* compact rows of a request fall outside the buffer */
 
+/* Launch flags of the attention entry points (bitwise OR). */
+/* SFI_ATTN_EARLY_KV_PREFETCH: the kernel that precedes this call on the stream does
+ * not write this call's paged KV pools, compact buffer, page table, lengths or
+ * request ids, nor the compact counts and capacities. The
+ * kernel may then start streaming them (programmatic dependent launch) before that
+ * preceding kernel has finished; q, k_new and v_new are still read, and every output
+ * written, only after it has finished. Without the flag nothing is read before then. */
+#define SFI_ATTN_EARLY_KV_PREFETCH 1u
+
 /* Attention geometry shared by all calls. */
 typedef struct {
     int32_t num_q_heads;  /* Hq */
@@ -136,6 +145,11 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  * [max(S, L - W), L). The compact buffer must have been filled by
  * sfi_compact_gather at a length >= min(S, L) (the sink is complete).
  *   q       : bf16 [B][Hq][D]
+ *   k_new, v_new : bf16 [B][Hkv][D] or both NULL. When given, the call first does
+ *                what sfi_paged_kv_append does (the current token goes to position
+ *                L - 1 of the pages) and attends to the cache after that append;
+ *                when L <= S the token is a sink row and is used in place of compact
+ *                row L - 1 (the compact buffer itself is not written).
  *   out     : fp32 [B][Hq][D]
  *   lse     : fp32 [B][Hq] or NULL
  *   max_tokens : an upper bound on S + max count + W + P over the batch, used to
@@ -143,6 +157,7 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  *                is small. It affects speed only, never results.
  *   num_splits : 0 = automatic; otherwise the number of KV splits per
  *                (request, KV head) (clamped to the plan's maximum).
+ *   flags      : 0 or SFI_ATTN_EARLY_KV_PREFETCH.
  *   workspace  : at least sfi_workspace_size(shape, batch, max_tokens, num_splits)
  *                bytes of device memory, zero-filled before its first use. The
  *                kernels leave it zero-filled again when they finish without a
@@ -152,8 +167,9 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  * SFI_DEV_BAD_COMPACT, SFI_DEV_TIMEOUT.
  */
 SFI_API sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
-                                int32_t sink, int32_t recent, const void *q, float *out, float *lse,
-                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                int32_t sink, int32_t recent, const void *q, const void *k_new, const void *v_new,
+                                float *out, float *lse,
+                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
                                 void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
@@ -165,16 +181,19 @@ SFI_API sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_p
  *   scores[r][kv][j] = -inf                                        for other j < L
  * in fp32; entries j >= L are not written. With scores == NULL this is the dense
  * full-KV decode attention (the denominator of Table 1).
+ *   k_new, v_new : bf16 [B][Hkv][D] or both NULL: the current token, appended at
+ *                  position L - 1 before the attention (as sfi_paged_kv_append)
  *   scores       : fp32 [B][Hkv][score_stride], score_stride >= max L, or NULL
  *   max_tokens   : an upper bound on L + P over the batch (split planning only)
- *   num_splits, workspace, workspace_bytes : as for sfi_fast_decode_attn
+ *   num_splits, flags, workspace, workspace_bytes : as for sfi_fast_decode_attn
  * Device errors: SFI_DEV_BAD_LEN (also when L > score_stride: the scores of that
  * request are then not written), SFI_DEV_BAD_PAGE, SFI_DEV_TIMEOUT.
  */
 SFI_API sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
-                                           int32_t recent, const void *q, float *out, float *lse, float *scores,
+                                           int32_t recent, const void *q, const void *k_new, const void *v_new,
+                                           float *out, float *lse, float *scores,
                                            int64_t score_stride, const int32_t *req_ids, int32_t batch,
-                                           int32_t max_tokens, int32_t num_splits, void *workspace,
+                                           int32_t max_tokens, int32_t num_splits, uint32_t flags, void *workspace,
                                            size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
@@ -188,8 +207,9 @@ SFI_API sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, 
  *   k_per_req : int32 [B], 0 <= k_r <= k_cap
  *   idx_out   : int32 [B][Hkv][k_cap]; entries past k_eff are not written
  *   count_out : int32 [B]
- * Device errors: SFI_DEV_K_OVERFLOW, SFI_DEV_BAD_LEN (L > score_stride); that
- * request's outputs are not written.
+ * Limits: |C| <= 262144 candidates per request.
+ * Device errors: SFI_DEV_K_OVERFLOW (also when |C| is past the limit),
+ * SFI_DEV_BAD_LEN (L > score_stride); that request's outputs are not written.
  */
 SFI_API sfi_status sfi_select_topk(const float *scores, int64_t score_stride, int32_t num_kv_heads, const int32_t *seq_lens,
                            int32_t sink, int32_t recent, const int32_t *k_per_req, int32_t k_cap, int32_t *idx_out,
@@ -239,8 +259,9 @@ SFI_API sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_pag
 #define SFI_NOALLOC_SCRATCH_BYTES (4u << 20)
 SFI_API sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
                                                 const sfi_compact_kv *compact, int32_t sink, int32_t recent,
-                                                const void *q, float *out, float *lse, const int32_t *req_ids,
-                                                int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                                const void *q, const void *k_new, const void *v_new, float *out,
+                                                float *lse, const int32_t *req_ids,
+                                                int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
                                                 int32_t *dev_status, void *stream);
 
 /*

@@ -259,3 +259,29 @@ def device_plant_heavy_hitters_(k_pool, page_table, q, seq_lens, sink: int, rece
         vals = flat[rows.view(-1)].float().view(Hkv, m, D) + beta * u[r].view(Hkv, 1, D)
         flat[rows.view(-1)] = vals.view(-1, D).to(k_pool.dtype)
     return k_pool
+
+
+def device_plant_key_profile_(k_pool, page_table, q, r: int, positions, betas, dup_pairs=()):
+    """K rows of request r at `positions` (host ints) get K += beta_j * u (u along the
+    group-summed query of each KV head), then K rows are copied bit for bit for each
+    (src, dst) in dup_pairs (exact logit ties). In place on the device pool."""
+    import torch
+    B, Hq, D = q.shape
+    Hkv, P = k_pool.shape[1], k_pool.shape[2]
+    G = Hq // Hkv
+    qbar = q[r].float().view(Hkv, G, D).sum(1)
+    u = qbar / qbar.norm(dim=-1, keepdim=True).clamp_min(1e-12)            # [Hkv][D]
+    flat = k_pool.view(-1, D)
+    pos = torch.as_tensor(np.asarray(positions, np.int64), device=q.device)
+    beta = torch.as_tensor(np.asarray(betas, np.float32), device=q.device)
+    pages = page_table[r].long()[pos // P]
+    kvh = torch.arange(Hkv, device=q.device).view(Hkv, 1)
+    rows = ((pages.view(1, -1) * Hkv + kvh) * P + (pos % P).view(1, -1)).view(-1)
+    vals = flat[rows].float().view(Hkv, -1, D) + beta.view(1, -1, 1) * u.view(Hkv, 1, D)
+    flat[rows] = vals.view(-1, D).to(k_pool.dtype)
+    for src, dst in dup_pairs:
+        for h in range(Hkv):
+            sr = (int(page_table[r, src // P]) * Hkv + h) * P + src % P
+            dr = (int(page_table[r, dst // P]) * Hkv + h) * P + dst % P
+            flat[dr] = flat[sr]
+    return k_pool

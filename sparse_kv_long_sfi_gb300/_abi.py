@@ -12,6 +12,7 @@ import threading
 from .build import LIB
 
 c_i32, c_i64, c_f32, c_vp, c_sz = ctypes.c_int32, ctypes.c_int64, ctypes.c_float, ctypes.c_void_p, ctypes.c_size_t
+c_u32 = ctypes.c_uint32
 
 
 class sfi_attn_shape(ctypes.Structure):
@@ -32,6 +33,7 @@ class sfi_compact_kv(ctypes.Structure):
 SFI_OK, SFI_ERR_INVALID_ARG, SFI_ERR_UNSUPPORTED, SFI_ERR_WORKSPACE, SFI_ERR_CUDA = range(5)
 SFI_DEV_BAD_PAGE, SFI_DEV_BAD_LEN, SFI_DEV_K_OVERFLOW = 1, 2, 4
 SFI_DEV_BAD_INDEX, SFI_DEV_TIMEOUT, SFI_DEV_BAD_COMPACT = 8, 16, 32
+SFI_ATTN_EARLY_KV_PREFETCH = 1
 
 P_SHAPE = ctypes.POINTER(sfi_attn_shape)
 P_PAGED = ctypes.POINTER(sfi_paged_kv)
@@ -40,16 +42,16 @@ P_COMPACT = ctypes.POINTER(sfi_compact_kv)
 # name -> (restype, argtypes), in the order of include/sfi.h
 PROTOTYPES = {
     "sfi_paged_kv_append": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_vp, c_i32, c_vp, c_vp]),
-    "sfi_fast_decode_attn": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i32,
-                                     c_i32, c_i32, c_vp, c_sz, c_vp, c_vp]),
-    "sfi_slow_dense_attn_with_scores": (c_i32, [P_SHAPE, P_PAGED, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_i64,
-                                                c_vp, c_i32, c_i32, c_i32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_fast_decode_attn": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                     c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_slow_dense_attn_with_scores": (c_i32, [P_SHAPE, P_PAGED, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                                c_i64, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
     "sfi_select_topk": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp,
                                 c_vp]),
     "sfi_compact_gather": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_i32, c_i32, P_COMPACT, c_vp, c_i32, c_vp,
                                    c_vp]),
     "sfi_fast_decode_attn_noalloc": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
-                                             c_i32, c_i32, c_i32, c_vp, c_vp]),
+                                             c_vp, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_vp]),
     "sfi_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32]),
     "sfi_plan_splits": (c_i32, [P_SHAPE, c_i32, c_i32, c_i32]),
     "sfi_status_string": (ctypes.c_char_p, [c_i32]),

@@ -16,6 +16,9 @@ import torch
 from . import _abi
 
 
+SFI_ATTN_EARLY_KV_PREFETCH = _abi.SFI_ATTN_EARLY_KV_PREFETCH
+
+
 class SFIError(RuntimeError):
     def __init__(self, status: int, where: str):
         name = _abi.lib().sfi_status_string(status).decode()
@@ -129,14 +132,17 @@ def sfi_fast_decode_attn(shape: AttnShape, kv: PagedKV, compact: CompactKV, sink
                          q: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                          req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None, max_tokens: int = 0,
                          num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
-                         dev_status: Optional[torch.Tensor] = None, stream=None):
+                         dev_status: Optional[torch.Tensor] = None, stream=None,
+                         k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                         flags: int = 0):
     ws = _ptr(workspace, torch.uint8, "workspace")
     st = _abi.lib().sfi_fast_decode_attn(
         ctypes.byref(shape.c()), ctypes.byref(kv.c()), ctypes.byref(compact.c()), int(sink), int(recent),
-        _ptr(q, torch.bfloat16, "q"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens), int(max_tokens),
-        int(num_splits), ws, 0 if workspace is None else workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"),
-        _stream(stream))
+        int(num_splits), int(flags), ws, 0 if workspace is None else workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "sfi_fast_decode_attn")
 
 
@@ -145,15 +151,17 @@ def sfi_slow_dense_attn_with_scores(shape: AttnShape, kv: PagedKV, sink: int, re
                                     scores: Optional[torch.Tensor] = None, req_ids: Optional[torch.Tensor] = None,
                                     batch: Optional[int] = None, max_tokens: int = 0, num_splits: int = 0,
                                     workspace: Optional[torch.Tensor] = None,
-                                    dev_status: Optional[torch.Tensor] = None, stream=None):
+                                    dev_status: Optional[torch.Tensor] = None, stream=None,
+                                    k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                                    flags: int = 0):
     ws = _ptr(workspace, torch.uint8, "workspace")
     stride = 0 if scores is None else int(scores.shape[-1])
     st = _abi.lib().sfi_slow_dense_attn_with_scores(
         ctypes.byref(shape.c()), ctypes.byref(kv.c()), int(sink), int(recent), _ptr(q, torch.bfloat16, "q"),
-        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(scores, torch.float32, "scores"),
+        _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"), _ptr(scores, torch.float32, "scores"),
         stride, _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens), int(max_tokens),
-        int(num_splits), ws, 0 if workspace is None else workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"),
-        _stream(stream))
+        int(num_splits), int(flags), ws, 0 if workspace is None else workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "sfi_slow_dense_attn_with_scores")
 
 
@@ -185,16 +193,19 @@ def sfi_fast_decode_attn_noalloc(shape: AttnShape, kv: PagedKV, compact: Compact
                                  q: torch.Tensor, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                                  req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None,
                                  max_tokens: int = 0, num_splits: int = 0,
-                                 dev_status: Optional[torch.Tensor] = None, stream=None):
+                                 dev_status: Optional[torch.Tensor] = None, stream=None,
+                                 k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                                 flags: int = 0):
     """sfi_fast_decode_attn without a workspace argument, for callers that cannot
     allocate device memory: the split-KV scratch is a fixed array inside the library
     (SFI_NOALLOC_SCRATCH_BYTES per GPU). Calls that may overlap on the GPU share that
     array and race; order them on one stream."""
     st = _abi.lib().sfi_fast_decode_attn_noalloc(
         ctypes.byref(shape.c()), ctypes.byref(kv.c()), ctypes.byref(compact.c()), int(sink), int(recent),
-        _ptr(q, torch.bfloat16, "q"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens), int(max_tokens),
-        int(num_splits), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+        int(num_splits), int(flags), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
     _check(st, "sfi_fast_decode_attn_noalloc")
 
 

@@ -8,12 +8,12 @@
 // in a contiguous compact buffer, recent tokens read in place from paged KV).
 //
 // Design (HBM-bound: every K/V byte is read once per step):
-//  * Grid (split, KV head, request). A (request, KV head) unit's token stream is cut
-//    into 16-token sub-blocks: compact rows first (fast mode), then the pages of the
-//    recent window (fast) or of [0, L) (dense). Split c owns a contiguous range of
-//    sub-blocks.
+//  * Grid (split, KV head, request), two CTAs per SM. A (request, KV head) unit's
+//    token stream is cut into 16-token sub-blocks: compact rows first (fast mode),
+//    then the pages of the recent window (fast) or of [0, L) (dense). Split c owns a
+//    contiguous range of sub-blocks.
 //  * One producer warp issues TMA tensor loads (2-D tiled, 128-byte swizzle, L2
-//    evict-first) of K and V sub-blocks into a ring of shared-memory stages;
+//    evict-first) of K and V sub-blocks into a 96 KB ring of shared-memory stages;
 //    completion is tracked by mbarriers (transaction bytes). Page ids are fetched a
 //    chunk of 32 sub-blocks ahead by the whole producer warp.
 //  * Four consumer warps each own one sub-block per stage. QK^T and PV run on the
@@ -22,9 +22,15 @@
 //    CUDA-core unpacking. Online softmax in fp32 on the C fragments.
 //  * The slow step sums the C fragments over the group's rows with warp shuffles and
 //    writes the fp32 masked scores.
-//  * Warps merge through shared memory; splits merge in-kernel: the last CTA of a
-//    unit (atomic counter, self-resetting) combines the partial (m, l, o) states.
-//  * Every wait is bounded and reports SFI_DEV_TIMEOUT instead of hanging.
+//  * With k_new/v_new the consumer warp owning position L - 1 writes the current token
+//    into its tile and into the page (the append fused into the attention).
+//  * Warps merge through shared memory. Splits of a unit merge in-kernel: with up to
+//    8 splits the unit's CTAs form one thread-block cluster and rank 0 reads the
+//    others' partial (m, l, o) states through distributed shared memory; with more,
+//    the last CTA of the unit (atomic counter, self-resetting) merges them from a
+//    global workspace.
+//  * Every wait on the pipeline or on a peer CTA is bounded and reports
+//    SFI_DEV_TIMEOUT instead of hanging.
 #include <atomic>
 
 #include "sfi_device.cuh"
@@ -37,10 +43,12 @@ struct AttnTile {
     static constexpr int kBoxes = D / 64;                        // 128-byte boxes per row
     static constexpr int kSubBytes = kSubTokens * D * 2;         // K (or V) of one sub-block
     static constexpr int kStageBytes = kConsumerWarps * 2 * kSubBytes;
-    static constexpr int kStages = (D == 128) ? 3 : 6;
+    static constexpr int kRingBytes = 96 * 1024;                 // two CTAs per SM
+    static constexpr int kStages = kRingBytes / kStageBytes;
     static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
     static constexpr int kKSteps = D / 16;                       // mma k-steps of QK^T
     static constexpr int kNTiles = D / 8;                        // mma n-tiles of PV
+    static constexpr int kMergeStride = D + 4;                   // padded rows of the warp-merge scratch
 };
 
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
@@ -59,24 +67,27 @@ struct UnitStream {
     int lo_pos;    // first valid position of the paged segment
     int nb;        // total sub-blocks
     int64_t crow0; // first compact row of this KV head (fast mode)
+    int sb_app;    // sub-block holding position L - 1 (the current token)
+    int row_app;   // its row inside that sub-block
 };
 
 template <int MODE>
 __device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh, UnitStream &u) {
+    // All per-request metadata is loaded up front, in one round trip.
     u.L = p.seq_lens[r];
+    const int cnt = MODE == kModeFast ? p.c_count[r] : 0;
+    const int cap = MODE == kModeFast ? p.c_capacity[r] : 0;
+    const int64_t off = MODE == kModeFast ? p.c_row_offset[r] : 0;
     if (u.L < 1 || u.L > p.max_pages * kSubTokens) {
         if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_LEN);
         return false;
     }
     if (MODE == kModeFast) {
         const int ns = min(p.sink, u.L);
-        const int cnt = p.c_count[r];
-        const int cap = p.c_capacity[r];
         if (cnt < 0 || cnt > cap - p.sink || (cnt > 0 && u.L < p.sink)) {
             if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_K_OVERFLOW);
             return false;
         }
-        const int64_t off = p.c_row_offset[r];
         if (off < 0 || off + (int64_t)p.hkv * cap > p.c_total_rows) {
             if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_COMPACT);
             return false;
@@ -89,10 +100,12 @@ __device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh,
             u.lo_pos = rs;
             u.page0 = rs / kSubTokens;
             u.nb = u.nb1 + ((u.L - 1) / kSubTokens - u.page0 + 1);
+            u.sb_app = u.nb1 + ((u.L - 1) / kSubTokens - u.page0);  // last page of the recent window
         } else {
             u.lo_pos = u.L;
             u.page0 = 0;
             u.nb = u.nb1;
+            u.sb_app = (u.L - 1) / kSubTokens;  // L <= S: the current token is a sink row
         }
     } else {
         u.crow0 = 0;
@@ -101,7 +114,9 @@ __device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh,
         u.lo_pos = 0;
         u.page0 = 0;
         u.nb = (u.L + kSubTokens - 1) / kSubTokens;
+        u.sb_app = u.nb - 1;
     }
+    u.row_app = (u.L - 1) % kSubTokens;
     return true;
 }
 
@@ -220,7 +235,38 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
     }
 }
 
-template <int D, int MODE, bool SCORES>
+// Write the current token's K/V (k_new/v_new of this KV head) into row u.row_app of
+// the swizzled K and V tiles at `tile` and into the paged cache at position L - 1.
+// One 16-byte chunk per lane; the writing lanes then order their generic-proxy
+// shared-memory writes before later TMA (async-proxy) writes into the same stage.
+template <int D>
+__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
+                                                   const UnitStream &u, int lane) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const int64_t src_off = ((int64_t)r * p.hkv + kvh) * D + c * 8;
+        const int4 val = *reinterpret_cast<const int4 *>((is_v ? p.v_new : p.k_new) + src_off);
+        const int row = u.row_app;
+        uint8_t *base = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128) + row * 128;
+        *reinterpret_cast<int4 *>(base + (((c & 7) ^ (row & 7)) << 4)) = val;
+        const int pos = u.L - 1;
+        const int page = p.page_table[(int64_t)r * p.max_pages + pos / kSubTokens];
+        if (page < 0 || page >= p.num_pages) {
+            if (lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
+        } else {
+            __nv_bfloat16 *dst = (is_v ? p.v_pool_w : p.k_pool_w) +
+                                 (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D + c * 8;
+            *reinterpret_cast<int4 *>(dst) = val;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+}
+
+template <int D, int MODE, bool SCORES, bool CLUSTER>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tm_pool_k, const __grid_constant__ CUtensorMap tm_pool_v,
                        const __grid_constant__ CUtensorMap tm_comp_k, const __grid_constant__ CUtensorMap tm_comp_v,
@@ -230,16 +276,35 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[T::kStages];
     __shared__ __align__(8) uint64_t empty_bar[T::kStages];
+    __shared__ __align__(8) uint64_t merge_bar;  // cluster merge handshake
     __shared__ int2 s_info[T::kStages][kConsumerWarps];
     __shared__ int s_last;
     __shared__ int s_timeout;
 
     const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
-    const int r = p.req_ids ? p.req_ids[b] : b;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tm_pool_k);
+        tma_prefetch_desc(&tm_pool_v);
+        if (MODE == kModeFast) {
+            tma_prefetch_desc(&tm_comp_k);
+            tma_prefetch_desc(&tm_comp_v);
+        }
+    }
+    // Programmatic dependent launch: this CTA may have started while the previous
+    // kernel in the stream was still running. By default it waits for that kernel
+    // (and its memory) before touching any global data. With early_prefetch the
+    // caller guarantees that kernel writes none of the KV state read below, so only
+    // the consumer warps wait, right before they read q and write anything. The next
+    // kernel is released only after this CTA's wait, so at most two kernels overlap.
+    if (!p.early_prefetch) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
+    const int r = p.req_ids ? p.req_ids[b] : b;
 
     UnitStream u;
-    if (!unit_stream<MODE>(p, r, kvh, u)) return;  // uniform across the CTA (and the unit)
+    if (!unit_stream<MODE>(p, r, kvh, u)) return;  // uniform across the CTA and its cluster
     const int per = (u.nb + p.splits - 1) / p.splits;
     const int sb_begin = split * per;
     const int sb_end = min(u.nb, sb_begin + per);
@@ -251,21 +316,18 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             mbar_init(&full_bar[i], kConsumerWarps);
             mbar_init(&empty_bar[i], kConsumerWarps);
         }
+        if (CLUSTER) mbar_init(&merge_bar, split == 0 ? p.splits - 1 : 1);
         s_timeout = 0;
         fence_barrier_init();
     }
-    __syncthreads();
+    // Every CTA of a cluster reaches this point unconditionally (the only branch
+    // before it depends on the unit's metadata, which all of them read alike): after
+    // it, each CTA's merge barrier is initialised for remote arrivals.
+    if (CLUSTER) cluster_sync_all();
+    else __syncthreads();
 
     if (warp == kConsumerWarps) {
         // ---------------- producer warp ----------------
-        if (lane == 0) {
-            tma_prefetch_desc(&tm_pool_k);
-            tma_prefetch_desc(&tm_pool_v);
-            if (MODE == kModeFast) {
-                tma_prefetch_desc(&tm_comp_k);
-                tma_prefetch_desc(&tm_comp_v);
-            }
-        }
         const uint64_t policy = l2_policy_evict_first();
         const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
         // Page id of sub-block sb (-1 for compact sub-blocks and past the end).
@@ -328,10 +390,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 }
             }
         }
-        return;
+        return;  // the producer takes no part in the merges
     }
 
     // ---------------- consumer warps ----------------
+    if (p.early_prefetch) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
     const int g = lane >> 2, t = lane & 3;
     const int G = p.group;
     uint32_t qa[D / 16][2];
@@ -370,6 +436,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
         const int2 in = s_info[slot][warp];
         const int lo = in.x & 0xffff, hi = in.x >> 16;
+        if (p.k_new != nullptr && sb_begin + st * kConsumerWarps + warp == u.sb_app) {
+            // Fused append: the current token's K/V replace row L - 1 of this tile (the
+            // attention sees the cache after the append) and are written to the pages.
+            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane);
+        }
         if (hi > lo) {
             const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);
             consume_sub_block<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, in.y, qa, o, m_run, l_run, p,
@@ -378,65 +449,116 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
     }
-    if (timed_out) {
-        if (lane == 0) {
-            report(p.dev_status, SFI_DEV_TIMEOUT);
-            s_timeout = 1;
-        }
+    if (timed_out && lane == 0) {
+        report(p.dev_status, SFI_DEV_TIMEOUT);
+        s_timeout = 1;
     }
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 1);
     l_run += __shfl_xor_sync(0xffffffffu, l_run, 2);
 
     // ---- merge the consumer warps through shared memory (stage buffers are free now) ----
     consumer_bar_sync();
-    if (s_timeout) return;
-    float *sm_o = reinterpret_cast<float *>(smem);                  // [warps][8][D]
-    float *sm_m = sm_o + kConsumerWarps * kMaxGroup * D;            // [warps][8]
+    const bool ok = s_timeout == 0;
+    constexpr int MS = T::kMergeStride;
+    float *sm_o = reinterpret_cast<float *>(smem);                  // [warps][8][MS]
+    float *sm_m = sm_o + kConsumerWarps * kMaxGroup * MS;           // [warps][8]
     float *sm_l = sm_m + kConsumerWarps * kMaxGroup;                // [warps][8]
+    float *cp_o = sm_l + kConsumerWarps * kMaxGroup;                // [8][D]  this CTA's partial (cluster merge)
+    float *cp_m = cp_o + kMaxGroup * D;                             // [8]
+    float *cp_l = cp_m + kMaxGroup;                                 // [8]
+    if (ok) {
 #pragma unroll
-    for (int nt = 0; nt < D / 8; ++nt) {
-        float2 v = make_float2(o[nt][0], o[nt][1]);
-        *reinterpret_cast<float2 *>(&sm_o[(warp * kMaxGroup + g) * D + nt * 8 + 2 * t]) = v;
-    }
-    if (t == 0) {
-        sm_m[warp * kMaxGroup + g] = m_run;
-        sm_l[warp * kMaxGroup + g] = l_run;
+        for (int nt = 0; nt < D / 8; ++nt) {
+            float2 v = make_float2(o[nt][0], o[nt][1]);
+            *reinterpret_cast<float2 *>(&sm_o[(warp * kMaxGroup + g) * MS + nt * 8 + 2 * t]) = v;
+        }
+        if (t == 0) {
+            sm_m[warp * kMaxGroup + g] = m_run;
+            sm_l[warp * kMaxGroup + g] = l_run;
+        }
     }
     consumer_bar_sync();
 
     const int ctid = threadIdx.x;  // 0 .. 127
     const int64_t unit = (int64_t)b * p.hkv + kvh;
     const int64_t head0 = (int64_t)r * p.hq + (int64_t)kvh * G;
-    for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-        const int row = e / D, d = e - (e / D) * D;
-        float M = -INFINITY;
+    if (ok) {
+        for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+            const int row = e / D, d = e - (e / D) * D;
+            float M = -INFINITY;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + row]);
-        float acc = 0.f, lsum = 0.f;
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kMaxGroup + row]);
+            float acc = 0.f, lsum = 0.f;
 #pragma unroll
-        for (int w = 0; w < kConsumerWarps; ++w) {
-            const float mw = sm_m[w * kMaxGroup + row];
-            if (mw != -INFINITY) {
-                const float f = fast_exp2(mw - M);
-                acc += sm_o[(w * kMaxGroup + row) * D + d] * f;
-                lsum += sm_l[w * kMaxGroup + row] * f;
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = sm_m[w * kMaxGroup + row];
+                if (mw != -INFINITY) {
+                    const float f = fast_exp2(mw - M);
+                    acc += sm_o[(w * kMaxGroup + row) * MS + d] * f;
+                    lsum += sm_l[w * kMaxGroup + row] * f;
+                }
             }
-        }
-        if (p.splits == 1) {
-            p.out[(head0 + row) * D + d] = acc / lsum;
-            if (d == 0 && p.lse) p.lse[head0 + row] = (M + log2f(lsum)) * kLn2;
-        } else {
-            const int64_t slot = (unit * p.splits + split) * kMaxGroup + row;
-            p.ws_part[slot * D + d] = acc;
-            if (d == 0) {
-                p.ws_ml[slot * 2 + 0] = M;
-                p.ws_ml[slot * 2 + 1] = lsum;
+            if (p.splits == 1) {
+                p.out[(head0 + row) * D + d] = acc / lsum;
+                if (d == 0 && p.lse) p.lse[head0 + row] = (M + log2f(lsum)) * kLn2;
+            } else if (CLUSTER) {
+                cp_o[row * D + d] = acc;
+                if (d == 0) {
+                    cp_m[row] = M;
+                    cp_l[row] = lsum;
+                }
+            } else {
+                const int64_t slot = (unit * p.splits + split) * kMaxGroup + row;
+                p.ws_part[slot * D + d] = acc;
+                if (d == 0) {
+                    p.ws_ml[slot * 2 + 0] = M;
+                    p.ws_ml[slot * 2 + 1] = lsum;
+                }
             }
         }
     }
     if (p.splits == 1) return;
 
-    // ---- split-KV merge by the last CTA of this unit ----
+    if (CLUSTER) {
+        // ---- split merge inside the cluster, through distributed shared memory ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        if (split != 0) {
+            if (ctid == 0) {
+                mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), 0));  // "my partial is ready"
+                // Stay alive (shared memory readable) until rank 0 has read it.
+                if (!mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            }
+            return;
+        }
+        if (ctid == 0) s_last = mbar_wait_cluster_bounded(&merge_bar, 0) ? 1 : 0;
+        consumer_bar_sync();
+        if (s_last && ok) {
+            for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
+                const int row = e / D, d = e - (e / D) * D;
+                float M = -INFINITY;
+                for (int s = 0; s < p.splits; ++s)
+                    M = fmaxf(M, ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s)));
+                float acc = 0.f, lsum = 0.f;
+                for (int s = 0; s < p.splits; ++s) {
+                    const float ls = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
+                    if (ls > 0.f) {
+                        const float f = fast_exp2(ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s)) - M);
+                        acc += ld_cluster_f32(cluster_map(smem_u32(&cp_o[row * D + d]), s)) * f;
+                        lsum += ls * f;
+                    }
+                }
+                p.out[(head0 + row) * D + d] = acc / lsum;
+                if (d == 0 && p.lse) p.lse[head0 + row] = (M + log2f(lsum)) * kLn2;
+            }
+        }
+        if (!s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
+        consumer_bar_sync();  // every read of the peers' shared memory is done
+        if (ctid > 0 && ctid < p.splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
+        return;
+    }
+
+    // ---- split merge by the last CTA of this unit, through the global workspace ----
+    if (!ok) return;
     __threadfence();
     consumer_bar_sync();
     if (ctid == 0) {
@@ -477,10 +599,10 @@ WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim) {
     return w;
 }
 
-template <int D, int MODE, bool SCORES>
+template <int D, int MODE, bool SCORES, bool CLUSTER>
 static cudaError_t launch_one(const AttnMaps &maps, const AttnParams &p, int batch, cudaStream_t stream) {
     using T = AttnTile<D>;
-    auto kern = attn_decode_kernel<D, MODE, SCORES>;
+    auto kern = attn_decode_kernel<D, MODE, SCORES, CLUSTER>;
     // The shared-memory opt-in is a per-device function attribute: set it once per device.
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -492,21 +614,45 @@ static cudaError_t launch_one(const AttnMaps &maps, const AttnParams &p, int bat
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
-    dim3 grid(p.splits, p.hkv, batch);
-    kern<<<grid, kAttnThreads, T::kSmemBytes, stream>>>(maps.pool_k, maps.pool_v, maps.comp_k, maps.comp_v, p);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(p.splits, p.hkv, batch);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n_attr = 1;
+    if (CLUSTER) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = p.splits;  // the splits of one unit form one cluster
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n_attr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    e = cudaLaunchKernelEx(&cfg, kern, maps.pool_k, maps.pool_v, maps.comp_k, maps.comp_v, p);
+    if (e != cudaSuccess) return e;
     return cudaGetLastError();
+}
+
+template <int D, bool CLUSTER>
+static cudaError_t launch_mode(int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p, int batch,
+                               cudaStream_t stream) {
+    if (mode == kModeFast) return launch_one<D, kModeFast, false, CLUSTER>(maps, p, batch, stream);
+    if (with_scores) return launch_one<D, kModeDense, true, CLUSTER>(maps, p, batch, stream);
+    return launch_one<D, kModeDense, false, CLUSTER>(maps, p, batch, stream);
 }
 
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream) {
-    if (head_dim == 128) {
-        if (mode == kModeFast) return launch_one<128, kModeFast, false>(maps, p, batch, stream);
-        if (with_scores) return launch_one<128, kModeDense, true>(maps, p, batch, stream);
-        return launch_one<128, kModeDense, false>(maps, p, batch, stream);
-    }
-    if (mode == kModeFast) return launch_one<64, kModeFast, false>(maps, p, batch, stream);
-    if (with_scores) return launch_one<64, kModeDense, true>(maps, p, batch, stream);
-    return launch_one<64, kModeDense, false>(maps, p, batch, stream);
+    const bool cluster = p.splits > 1 && p.splits <= kMaxClusterSplits;
+    if (head_dim == 128)
+        return cluster ? launch_mode<128, true>(mode, with_scores, maps, p, batch, stream)
+                       : launch_mode<128, false>(mode, with_scores, maps, p, batch, stream);
+    return cluster ? launch_mode<64, true>(mode, with_scores, maps, p, batch, stream)
+                   : launch_mode<64, false>(mode, with_scores, maps, p, batch, stream);
 }
 
 }  // namespace sfi

@@ -47,9 +47,10 @@ sfi_status scratch_address(void **out) {
 
 extern "C" sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
                                                    const sfi_compact_kv *compact, int32_t sink, int32_t recent,
-                                                   const void *q, float *out, float *lse, const int32_t *req_ids,
+                                                   const void *q, const void *k_new, const void *v_new, float *out,
+                                                   float *lse, const int32_t *req_ids,
                                                    int32_t batch, int32_t max_tokens, int32_t num_splits,
-                                                   int32_t *dev_status, void *stream) {
+                                                   uint32_t flags, int32_t *dev_status, void *stream) {
     if (!shape || batch < 0 || num_splits < 0) return SFI_ERR_INVALID_ARG;
     const size_t need = sfi_workspace_size(shape, batch, max_tokens, num_splits);
     if (need > kScratchBytes) return SFI_ERR_WORKSPACE;  // the plan needs more than the fixed scratch
@@ -67,6 +68,6 @@ extern "C" sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, 
                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return SFI_ERR_CUDA;
     }
-    return sfi_fast_decode_attn(shape, kv, compact, sink, recent, q, out, lse, req_ids, batch, max_tokens,
-                                num_splits, scratch, kScratchBytes, dev_status, stream);
+    return sfi_fast_decode_attn(shape, kv, compact, sink, recent, q, k_new, v_new, out, lse, req_ids, batch,
+                                max_tokens, num_splits, flags, scratch, kScratchBytes, dev_status, stream);
 }

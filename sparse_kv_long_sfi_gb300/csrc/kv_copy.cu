@@ -17,6 +17,8 @@ namespace sfi {
 
 constexpr int kCopyThreads = 256;
 constexpr int kCompactRowsPerCta = 64;
+// Requests handled by one compaction launch (the chunk prefix lives in shared memory).
+constexpr int kCompactMaxBatch = 2048;
 
 __device__ __forceinline__ int4 ld_nc_v4(const void *p) {
     int4 v;
@@ -59,71 +61,145 @@ __global__ void __launch_bounds__(kCopyThreads) paged_append_kernel(const CopyPa
     }
 }
 
-template <int D>
-__global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const CopyParams p) {
-    constexpr int kChunks = D / 8;
-    constexpr int kThreadsPerRow = 2 * kChunks;  // K chunks then V chunks
-    constexpr int kRowsPerIter = kCopyThreads / kThreadsPerRow;
-    constexpr int kIters = kCompactRowsPerCta / kRowsPerIter;
-    const int kvh = blockIdx.y, b = blockIdx.z;
-    const int r = p.req_ids ? p.req_ids[b] : b;
+// Rows a request's compaction writes per KV head: the sink [0, min(S, L)) and, when
+// L >= S, the selection [S, S + count). -1 marks a request with invalid arguments
+// (the reason is ORed into *err).
+__device__ __forceinline__ int compact_rows(const CopyParams &p, int r, uint32_t *err) {
     const int L = p.seq_lens[r];
-    const bool lead = threadIdx.x == 0 && blockIdx.x == 0 && kvh == 0;
     if (L < 1 || L > p.max_pages * kSubTokens) {
-        if (lead) report(p.dev_status, SFI_DEV_BAD_LEN);
-        return;
+        *err |= SFI_DEV_BAD_LEN;
+        return -1;
     }
     const int cnt = p.count[r];
     const int cap = p.c_capacity[r];
     const int64_t off = p.c_row_offset[r];
     if (cnt < 0 || cnt > p.k_cap || p.sink + cnt > cap || (cnt > 0 && L < p.sink)) {
-        if (lead) report(p.dev_status, SFI_DEV_K_OVERFLOW);
-        return;
+        *err |= SFI_DEV_K_OVERFLOW;
+        return -1;
     }
     if (off < 0 || off + (int64_t)p.hkv * cap > p.c_total_rows) {
-        if (lead) report(p.dev_status, SFI_DEV_BAD_COMPACT);
-        return;
+        *err |= SFI_DEV_BAD_COMPACT;
+        return -1;
     }
-    const int ns = min(p.sink, L);
-    const int sub = threadIdx.x / kThreadsPerRow;
-    const int c = threadIdx.x - sub * kThreadsPerRow;
-    const bool is_v = c >= kChunks;
-    const int chunk = is_v ? c - kChunks : c;
-    const __nv_bfloat16 *pool = is_v ? p.v_pool_src : p.k_pool_src;
-    __nv_bfloat16 *dst_base = (is_v ? p.cv : p.ck) + (off + (int64_t)kvh * cap) * D + chunk * 8;
-    const int32_t *sel = p.idx + ((int64_t)r * p.hkv + kvh) * p.k_cap;
-    const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+    return L < p.sink ? L : p.sink + cnt;
+}
 
-    int4 vals[kIters];
-    int rows[kIters];
+// Persistent grid: every CTA derives the same list of 64-row chunks from the device
+// counts (an exclusive prefix over the launch's requests, in shared memory) and walks
+// it with a grid stride, so the work follows the rows actually selected, not k_cap.
+template <int D>
+__global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const CopyParams p, int b_begin, int nb) {
+    constexpr int kChunks = D / 8;
+    constexpr int kThreadsPerRow = 2 * kChunks;  // K chunks then V chunks
+    constexpr int kRowsPerIter = kCopyThreads / kThreadsPerRow;
+    constexpr int kIters = kCompactRowsPerCta / kRowsPerIter;
+    constexpr int kWarps = kCopyThreads / 32;
+    __shared__ int s_prefix[kCompactMaxBatch];  // first chunk of each request entry
+    __shared__ int s_rows[kCompactMaxBatch];    // rows per KV head of each request entry
+    __shared__ int s_warp[kWarps];
+    __shared__ int s_total;
+
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    uint32_t err = 0;
+    int carry = 0;
+    for (int base = 0; base < nb; base += kCopyThreads) {
+        const int b = base + tid;
+        int c = 0, rows = -1;
+        if (b < nb) {
+            const int r = p.req_ids ? p.req_ids[b_begin + b] : b_begin + b;
+            rows = compact_rows(p, r, &err);
+            c = rows > 0 ? p.hkv * ((rows + kCompactRowsPerCta - 1) / kCompactRowsPerCta) : 0;
+        }
+        int incl = c;
 #pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-        const int i = blockIdx.x * kCompactRowsPerCta + it * kRowsPerIter + sub;
-        int pos = -1;
-        if (i < ns) {
-            pos = i;
-        } else if (i >= p.sink && i < p.sink + cnt) {
-            pos = sel[i - p.sink];
-            if (pos < 0 || pos >= L) {
-                report(p.dev_status, SFI_DEV_BAD_INDEX);
-                pos = -1;
-            }
+        for (int off = 1; off < 32; off <<= 1) {
+            const int v = __shfl_up_sync(0xffffffffu, incl, off);
+            if (lane >= off) incl += v;
         }
-        rows[it] = -1;
-        if (pos >= 0) {
-            const int page = ptab[pos / kSubTokens];
-            if (page < 0 || page >= p.num_pages) {
-                report(p.dev_status, SFI_DEV_BAD_PAGE);
-            } else {
-                vals[it] = ld_nc_v4(pool + (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D +
-                                    chunk * 8);
-                rows[it] = i;
+        if (lane == 31) s_warp[warp] = incl;
+        __syncthreads();
+        if (warp == 0) {
+            const int w = lane < kWarps ? s_warp[lane] : 0;
+            int wi = w;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int v = __shfl_up_sync(0xffffffffu, wi, off);
+                if (lane >= off) wi += v;
             }
+            if (lane < kWarps) s_warp[lane] = wi - w;
+            if (lane == 31) s_total = wi;
         }
+        __syncthreads();
+        if (b < nb) {
+            s_prefix[b] = carry + s_warp[warp] + incl - c;
+            s_rows[b] = rows;
+        }
+        carry += s_total;
+        __syncthreads();
     }
+    if (err && blockIdx.x == 0) report(p.dev_status, err);
+    const int total = carry;
+
+    const int sub = tid / kThreadsPerRow;
+    const int cc = tid - sub * kThreadsPerRow;
+    const bool is_v = cc >= kChunks;
+    const int chunk = is_v ? cc - kChunks : cc;
+    const __nv_bfloat16 *pool = is_v ? p.v_pool_src : p.k_pool_src;
+    for (int work = blockIdx.x; work < total; work += gridDim.x) {
+        // request entry owning this chunk: the last b with s_prefix[b] <= work (an entry
+        // without chunks shares its prefix with the next entry, so it is never the last)
+        int lo = 0, hi = nb - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (s_prefix[mid] <= work) lo = mid; else hi = mid - 1;
+        }
+        const int b = lo;
+        const int r = p.req_ids ? p.req_ids[b_begin + b] : b_begin + b;
+        const int rows = s_rows[b];
+        const int per_head = (rows + kCompactRowsPerCta - 1) / kCompactRowsPerCta;
+        const int within = work - s_prefix[b];
+        const int kvh = within / per_head;
+        const int row0 = (within - kvh * per_head) * kCompactRowsPerCta;
+        const int L = p.seq_lens[r];
+        const int ns = min(p.sink, L);
+        const int cnt = p.count[r];
+        const int cap = p.c_capacity[r];
+        const int64_t off = p.c_row_offset[r];
+        __nv_bfloat16 *dst_base = (is_v ? p.cv : p.ck) + (off + (int64_t)kvh * cap) * D + chunk * 8;
+        const int32_t *sel = p.idx + ((int64_t)r * p.hkv + kvh) * p.k_cap;
+        const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+
+        int4 vals[kIters];
+        int dst_row[kIters];
 #pragma unroll
-    for (int it = 0; it < kIters; ++it)
-        if (rows[it] >= 0) st_v4(dst_base + (int64_t)rows[it] * D, vals[it]);
+        for (int it = 0; it < kIters; ++it) {
+            const int i = row0 + it * kRowsPerIter + sub;
+            int pos = -1;
+            if (i < ns) {
+                pos = i;
+            } else if (i >= p.sink && i < p.sink + cnt) {
+                pos = sel[i - p.sink];
+                if (pos < 0 || pos >= L) {
+                    report(p.dev_status, SFI_DEV_BAD_INDEX);
+                    pos = -1;
+                }
+            }
+            dst_row[it] = -1;
+            if (pos >= 0) {
+                const int page = ptab[pos / kSubTokens];
+                if (page < 0 || page >= p.num_pages) {
+                    report(p.dev_status, SFI_DEV_BAD_PAGE);
+                } else {
+                    vals[it] = ld_nc_v4(pool + (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D +
+                                        chunk * 8);
+                    dst_row[it] = i;
+                }
+            }
+        }
+#pragma unroll
+        for (int it = 0; it < kIters; ++it)
+            if (dst_row[it] >= 0) st_v4(dst_base + (int64_t)dst_row[it] * D, vals[it]);
+    }
 }
 
 cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t stream) {
@@ -135,12 +211,22 @@ cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t str
 }
 
 cudaError_t launch_compact_gather(const CopyParams &p, int batch, int max_rows, cudaStream_t stream) {
-    dim3 grid((max_rows + kCompactRowsPerCta - 1) / kCompactRowsPerCta, p.hkv, batch);
-    if (p.head_dim == 128)
-        compact_gather_kernel<128><<<grid, kCopyThreads, 0, stream>>>(p);
-    else
-        compact_gather_kernel<64><<<grid, kCopyThreads, 0, stream>>>(p);
-    return cudaGetLastError();
+    (void)max_rows;  // the grid follows the device counts
+    int dev = 0, sms = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    const int grid = sms * 6;  // enough 32 KB chunks in flight to saturate HBM
+    for (int b0 = 0; b0 < batch; b0 += kCompactMaxBatch) {
+        const int nb = batch - b0 < kCompactMaxBatch ? batch - b0 : kCompactMaxBatch;
+        if (p.head_dim == 128)
+            compact_gather_kernel<128><<<grid, kCopyThreads, 0, stream>>>(p, b0, nb);
+        else
+            compact_gather_kernel<64><<<grid, kCopyThreads, 0, stream>>>(p, b0, nb);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace sfi

@@ -7,17 +7,19 @@
 // Design: one CTA of 1024 threads per (request, KV head).
 //  * Scores are mapped to order-preserving uint32 keys (-0 -> +0, NaN -> 0, below
 //    -inf).
+//  * The candidates are walked in rounds of 16384 positions; in a round, warp w owns
+//    the contiguous positions [512 w, 512 w + 512) and lane l holds positions
+//    512 w + 32 j + l, j < 16, loaded together (16 independent coalesced loads per
+//    thread). With at most one round (|C| <= 16384) the keys stay in registers for
+//    the whole selection: the scores are read from memory once.
 //  * Radix select, 4 passes of 8 bits from the top: a 256-bin shared histogram of the
 //    keys that share the current prefix (warp-aggregated atomics via match.any),
 //    then one warp scans the bins from the top to find the bin holding the k-th key.
 //    The result is the exact k-th largest key tau and the number of keys equal to
 //    tau that must be taken (the lowest positions among them).
-//  * Output in ascending position order without sorting: each warp owns a
-//    contiguous range of candidates; a counting pass gives per-warp (above tau,
-//    equal tau) totals, a scan gives each warp's output offset and tie rank, and a
-//    second pass writes positions with ballot/popc prefix counts.
-// The candidates of a slow step are a few K to 128K floats, read from L2 for every
-// pass after the first.
+//  * Output in ascending position order without sorting: per (round, warp) counts of
+//    keys above / equal to tau, an exclusive scan over (round, warp) in position
+//    order, then each warp writes its taken positions with ballot/popc ranks.
 #include "sfi_device.cuh"
 #include "sfi_internal.h"
 
@@ -25,6 +27,10 @@ namespace sfi {
 
 constexpr int kTopkThreads = 1024;
 constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkPerThread = 16;                               // keys per thread and round
+constexpr int kTopkRound = kTopkThreads * kTopkPerThread;        // 16384 positions per round
+constexpr int kTopkMaxRounds = 16;                               // |C| up to 262144
+constexpr uint32_t kNoKey = 0xffffffffu;                         // marks positions past |C| (never counted)
 
 __device__ __forceinline__ uint32_t order_key(float x) {
     uint32_t u = __float_as_uint(x);
@@ -33,10 +39,35 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
+// Keys of one round for this thread: position base + 512 * warp + 32 * j + lane.
+__device__ __forceinline__ void load_round(const float *row, int n, int base, int warp, int lane,
+                                           uint32_t (&key)[kTopkPerThread]) {
+#pragma unroll
+    for (int j = 0; j < kTopkPerThread; ++j) {
+        const int i = base + warp * (32 * kTopkPerThread) + 32 * j + lane;
+        key[j] = i < n ? order_key(__ldg(row + i)) : kNoKey;
+    }
+}
+
+// Add this thread's keys that share `prefix` under `mask` to the histogram of bits [shift, shift+8).
+__device__ __forceinline__ void histogram_round(const uint32_t (&key)[kTopkPerThread], uint32_t prefix, uint32_t mask,
+                                                int shift, int lane, uint32_t *hist) {
+#pragma unroll
+    for (int j = 0; j < kTopkPerThread; ++j) {
+        const bool in = key[j] != kNoKey && (key[j] & mask) == prefix;
+        const uint32_t bin = (key[j] >> shift) & 255u;
+        const uint32_t active = __ballot_sync(0xffffffffu, in);
+        if (in) {
+            const uint32_t same = __match_any_sync(active, bin);
+            if ((same & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[bin], (uint32_t)__popc(same));
+        }
+    }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p) {
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_bin, s_rem;
-    __shared__ int32_t w_gt[kTopkWarps], w_eq[kTopkWarps];
+    __shared__ int32_t s_gt[kTopkMaxRounds * kTopkWarps], s_eq[kTopkMaxRounds * kTopkWarps];
 
     const int kvh = blockIdx.x, b = blockIdx.y;
     const int r = p.req_ids ? p.req_ids[b] : b;
@@ -48,7 +79,8 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     }
     const int n = max(0, L - p.recent - p.sink);  // |C|, C = [S, L - W)
     const int k = p.k_per_req[r];
-    if (k < 0 || k > p.k_cap) {
+    const int rounds = (n + kTopkRound - 1) / kTopkRound;
+    if (k < 0 || k > p.k_cap || rounds > kTopkMaxRounds) {
         if (tid == 0 && kvh == 0) report(p.dev_status, SFI_DEV_K_OVERFLOW);
         return;
     }
@@ -62,25 +94,21 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
         return;
     }
 
+    uint32_t key[kTopkPerThread];
+    if (rounds == 1) load_round(row, n, 0, warp, lane, key);  // resident for the whole selection
+
     // ---- radix select of the keff-th largest key ----
     uint32_t prefix = 0u, mask = 0u;
     uint32_t rem = (uint32_t)keff;  // how many still to take inside the current prefix
     for (int shift = 24; shift >= 0; shift -= 8) {
         for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
         __syncthreads();
-        const int n_round = (n + 31) & ~31;  // whole warps iterate together for match.any
-        for (int i = tid; i < n_round; i += kTopkThreads) {
-            bool in = false;
-            uint32_t bin = 0u;
-            if (i < n) {
-                const uint32_t key = order_key(__ldg(row + i));
-                in = (key & mask) == prefix;
-                bin = (key >> shift) & 255u;
-            }
-            const uint32_t active = __ballot_sync(0xffffffffu, in);
-            if (in) {
-                const uint32_t same = __match_any_sync(active, bin);
-                if ((same & ((1u << lane) - 1u)) == 0u) atomicAdd(&hist[bin], (uint32_t)__popc(same));
+        if (rounds == 1) {
+            histogram_round(key, prefix, mask, shift, lane, hist);
+        } else {
+            for (int rd = 0; rd < rounds; ++rd) {
+                load_round(row, n, rd * kTopkRound, warp, lane, key);
+                histogram_round(key, prefix, mask, shift, lane, hist);
             }
         }
         __syncthreads();
@@ -124,54 +152,61 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     const uint32_t tau = prefix;
     const int take_eq = (int)rem;  // keys equal to tau to take, lowest positions first
 
-    // ---- ascending output ----
-    const int per_warp = (((n + kTopkWarps - 1) / kTopkWarps) + 31) & ~31;
-    const int w_lo = warp * per_warp;
-    const int w_hi = min(n, w_lo + per_warp);
-    int gt = 0, eq = 0;
-    for (int base = w_lo; base < w_hi; base += 32) {
-        const int i = base + lane;
-        uint32_t key = 0u;
-        if (i < w_hi) key = order_key(__ldg(row + i));
-        const bool valid = i < w_hi;
-        gt += __popc(__ballot_sync(0xffffffffu, valid && key > tau));
-        eq += __popc(__ballot_sync(0xffffffffu, valid && key == tau));
-    }
-    if (lane == 0) {
-        w_gt[warp] = gt;
-        w_eq[warp] = eq;
-    }
-    __syncthreads();
-    if (warp == 0) {
-        int a = w_gt[lane], e = w_eq[lane];
+    // ---- ascending output: counts per (round, warp), scan, then ranked writes ----
+    for (int rd = 0; rd < rounds; ++rd) {
+        if (rounds > 1) load_round(row, n, rd * kTopkRound, warp, lane, key);
+        int gt = 0, eq = 0;
 #pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const int va = __shfl_up_sync(0xffffffffu, a, off);
-            const int ve = __shfl_up_sync(0xffffffffu, e, off);
-            if (lane >= off) {
-                a += va;
-                e += ve;
-            }
+        for (int j = 0; j < kTopkPerThread; ++j) {
+            gt += __popc(__ballot_sync(0xffffffffu, key[j] != kNoKey && key[j] > tau));
+            eq += __popc(__ballot_sync(0xffffffffu, key[j] == tau));
         }
-        w_gt[lane] = a - w_gt[lane];  // exclusive
-        w_eq[lane] = e - w_eq[lane];
+        if (lane == 0) {
+            s_gt[rd * kTopkWarps + warp] = gt;
+            s_eq[rd * kTopkWarps + warp] = eq;
+        }
     }
     __syncthreads();
-    int eq_before = w_eq[warp];
-    int out_pos = w_gt[warp] + min(eq_before, take_eq);
+    if (warp == 0) {  // exclusive scan over (round, warp) in position order
+        int carry_gt = 0, carry_eq = 0;
+        for (int base = 0; base < rounds * kTopkWarps; base += 32) {
+            const int a0 = s_gt[base + lane], e0 = s_eq[base + lane];
+            int a = a0, e = e0;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int va = __shfl_up_sync(0xffffffffu, a, off);
+                const int ve = __shfl_up_sync(0xffffffffu, e, off);
+                if (lane >= off) {
+                    a += va;
+                    e += ve;
+                }
+            }
+            s_gt[base + lane] = carry_gt + a - a0;
+            s_eq[base + lane] = carry_eq + e - e0;
+            carry_gt += __shfl_sync(0xffffffffu, a, 31);
+            carry_eq += __shfl_sync(0xffffffffu, e, 31);
+        }
+    }
+    __syncthreads();
     const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int base = w_lo; base < w_hi; base += 32) {
-        const int i = base + lane;
-        const bool valid = i < w_hi;
-        const uint32_t key = valid ? order_key(__ldg(row + i)) : 0u;
-        const bool is_eq = valid && key == tau;
-        const uint32_t eq_bal = __ballot_sync(0xffffffffu, is_eq);
-        const int eq_rank = eq_before + __popc(eq_bal & lt_mask);
-        const bool take = valid && (key > tau || (is_eq && eq_rank < take_eq));
-        const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
-        if (take) out[out_pos + __popc(take_bal & lt_mask)] = p.sink + i;
-        out_pos += __popc(take_bal);
-        eq_before += __popc(eq_bal);
+    for (int rd = 0; rd < rounds; ++rd) {
+        if (rounds > 1) load_round(row, n, rd * kTopkRound, warp, lane, key);
+        int eq_before = s_eq[rd * kTopkWarps + warp];
+        int out_pos = s_gt[rd * kTopkWarps + warp] + min(eq_before, take_eq);
+#pragma unroll
+        for (int j = 0; j < kTopkPerThread; ++j) {
+            const bool valid = key[j] != kNoKey;
+            const bool is_eq = valid && key[j] == tau;
+            const uint32_t eq_bal = __ballot_sync(0xffffffffu, is_eq);
+            const int eq_rank = eq_before + __popc(eq_bal & lt_mask);
+            const bool take = valid && (key[j] > tau || (is_eq && eq_rank < take_eq));
+            const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
+            if (take)
+                out[out_pos + __popc(take_bal & lt_mask)] =
+                    p.sink + rd * kTopkRound + warp * (32 * kTopkPerThread) + 32 * j + lane;
+            out_pos += __popc(take_bal);
+            eq_before += __popc(eq_bal);
+        }
     }
 }
 

@@ -82,26 +82,28 @@ sfi_status check_paged(const sfi_attn_shape *s, const sfi_paged_kv *kv) {
     return SFI_OK;
 }
 
+// Split-KV plan of one attention launch. Automatic plans fill one wave of resident
+// CTAs (two per SM) and keep at least four full stages of sub-blocks per split; an
+// explicit request is honoured down to two stages per split. Plans of up to
+// kMaxClusterSplits merge inside a thread-block cluster (no workspace).
 int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_count) {
     constexpr int kMaxSplits = 256;
     if (units <= 0) return 1;
-    int by_tokens = kMaxSplits;
-    if (max_tokens > 0) {
-        // at least two full stages of sub-blocks per split
-        const int nb = (max_tokens + sfi::kSubTokens - 1) / sfi::kSubTokens + 1;
-        by_tokens = std::max(1, nb / (2 * sfi::kConsumerWarps));
-    }
+    const int nb = max_tokens > 0 ? (max_tokens + sfi::kSubTokens - 1) / sfi::kSubTokens + 1 : 0;
     int s;
     if (requested > 0) {
         s = requested;
-    } else if (max_tokens <= 0) {
+        if (nb > 0) s = std::min(s, std::max(1, nb / (2 * sfi::kConsumerWarps)));
+    } else if (nb == 0) {
         s = 1;
     } else {
-        // one wave of resident CTAs: every split of every unit is on an SM at once
         s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm / units);
+        s = std::min(s, std::max(1, nb / (4 * sfi::kConsumerWarps)));
     }
-    return std::max(1, std::min({s, by_tokens, kMaxSplits}));
+    return std::max(1, std::min(s, kMaxSplits));
 }
+
+bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
 
 float resolve_scale(const sfi_attn_shape *s) {
     return s->softmax_scale > 0.f ? s->softmax_scale : 1.0f / std::sqrt((float)s->head_dim);
@@ -131,13 +133,17 @@ void fill_common(AttnParams &p, const sfi_attn_shape *s, const sfi_paged_kv *kv,
     p.scale = resolve_scale(s);
     p.scale_log2 = p.scale * 1.4426950408889634f;
     p.dev_status = dev_status;
+    p.k_new = nullptr;
+    p.v_new = nullptr;
+    p.k_pool_w = static_cast<__nv_bfloat16 *>(kv->k_pool);
+    p.v_pool_w = static_cast<__nv_bfloat16 *>(kv->v_pool);
 }
 
 sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, size_t ws_bytes) {
     p.ws_count = nullptr;
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
-    if (p.splits <= 1) return SFI_OK;
+    if (!needs_workspace(p.splits)) return SFI_OK;
     const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim);
     if (!ws || ws_bytes < l.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SFI_ERR_WORKSPACE;
     char *base = static_cast<char *>(ws);
@@ -171,7 +177,7 @@ int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_
 
 size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits) {
     const int32_t s = sfi_plan_splits(shape, batch, max_tokens, num_splits);
-    if (s <= 1) return 0;
+    if (!needs_workspace(s)) return 0;
     return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, s, shape->head_dim).total;
 }
 
@@ -201,8 +207,9 @@ sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_paged_kv *
 }
 
 sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
-                                int32_t sink, int32_t recent, const void *q, float *out, float *lse,
-                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits,
+                                int32_t sink, int32_t recent, const void *q, const void *k_new, const void *v_new,
+                                float *out, float *lse,
+                                const int32_t *req_ids, int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
                                 void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream) {
     sfi_status st = check_shape(shape);
     if (st != SFI_OK) return st;
@@ -214,8 +221,13 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
         return SFI_ERR_INVALID_ARG;
     if (compact->total_rows >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
     if (batch == 0) return SFI_OK;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return SFI_ERR_INVALID_ARG;
     AttnParams p{};
     fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
     p.c_row_offset = compact->row_offset;
     p.c_capacity = compact->capacity;
     p.c_count = compact->count;
@@ -237,9 +249,10 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
 }
 
 sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
-                                           int32_t recent, const void *q, float *out, float *lse, float *scores,
+                                           int32_t recent, const void *q, const void *k_new, const void *v_new,
+                                           float *out, float *lse, float *scores,
                                            int64_t score_stride, const int32_t *req_ids, int32_t batch,
-                                           int32_t max_tokens, int32_t num_splits, void *workspace,
+                                           int32_t max_tokens, int32_t num_splits, uint32_t flags, void *workspace,
                                            size_t workspace_bytes, int32_t *dev_status, void *stream) {
     sfi_status st = check_shape(shape);
     if (st != SFI_OK) return st;
@@ -248,8 +261,13 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
         return SFI_ERR_INVALID_ARG;
     if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
     if (batch == 0) return SFI_OK;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return SFI_ERR_INVALID_ARG;
     AttnParams p{};
     fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
     p.scores = scores;
     p.score_stride = score_stride;
     const int64_t units = (int64_t)batch * shape->num_kv_heads;

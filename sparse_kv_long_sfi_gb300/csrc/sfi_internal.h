@@ -19,6 +19,9 @@ constexpr int kConsumerWarps = 4;
 constexpr int kMaxGroup = 8;
 // Attention CTAs resident per SM (shared memory sized for this).
 constexpr int kAttnCtasPerSm = 2;
+// Splits of one unit that merge inside a thread-block cluster (portable cluster size);
+// more splits merge through the global workspace.
+constexpr int kMaxClusterSplits = 8;
 
 enum AttnMode : int { kModeFast = 0, kModeDense = 1 };
 
@@ -42,6 +45,12 @@ struct AttnParams {
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
     int32_t splits;
+    int32_t early_prefetch;  // SFI_ATTN_EARLY_KV_PREFETCH: stream KV before the dependency wait
+    // fused append of the current token (position L - 1), or null
+    const __nv_bfloat16 *k_new;  // [B][Hkv][D]
+    const __nv_bfloat16 *v_new;
+    __nv_bfloat16 *k_pool_w;     // the paged pools, for the append's writes
+    __nv_bfloat16 *v_pool_w;
     int32_t *ws_count;  // [units]
     float *ws_ml;       // [units][splits][8][2]
     float *ws_part;     // [units][splits][8][D]

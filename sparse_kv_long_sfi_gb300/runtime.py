@@ -17,8 +17,8 @@ from typing import List, Optional
 import numpy as np
 import torch
 
-from .api import (AttnShape, CompactKV, PagedKV, alloc_workspace, sfi_compact_gather, sfi_fast_decode_attn,
-                  sfi_paged_kv_append, sfi_select_topk, sfi_slow_dense_attn_with_scores)
+from .api import (SFI_ATTN_EARLY_KV_PREFETCH, AttnShape, CompactKV, PagedKV, alloc_workspace, sfi_compact_gather,
+                  sfi_fast_decode_attn, sfi_paged_kv_append, sfi_select_topk, sfi_slow_dense_attn_with_scores)
 
 
 class SlowFastSchedule:
@@ -116,8 +116,12 @@ class SFIDecoder:
 
     def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
                  max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
-                 main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None):
+                 main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None,
+                 fuse_append: bool = True):
         self.shape, self.layers, self.batch = shape, layers, batch
+        # fuse_append: the attention kernels write the current token into the pages
+        # themselves (no separate append launch per layer)
+        self.fuse_append = bool(fuse_append)
         self.sink, self.recent = int(sink), int(recent)
         self.max_len = int(max_len)
         B = batch.page_table.shape[0]
@@ -132,6 +136,11 @@ class SFIDecoder:
         self.e_attn = [torch.cuda.Event() for _ in layers]
         self.e_aux = [torch.cuda.Event() for _ in layers]
         self.pending = [False] * len(layers)
+        # Consecutive attention launches on the main stream touch different layers (or,
+        # within a mixed step, different requests' pages): each may stream its KV while
+        # the previous one finishes. The separate-append path writes the pages right
+        # before the attention, so it keeps the conservative launch.
+        self.attn_flags = SFI_ATTN_EARLY_KV_PREFETCH if self.fuse_append else 0
         # Optional instrumentation: called as timer(kind, "start"|"end", stream) around
         # each attention launch (kind "slow", "fast" or "dense"), e.g. to record events.
         self.timer = None
@@ -144,6 +153,32 @@ class SFIDecoder:
         L = self.layers[i]
         return PagedKV(L.k_pool, L.v_pool, self.batch.page_table, seq_lens)
 
+    def _append(self, i, kv, io, append, req_ids, n):
+        """The current token of layer i: returned for the attention kernel to write
+        (fused), or written now by the paged-append kernel."""
+        if not append:
+            return None, None
+        if self.fuse_append:
+            return io.k_new[i], io.v_new[i]
+        sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], req_ids=req_ids, batch=n,
+                            dev_status=self.dev_status, stream=self.main)
+        return None, None
+
+    def _enter(self):
+        """Order the main stream after the caller's stream (inputs such as seq_lens, q or
+        k_new may have just been written there; torch streams do not synchronise with
+        each other implicitly)."""
+        cur = torch.cuda.current_stream(self.main.device)
+        if cur != self.main:
+            self.main.wait_stream(cur)
+
+    def _leave(self):
+        """Order the caller's stream after the main stream (outputs, and reuse of the
+        input tensors' memory by the caching allocator)."""
+        cur = torch.cuda.current_stream(self.main.device)
+        if cur != self.main:
+            cur.wait_stream(self.main)
+
     def _wait_aux(self, i: int):
         if self.pending[i]:
             self.main.wait_event(self.e_aux[i])
@@ -152,17 +187,17 @@ class SFIDecoder:
     def slow_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
                   append: bool = True):
         n = None if req_ids is None else req_ids.numel()
+        self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
-            if append:
-                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], req_ids=req_ids, batch=n,
-                                    dev_status=self.dev_status, stream=self.main)
+            kn, vn = self._append(i, kv, io, append, req_ids, n)
             self._mark("slow", "start")
             sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
-                                            None if io.lse is None else io.lse[i], L.scores, req_ids=req_ids,
-                                            batch=n, max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
-                                            dev_status=self.dev_status, stream=self.main)
+                                            None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
+                                            req_ids=req_ids, batch=n, max_tokens=self.max_dense_tokens,
+                                            workspace=self.ws_dense, dev_status=self.dev_status, stream=self.main,
+                                            flags=self.attn_flags)
             self._mark("slow", "end")
             self.e_attn[i].record(self.main)
             self.aux.wait_event(self.e_attn[i])
@@ -173,42 +208,43 @@ class SFIDecoder:
                                batch=n, dev_status=self.dev_status, stream=self.aux)
             self.e_aux[i].record(self.aux)
             self.pending[i] = True
+        self._leave()
 
     def fast_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
                   append: bool = True):
         n = None if req_ids is None else req_ids.numel()
+        self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
-            if append:
-                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], req_ids=req_ids, batch=n,
-                                    dev_status=self.dev_status, stream=self.main)
+            kn, vn = self._append(i, kv, io, append, req_ids, n)
             self._mark("fast", "start")
             sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
-                                 None if io.lse is None else io.lse[i], req_ids=req_ids, batch=n,
-                                 max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
-                                 dev_status=self.dev_status, stream=self.main)
+                                 None if io.lse is None else io.lse[i], k_new=kn, v_new=vn, req_ids=req_ids,
+                                 batch=n, max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
+                                 dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
             self._mark("fast", "end")
+        self._leave()
 
     def mixed_step(self, io: StepIO, seq_lens: torch.Tensor, slow_ids: torch.Tensor, fast_ids: torch.Tensor):
         """One step where each request is slow or fast (ASPIRE-style mixed batch, two launches per layer)."""
         ns, nf = slow_ids.numel(), fast_ids.numel()
+        self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
-            sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], dev_status=self.dev_status,
-                                stream=self.main)
+            kn, vn = self._append(i, kv, io, True, None, None)
             if nf:
                 sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
-                                     None if io.lse is None else io.lse[i], req_ids=fast_ids, batch=nf,
-                                     max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
-                                     dev_status=self.dev_status, stream=self.main)
+                                     None if io.lse is None else io.lse[i], k_new=kn, v_new=vn, req_ids=fast_ids,
+                                     batch=nf, max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
+                                     dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
             if ns:
                 sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
-                                                None if io.lse is None else io.lse[i], L.scores, req_ids=slow_ids,
-                                                batch=ns, max_tokens=self.max_dense_tokens,
+                                                None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
+                                                req_ids=slow_ids, batch=ns, max_tokens=self.max_dense_tokens,
                                                 workspace=self.ws_dense, dev_status=self.dev_status,
-                                                stream=self.main)
+                                                stream=self.main, flags=self.attn_flags)
                 self.e_attn[i].record(self.main)
                 self.aux.wait_event(self.e_attn[i])
                 sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,
@@ -218,22 +254,24 @@ class SFIDecoder:
                                    req_ids=slow_ids, batch=ns, dev_status=self.dev_status, stream=self.aux)
                 self.e_aux[i].record(self.aux)
                 self.pending[i] = True
+        self._leave()
 
     def dense_step(self, io: StepIO, seq_lens: torch.Tensor, append: bool = True):
         """Full-KV decode step (the baseline of the paper's Table 1)."""
+        self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
-            if append:
-                sfi_paged_kv_append(self.shape, kv, io.k_new[i], io.v_new[i], dev_status=self.dev_status,
-                                    stream=self.main)
+            kn, vn = self._append(i, kv, io, append, None, None)
             self._mark("dense", "start")
             sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
-                                            None if io.lse is None else io.lse[i], None,
+                                            None if io.lse is None else io.lse[i], None, k_new=kn, v_new=vn,
                                             max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
-                                            dev_status=self.dev_status, stream=self.main)
+                                            dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
             self._mark("dense", "end")
+        self._leave()
 
     def join(self):
-        """Make the main stream wait for all outstanding aux work."""
+        """Make the main stream (and the caller's stream) wait for all outstanding aux work."""
         for i in range(len(self.layers)):
             self._wait_aux(i)
+        self._leave()

@@ -73,8 +73,8 @@ def _paged(npages=4, maxp=4):
 def test_shape_validation_before_launch(libsfi, shape_args, expect):
     sh = _shape(*shape_args)
     kv = _paged()
-    st = libsfi.sfi_slow_dense_attn_with_scores(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, 8192, None, None,
-                                                0, None, 1, 0, 0, None, 0, None, None)
+    st = libsfi.sfi_slow_dense_attn_with_scores(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, None, None, 8192,
+                                                None, None, 0, None, 1, 0, 0, 0, None, 0, None, None)
     assert st == expect
 
 
@@ -86,10 +86,13 @@ def test_null_and_negative_arguments(libsfi):
     assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(kv), None, 4096, None, 1, None, None) == 1
     assert libsfi.sfi_paged_kv_append(ctypes.byref(sh), ctypes.byref(kv), 4097, 4096, None, 1, None, None) == 1
     comp = _abi.sfi_compact_kv(4096, 4096, 100, 4096, 4096, 4096)
-    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), ctypes.byref(comp), -1, 32, 4096, 4096,
-                                       None, None, 1, 0, 0, None, 0, None, None) == 1
-    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), None, 4, 32, 4096, 4096,
-                                       None, None, 1, 0, 0, None, 0, None, None) == 1
+    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), ctypes.byref(comp), -1, 32, 4096, None,
+                                       None, 4096, None, None, 1, 0, 0, 0, None, 0, None, None) == 1
+    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), None, 4, 32, 4096, None, None, 4096,
+                                       None, None, 1, 0, 0, 0, None, 0, None, None) == 1
+    # k_new without v_new
+    assert libsfi.sfi_fast_decode_attn(ctypes.byref(sh), ctypes.byref(kv), ctypes.byref(comp), 4, 32, 4096, 4096,
+                                       None, 4096, None, None, 1, 0, 0, 0, None, 0, None, None) == 1
     assert libsfi.sfi_select_topk(None, 16, 8, 4096, 4, 32, 4096, 8, 4096, 4096, None, 1, None, None) == 1
     assert libsfi.sfi_select_topk(4096, 0, 8, 4096, 4, 32, 4096, 8, 4096, 4096, None, 1, None, None) == 1
     assert libsfi.sfi_compact_gather(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, -1, 4, ctypes.byref(comp),

@@ -389,3 +389,143 @@ def test_bad_selected_index_is_reported():
     sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, 4, comp, dev_status=st)
     torch.cuda.synchronize()
     assert st.item() & 8
+
+
+# ---------------------------------------------------------------------------
+# Fused append (k_new / v_new passed to the attention entry points)
+# ---------------------------------------------------------------------------
+def _grow(prob, g):
+    """Advance every request by one token: new lengths and seeded K/V for position L - 1."""
+    kn = syn.normal_bf16(g, (prob.B, prob.Hkv, prob.D))
+    vn = syn.normal_bf16(g, (prob.B, prob.Hkv, prob.D))
+    prob.set_lens(prob.lens + 1)
+    return kn, vn
+
+
+@pytest.mark.parametrize("W", [32, 0])
+def test_fused_append_dense_with_scores_matches_oracle(W):
+    """Slow step with the append fused: equals append-then-attend, scores included
+    (W = 0 puts the new token among the candidates), and the pages hold the token."""
+    sfi = _sfi()
+    lens = [1023, 40, 16, 1, 500]
+    prob = Problem(seed=61 + W, lens=lens, Hq=16, Hkv=8, D=128, S=4, W=W, extra_tokens=16).to_device()
+    kn, vn = _grow(prob, syn.rng(400, W))
+    stride = int(prob.lens.max())
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    out = torch.full((prob.B, 16, 128), float("nan"), device="cuda")
+    lse = torch.full((prob.B, 16), float("nan"), device="cuda")
+    ws = sfi.alloc_workspace(prob.shape, prob.B, stride + 16)
+    st = _status()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, W, prob.d_q, out, lse, scores,
+                                        k_new=dev_bf16(kn), v_new=dev_bf16(vn), max_tokens=stride + 16,
+                                        workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for r in range(prob.B):
+        oracle.paged_append(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], prob.lens[r], kn[r], vn[r],
+                            prob.Hkv, prob.D, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.v_pool), prob.kv.v_pool)
+    o, l, sc = out.cpu().numpy(), lse.cpu().numpy(), scores.cpu().numpy()
+    for r in range(prob.B):
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(o[r], o_ref, f"out r={r}")
+        assert_close(l[r], l_ref, f"lse r={r}")
+        L = prob.lens[r]
+        ref = prob.oracle_scores(r, stride)
+        masked = np.isneginf(ref[:, :L])
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+        err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
+        assert (err <= prob.score_bound(r, stride)[:, :L][~masked]).all()
+
+
+@pytest.mark.parametrize("splits", [1, 3, 0])
+def test_fused_append_fast_step_matches_oracle(splits):
+    """Fast step with the append fused, at L_slow + 1: the new token is the last row of
+    the recent window (or a sink row when L <= S)."""
+    sfi = _sfi()
+    S, W, k = 4, 32, 64
+    lens = [1024, 700, 36, 3, 2]
+    prob = Problem(seed=71 + splits, lens=lens, Hq=16, Hkv=8, D=128, S=S, W=W, extra_tokens=16,
+                   heavy_frac=0.02).to_device()
+    # slow step + Selector + compaction at L_slow (regular calls)
+    stride = int(prob.lens.max())
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    comp = _compact_buffers(prob, [k] * prob.B)
+    idx = torch.zeros((prob.B, prob.Hkv, k), dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_topk(scores, prob.Hkv, prob.d_kv.seq_lens, S, W, dev_i32([k] * prob.B), idx, comp.count,
+                        dev_status=st)
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
+    torch.cuda.synchronize()
+    ref_idx, ref_count = run_oracle_selection(prob, scores.cpu().numpy(), [k] * prob.B, k)
+    cap = comp.capacity.cpu().numpy()
+    compacts = [oracle_compact_request(prob, r, ref_idx[r], ref_count[r], cap[r]) for r in range(prob.B)]
+    # one more token, fused into the fast step
+    kn, vn = _grow(prob, syn.rng(401, splits))
+    q = syn.normal_bf16(syn.rng(402, splits), (prob.B, 16, 128))
+    out = torch.full((prob.B, 16, 128), float("nan"), device="cuda")
+    lse = torch.full((prob.B, 16), float("nan"), device="cuda")
+    max_tokens = S + k + W + 32
+    ws = sfi.alloc_workspace(prob.shape, prob.B, max_tokens, splits)
+    sfi.sfi_fast_decode_attn(prob.shape, prob.d_kv, comp, S, W, dev_bf16(q), out, lse, k_new=dev_bf16(kn),
+                             v_new=dev_bf16(vn), max_tokens=max_tokens, num_splits=splits, workspace=ws,
+                             dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for r in range(prob.B):
+        oracle.paged_append(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], prob.lens[r], kn[r], vn[r],
+                            prob.Hkv, prob.D, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    for r in range(prob.B):
+        rk, rv = compacts[r]
+        if prob.lens[r] <= S:  # the new token is a sink row: the oracle's compact copy must hold it too
+            rk[:, prob.lens[r] - 1], rv[:, prob.lens[r] - 1] = kn[r], vn[r]
+        o_ref, l_ref = oracle.fast_attn(q[r], rk, rv, ref_count[r], prob.kv.k_pool, prob.kv.v_pool,
+                                        prob.kv.page_table[r], prob.lens[r], S, W, 16, 8, 128, 16)
+        assert_close(o[r], o_ref, f"fast out r={r}")
+        assert_close(l[r], l_ref, f"fast lse r={r}")
+
+
+def test_early_prefetch_flag_gives_identical_results():
+    """Back-to-back launches on one stream, each reading KV state the previous launch
+    does not write, with SFI_ATTN_EARLY_KV_PREFETCH: bit-identical to the default."""
+    sfi = _sfi()
+    S, W, k = 4, 32, 64
+    probs = [Problem(seed=81 + i, lens=[1024, 1500, 700, 40], Hq=16, Hkv=8, D=128, S=S, W=W,
+                     heavy_frac=0.02).to_device() for i in range(3)]
+    comps = []
+    for prob in probs:
+        scores = torch.empty((prob.B, prob.Hkv, 1500), device="cuda")
+        _dense(prob, scores=scores)
+        comp = _compact_buffers(prob, [k] * prob.B)
+        idx = torch.zeros((prob.B, prob.Hkv, k), dtype=torch.int32, device="cuda")
+        sfi.sfi_select_topk(scores, prob.Hkv, prob.d_kv.seq_lens, S, W, dev_i32([k] * prob.B), idx, comp.count)
+        sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp)
+        comps.append(comp)
+    torch.cuda.synchronize()
+
+    def run(flags):
+        outs = []
+        st = _status()
+        for rep in range(2):
+            for prob, comp in zip(probs, comps):
+                fo = torch.empty((prob.B, 16, 128), device="cuda")
+                do = torch.empty((prob.B, 16, 128), device="cuda")
+                sc = torch.full((prob.B, prob.Hkv, 1500), float("nan"), device="cuda")
+                sfi.sfi_fast_decode_attn(prob.shape, prob.d_kv, comp, S, W, prob.d_q, fo, max_tokens=S + k + W + 32,
+                                         workspace=sfi.alloc_workspace(prob.shape, prob.B, S + k + W + 32),
+                                         dev_status=st, flags=flags)
+                sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, S, W, prob.d_q, do, None, sc,
+                                                    max_tokens=1516, workspace=sfi.alloc_workspace(prob.shape, prob.B,
+                                                                                                   1516),
+                                                    dev_status=st, flags=flags)
+                outs += [fo, do, sc]
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        return [x.cpu().numpy() for x in outs]
+
+    for a, b in zip(run(0), run(sfi.SFI_ATTN_EARLY_KV_PREFETCH)):
+        np.testing.assert_array_equal(a, b)

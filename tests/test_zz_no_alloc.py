@@ -6,7 +6,7 @@ cudaMalloc), so they cannot hand sfi_fast_decode_attn a workspace. The no-alloc
 entry point keeps the split-KV scratch in a fixed array inside the library instead.
 This test calls it through the C ABI twice in a row, with different queries, and
 checks each result against the regular entry point (with a workspace) within the
-parity tolerance. Splits are forced above one so the scratch is really used.
+parity tolerance. The split count is forced high enough that the scratch is used.
 This file is named to be collected last.
 """
 import numpy as np
@@ -55,12 +55,15 @@ def _filled_compact(sfi, prob, k):
 
 def test_noalloc_fast_step_matches_regular_entry_point_on_two_calls():
     sfi = _setup()
-    S, W, k, splits = 4, 32, 512, 4
-    prob = Problem(seed=901, lens=[4096, 3000, 1200, 40], Hq=16, Hkv=8, D=128, S=S, W=W,
+    # 12 splits: more than fit in one thread-block cluster, so the partial results go
+    # through the scratch (plans of up to 8 splits merge in shared memory and need none)
+    S, W, k, splits = 4, 32, 1536, 12
+    prob = Problem(seed=901, lens=[4096, 3000, 2000, 1600], Hq=16, Hkv=8, D=128, S=S, W=W,
                    heavy_frac=0.02).to_device()
     comp = _filled_compact(sfi, prob, k)
     max_tokens = S + k + W + 32
     assert sfi.sfi_plan_splits(prob.shape, prob.B, max_tokens, splits) == splits
+    assert 0 < sfi.sfi_workspace_size(prob.shape, prob.B, max_tokens, splits) <= (4 << 20)
     g = syn.rng(902, 1)
     for call in range(2):
         q = prob.d_q if call == 0 else dev_bf16(syn.normal_bf16(g, (prob.B, prob.Hq, prob.D)))
