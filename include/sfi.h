@@ -150,7 +150,7 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  *                L - 1 of the pages) and attends to the cache after that append;
  *                when L <= S the token is a sink row and is used in place of compact
  *                row L - 1 (the compact buffer itself is not written).
- *   out     : fp32 [B][Hq][D]
+ *   out     : fp32 [B][Hq][D], 8-byte aligned
  *   lse     : fp32 [B][Hq] or NULL
  *   max_tokens : an upper bound on S + max count + W + P over the batch, used to
  *                plan split-KV; 0 lets the library assume the compact capacity

@@ -533,21 +533,35 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         if (ctid == 0) s_last = mbar_wait_cluster_bounded(&merge_bar, 0) ? 1 : 0;
         consumer_bar_sync();
         if (s_last && ok) {
-            for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
-                const int row = e / D, d = e - (e / D) * D;
-                float M = -INFINITY;
-                for (int s = 0; s < p.splits; ++s)
-                    M = fmaxf(M, ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s)));
-                float acc = 0.f, lsum = 0.f;
-                for (int s = 0; s < p.splits; ++s) {
-                    const float ls = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
-                    if (ls > 0.f) {
-                        const float f = fast_exp2(ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s)) - M);
-                        acc += ld_cluster_f32(cluster_map(smem_u32(&cp_o[row * D + d]), s)) * f;
-                        lsum += ls * f;
+            // Each thread merges pairs of outputs. All loads from the peers' shared
+            // memory are issued before any is used, so their latencies overlap.
+            for (int e2 = ctid; e2 < G * D / 2; e2 += kConsumerWarps * 32) {
+                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+                float2 os[kMaxClusterSplits];
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < p.splits) {
+                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
+                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
+                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
                     }
                 }
-                p.out[(head0 + row) * D + d] = acc / lsum;
+                float M = -INFINITY;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s)
+                    if (s < p.splits) M = fmaxf(M, ms[s]);
+                float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < p.splits && ls[s] > 0.f) {
+                        const float f = fast_exp2(ms[s] - M);
+                        ax += os[s].x * f;
+                        ay += os[s].y * f;
+                        lsum += ls[s] * f;
+                    }
+                }
+                *reinterpret_cast<float2 *>(&p.out[(head0 + row) * D + d]) = make_float2(ax / lsum, ay / lsum);
                 if (d == 0 && p.lse) p.lse[head0 + row] = (M + log2f(lsum)) * kLn2;
             }
         }

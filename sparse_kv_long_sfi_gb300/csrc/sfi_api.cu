@@ -60,6 +60,7 @@ int sm_count_current_device() {
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned8(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 7u) == 0; }
 
 sfi_status check_shape(const sfi_attn_shape *s) {
     if (!s) return SFI_ERR_INVALID_ARG;
@@ -214,7 +215,8 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
     sfi_status st = check_shape(shape);
     if (st != SFI_OK) return st;
     if ((st = check_paged(shape, kv)) != SFI_OK) return st;
-    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out) return SFI_ERR_INVALID_ARG;
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned8(out))
+        return SFI_ERR_INVALID_ARG;
     if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity || !compact->count)
         return SFI_ERR_INVALID_ARG;
     if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v) || !aligned16(q))
@@ -257,7 +259,7 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
     sfi_status st = check_shape(shape);
     if (st != SFI_OK) return st;
     if ((st = check_paged(shape, kv)) != SFI_OK) return st;
-    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned16(q))
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned16(q) || !aligned8(out))
         return SFI_ERR_INVALID_ARG;
     if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
     if (batch == 0) return SFI_OK;

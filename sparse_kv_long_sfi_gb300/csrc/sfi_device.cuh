@@ -102,6 +102,12 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     return v;
 }
 
+__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t caddr) {
+    float2 v;
+    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
+    return v;
+}
+
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
