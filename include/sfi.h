@@ -197,6 +197,39 @@ SFI_API sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, 
                                            size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /*
+ * sfi_mixed_decode_attn - one launch for a batch whose requests are at different
+ * steps: the requests fast_ids[0 .. n_fast) do the fast step of
+ * sfi_fast_decode_attn, the requests slow_ids[0 .. n_slow) the slow step of
+ * sfi_slow_dense_attn_with_scores (dense attention, plus the masked scores when
+ * scores is non-NULL). "ASPIRE: Asynchronous Batched Self-Speculative Decoding for
+ * Long-Context LLM Inference" (abstract): drafting and verifying requests coexist in
+ * the same batched forward pass; SFI (Figure 2 caption): each request takes fast steps
+ * and, at its own boundaries, slow steps. A request id must appear in at most one of
+ * the two lists.
+ *   q, k_new, v_new, out, lse, scores, score_stride : as for the two calls above
+ *   compact          : required when n_fast > 0
+ *   max_fast_tokens  : an upper bound on S + max count + W + P over the fast requests
+ *   max_dense_tokens : an upper bound on L + P over the slow requests
+ *   flags            : 0 or SFI_ATTN_EARLY_KV_PREFETCH
+ *   workspace        : at least sfi_mixed_workspace_size(...) bytes, zero-filled before
+ *                      its first use (left zero-filled after each launch without
+ *                      device error); launches sharing it must not overlap.
+ * Device errors: those of sfi_fast_decode_attn and sfi_slow_dense_attn_with_scores.
+ */
+SFI_API sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
+                                         const sfi_compact_kv *compact, int32_t sink, int32_t recent, const void *q,
+                                         const void *k_new, const void *v_new, float *out, float *lse, float *scores,
+                                         int64_t score_stride, const int32_t *fast_ids, int32_t n_fast,
+                                         const int32_t *slow_ids, int32_t n_slow, int32_t max_fast_tokens,
+                                         int32_t max_dense_tokens, uint32_t flags, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Workspace bytes sfi_mixed_decode_attn needs for these arguments on the current
+ * device (0 when it needs none). */
+SFI_API size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_fast, int32_t n_slow,
+                                        int32_t max_fast_tokens, int32_t max_dense_tokens);
+
+/*
  * sfi_select_topk - the Selector (Figure 2 caption): for every (request r, KV
  * head kv) keep the k_eff = min(k_per_req[r], |C|) candidates of C = [S, L - W)
  * with the largest score; equal scores go to the lower position; -0 equals +0;

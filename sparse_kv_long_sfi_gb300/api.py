@@ -165,6 +165,42 @@ def sfi_slow_dense_attn_with_scores(shape: AttnShape, kv: PagedKV, sink: int, re
     _check(st, "sfi_slow_dense_attn_with_scores")
 
 
+def sfi_mixed_decode_attn(shape: AttnShape, kv: PagedKV, compact: Optional[CompactKV], sink: int, recent: int,
+                          q: torch.Tensor, out: torch.Tensor, fast_ids: torch.Tensor, slow_ids: torch.Tensor,
+                          lse: Optional[torch.Tensor] = None, scores: Optional[torch.Tensor] = None,
+                          k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None,
+                          max_fast_tokens: int = 0, max_dense_tokens: int = 0, flags: int = 0,
+                          workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                          stream=None):
+    ws = _ptr(workspace, torch.uint8, "workspace")
+    n_fast, n_slow = int(fast_ids.numel()), int(slow_ids.numel())
+    st = _abi.lib().sfi_mixed_decode_attn(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), None if compact is None else ctypes.byref(compact.c()),
+        int(sink), int(recent), _ptr(q, torch.bfloat16, "q"), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(scores, torch.float32, "scores"), 0 if scores is None else int(scores.shape[-1]),
+        _ptr(fast_ids, torch.int32, "fast_ids") if n_fast else None, n_fast,
+        _ptr(slow_ids, torch.int32, "slow_ids") if n_slow else None, n_slow, int(max_fast_tokens),
+        int(max_dense_tokens), int(flags), ws, 0 if workspace is None else workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_mixed_decode_attn")
+
+
+def sfi_mixed_workspace_size(shape: AttnShape, n_fast: int, n_slow: int, max_fast_tokens: int,
+                             max_dense_tokens: int) -> int:
+    return int(_abi.lib().sfi_mixed_workspace_size(ctypes.byref(shape.c()), int(n_fast), int(n_slow),
+                                                   int(max_fast_tokens), int(max_dense_tokens)))
+
+
+def alloc_mixed_workspace(shape: AttnShape, batch: int, max_fast_tokens: int, max_dense_tokens: int,
+                          device="cuda") -> torch.Tensor:
+    """A zero-filled workspace large enough for every split of `batch` requests into
+    fast and slow subsets."""
+    n = max([256] + [sfi_mixed_workspace_size(shape, batch - ns, ns, max_fast_tokens, max_dense_tokens)
+                     for ns in range(batch + 1)])
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
 def sfi_select_topk(scores: torch.Tensor, num_kv_heads: int, seq_lens: torch.Tensor, sink: int, recent: int,
                     k_per_req: torch.Tensor, idx_out: torch.Tensor, count_out: torch.Tensor,
                     req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None,

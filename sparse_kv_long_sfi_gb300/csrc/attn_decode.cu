@@ -71,25 +71,27 @@ struct UnitStream {
     int row_app;   // its row inside that sub-block
 };
 
-template <int MODE>
-__device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh, UnitStream &u) {
+// `lead` marks one CTA per request, which reports the request's errors.
+__device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh, bool fast, bool lead,
+                                            UnitStream &u) {
     // All per-request metadata is loaded up front, in one round trip.
     u.L = p.seq_lens[r];
-    const int cnt = MODE == kModeFast ? p.c_count[r] : 0;
-    const int cap = MODE == kModeFast ? p.c_capacity[r] : 0;
-    const int64_t off = MODE == kModeFast ? p.c_row_offset[r] : 0;
+    const int cnt = fast ? p.c_count[r] : 0;
+    const int cap = fast ? p.c_capacity[r] : 0;
+    const int64_t off = fast ? p.c_row_offset[r] : 0;
+    lead = lead && threadIdx.x == 0 && kvh == 0;
     if (u.L < 1 || u.L > p.max_pages * kSubTokens) {
-        if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_LEN);
+        if (lead) report(p.dev_status, SFI_DEV_BAD_LEN);
         return false;
     }
-    if (MODE == kModeFast) {
+    if (fast) {
         const int ns = min(p.sink, u.L);
         if (cnt < 0 || cnt > cap - p.sink || (cnt > 0 && u.L < p.sink)) {
-            if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_K_OVERFLOW);
+            if (lead) report(p.dev_status, SFI_DEV_K_OVERFLOW);
             return false;
         }
         if (off < 0 || off + (int64_t)p.hkv * cap > p.c_total_rows) {
-            if (threadIdx.x == 0 && kvh == 0 && blockIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_COMPACT);
+            if (lead) report(p.dev_status, SFI_DEV_BAD_COMPACT);
             return false;
         }
         u.crow0 = off + (int64_t)kvh * cap;
@@ -281,12 +283,39 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __shared__ int s_last;
     __shared__ int s_timeout;
 
-    const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+    // ---- this CTA's work item: (request, KV head, split) and the unit's mode ----
+    int split, kvh, b, splits;
+    bool fast;
+    int64_t unit, slot0;  // merge counter index; first partial slot of the unit
+    const int *ids = p.req_ids;
+    if (MODE == kModeMixed) {
+        // 1-D grid: the slow units' splits first, then the fast units'
+        int item = blockIdx.x;
+        const int n_slow_items = p.n_slow * p.hkv * p.slow_splits;
+        fast = item >= n_slow_items;
+        splits = fast ? p.fast_splits : p.slow_splits;
+        if (fast) item -= n_slow_items;
+        split = item % splits;
+        const int u_local = item / splits;
+        kvh = u_local % p.hkv;
+        b = u_local / p.hkv;
+        ids = fast ? p.fast_ids : p.slow_ids;
+        unit = fast ? (int64_t)p.n_slow * p.hkv + u_local : u_local;
+        slot0 = fast ? (int64_t)p.n_slow * p.hkv * p.slow_splits + (int64_t)u_local * splits : (int64_t)u_local * splits;
+    } else {
+        split = blockIdx.x;
+        kvh = blockIdx.y;
+        b = blockIdx.z;
+        splits = p.splits;
+        fast = MODE == kModeFast;
+        unit = (int64_t)b * p.hkv + kvh;
+        slot0 = unit * splits;
+    }
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         tma_prefetch_desc(&tm_pool_k);
         tma_prefetch_desc(&tm_pool_v);
-        if (MODE == kModeFast) {
+        if (MODE != kModeDense) {
             tma_prefetch_desc(&tm_comp_k);
             tma_prefetch_desc(&tm_comp_v);
         }
@@ -301,11 +330,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         grid_dependency_wait();
         grid_launch_dependents();
     }
-    const int r = p.req_ids ? p.req_ids[b] : b;
+    const int r = ids ? ids[b] : b;
 
     UnitStream u;
-    if (!unit_stream<MODE>(p, r, kvh, u)) return;  // uniform across the CTA and its cluster
-    const int per = (u.nb + p.splits - 1) / p.splits;
+    if (!unit_stream(p, r, kvh, fast, split == 0, u)) return;  // uniform across the CTA and its cluster
+    const int per = (u.nb + splits - 1) / splits;
     const int sb_begin = split * per;
     const int sb_end = min(u.nb, sb_begin + per);
     const int n_my = max(0, sb_end - sb_begin);
@@ -316,7 +345,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             mbar_init(&full_bar[i], kConsumerWarps);
             mbar_init(&empty_bar[i], kConsumerWarps);
         }
-        if (CLUSTER) mbar_init(&merge_bar, split == 0 ? p.splits - 1 : 1);
+        if (CLUSTER) mbar_init(&merge_bar, split == 0 ? splits - 1 : 1);
         s_timeout = 0;
         fence_barrier_init();
     }
@@ -419,10 +448,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
     float *score_row = nullptr;
-    if (SCORES && p.scores) {
+    if (SCORES && p.scores && !fast) {
         if (u.L <= p.score_stride) {
             score_row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride;
-        } else if (threadIdx.x == 0 && blockIdx.x == 0) {
+        } else if (threadIdx.x == 0 && split == 0) {
             report(p.dev_status, SFI_DEV_BAD_LEN);  // score row too short: scores not written
         }
     }
@@ -480,7 +509,6 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     consumer_bar_sync();
 
     const int ctid = threadIdx.x;  // 0 .. 127
-    const int64_t unit = (int64_t)b * p.hkv + kvh;
     const int64_t head0 = (int64_t)r * p.hq + (int64_t)kvh * G;
     if (ok) {
         for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
@@ -498,7 +526,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     lsum += sm_l[w * kMaxGroup + row] * f;
                 }
             }
-            if (p.splits == 1) {
+            if (splits == 1) {
                 p.out[(head0 + row) * D + d] = acc / lsum;
                 if (d == 0 && p.lse) p.lse[head0 + row] = (M + log2f(lsum)) * kLn2;
             } else if (CLUSTER) {
@@ -508,7 +536,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     cp_l[row] = lsum;
                 }
             } else {
-                const int64_t slot = (unit * p.splits + split) * kMaxGroup + row;
+                const int64_t slot = (slot0 + split) * kMaxGroup + row;
                 p.ws_part[slot * D + d] = acc;
                 if (d == 0) {
                     p.ws_ml[slot * 2 + 0] = M;
@@ -517,7 +545,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             }
         }
     }
-    if (p.splits == 1) return;
+    if (splits == 1) return;
 
     if (CLUSTER) {
         // ---- split merge inside the cluster, through distributed shared memory ----
@@ -541,7 +569,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 float2 os[kMaxClusterSplits];
 #pragma unroll
                 for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < p.splits) {
+                    if (s < splits) {
                         ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
                         ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
                         os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
@@ -550,11 +578,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 float M = -INFINITY;
 #pragma unroll
                 for (int s = 0; s < kMaxClusterSplits; ++s)
-                    if (s < p.splits) M = fmaxf(M, ms[s]);
+                    if (s < splits) M = fmaxf(M, ms[s]);
                 float ax = 0.f, ay = 0.f, lsum = 0.f;
 #pragma unroll
                 for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < p.splits && ls[s] > 0.f) {
+                    if (s < splits && ls[s] > 0.f) {
                         const float f = fast_exp2(ms[s] - M);
                         ax += os[s].x * f;
                         ay += os[s].y * f;
@@ -567,7 +595,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
         if (!s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
         consumer_bar_sync();  // every read of the peers' shared memory is done
-        if (ctid > 0 && ctid < p.splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
+        if (ctid > 0 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
         return;
     }
 
@@ -577,7 +605,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     consumer_bar_sync();
     if (ctid == 0) {
         const int prev = atomicAdd(&p.ws_count[unit], 1);
-        s_last = (prev == p.splits - 1);
+        s_last = (prev == splits - 1);
     }
     consumer_bar_sync();
     if (!s_last) return;
@@ -585,11 +613,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     for (int e = ctid; e < G * D; e += kConsumerWarps * 32) {
         const int row = e / D, d = e - (e / D) * D;
         float M = -INFINITY;
-        for (int s = 0; s < p.splits; ++s)
-            M = fmaxf(M, __ldcg(&p.ws_ml[((unit * p.splits + s) * kMaxGroup + row) * 2]));
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[((slot0 + s) * kMaxGroup + row) * 2]));
         float acc = 0.f, lsum = 0.f;
-        for (int s = 0; s < p.splits; ++s) {
-            const int64_t slot = (unit * p.splits + s) * kMaxGroup + row;
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) {
+            const int64_t slot = (slot0 + s) * kMaxGroup + row;
             const float ls = __ldcg(&p.ws_ml[slot * 2 + 1]);
             if (ls > 0.f) {
                 const float f = fast_exp2(__ldcg(&p.ws_ml[slot * 2]) - M);
@@ -603,14 +632,18 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     if (ctid == 0) p.ws_count[unit] = 0;  // leave the workspace zeroed for the next launch
 }
 
-WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim) {
+WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim) {
     WorkspaceLayout w;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
     w.count_off = 0;
     w.ml_off = up(sizeof(int32_t) * (size_t)units);
-    w.part_off = w.ml_off + up(sizeof(float) * 2 * kMaxGroup * (size_t)units * (size_t)splits);
-    w.total = w.part_off + up(sizeof(float) * (size_t)head_dim * kMaxGroup * (size_t)units * (size_t)splits);
+    w.part_off = w.ml_off + up(sizeof(float) * 2 * kMaxGroup * (size_t)slots);
+    w.total = w.part_off + up(sizeof(float) * (size_t)head_dim * kMaxGroup * (size_t)slots);
     return w;
+}
+
+WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim) {
+    return workspace_layout_slots(units, units * splits, head_dim);
 }
 
 template <int D, int MODE, bool SCORES, bool CLUSTER>
@@ -629,7 +662,10 @@ static cudaError_t launch_one(const AttnMaps &maps, const AttnParams &p, int bat
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(p.splits, p.hkv, batch);
+    if (MODE == kModeMixed)
+        cfg.gridDim = dim3((unsigned)(p.n_slow * p.hkv * p.slow_splits + p.n_fast * p.hkv * p.fast_splits));
+    else
+        cfg.gridDim = dim3(p.splits, p.hkv, batch);
     cfg.blockDim = dim3(kAttnThreads);
     cfg.dynamicSmemBytes = T::kSmemBytes;
     cfg.stream = stream;
@@ -654,6 +690,7 @@ static cudaError_t launch_one(const AttnMaps &maps, const AttnParams &p, int bat
 template <int D, bool CLUSTER>
 static cudaError_t launch_mode(int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p, int batch,
                                cudaStream_t stream) {
+    if (mode == kModeMixed) return launch_one<D, kModeMixed, true, false>(maps, p, batch, stream);
     if (mode == kModeFast) return launch_one<D, kModeFast, false, CLUSTER>(maps, p, batch, stream);
     if (with_scores) return launch_one<D, kModeDense, true, CLUSTER>(maps, p, batch, stream);
     return launch_one<D, kModeDense, false, CLUSTER>(maps, p, batch, stream);
@@ -661,7 +698,7 @@ static cudaError_t launch_mode(int mode, bool with_scores, const AttnMaps &maps,
 
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream) {
-    const bool cluster = p.splits > 1 && p.splits <= kMaxClusterSplits;
+    const bool cluster = mode != kModeMixed && p.splits > 1 && p.splits <= kMaxClusterSplits;
     if (head_dim == 128)
         return cluster ? launch_mode<128, true>(mode, with_scores, maps, p, batch, stream)
                        : launch_mode<128, false>(mode, with_scores, maps, p, batch, stream);

@@ -169,8 +169,10 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     __syncthreads();
     if (warp == 0) {  // exclusive scan over (round, warp) in position order
         int carry_gt = 0, carry_eq = 0;
-        for (int base = 0; base < rounds * kTopkWarps; base += 32) {
-            const int a0 = s_gt[base + lane], e0 = s_eq[base + lane];
+        const int entries = rounds * kTopkWarps;
+        for (int base = 0; base < entries; base += 32) {
+            const bool have = base + lane < entries;
+            const int a0 = have ? s_gt[base + lane] : 0, e0 = have ? s_eq[base + lane] : 0;
             int a = a0, e = e0;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -181,8 +183,10 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
                     e += ve;
                 }
             }
-            s_gt[base + lane] = carry_gt + a - a0;
-            s_eq[base + lane] = carry_eq + e - e0;
+            if (have) {
+                s_gt[base + lane] = carry_gt + a - a0;
+                s_eq[base + lane] = carry_eq + e - e0;
+            }
             carry_gt += __shfl_sync(0xffffffffu, a, 31);
             carry_eq += __shfl_sync(0xffffffffu, e, 31);
         }

@@ -106,6 +106,30 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
 
 bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
 
+// Plan of a mixed launch: every CTA gets about the same number of tokens (one wave of
+// two CTAs per SM over all units), with at least four stages of work per split.
+struct MixedPlan {
+    int fast_splits, slow_splits;
+    int64_t units, slots;
+};
+
+MixedPlan plan_mixed(int64_t fast_units, int64_t slow_units, int32_t max_fast_tokens, int32_t max_dense_tokens,
+                     int sm_count) {
+    MixedPlan m{1, 1, fast_units + slow_units, 0};
+    const double total = (double)fast_units * std::max(1, max_fast_tokens) +
+                         (double)slow_units * std::max(1, max_dense_tokens);
+    const double per_cta = std::max(1.0, total / std::max(1, sm_count * sfi::kAttnCtasPerSm));
+    auto splits_for = [&](int32_t tokens) {
+        const int nb = (std::max(1, tokens) + sfi::kSubTokens - 1) / sfi::kSubTokens + 1;
+        const int want = (int)std::ceil(std::max(1, tokens) / per_cta);
+        return std::max(1, std::min({want, std::max(1, nb / (4 * sfi::kConsumerWarps)), 256}));
+    };
+    if (fast_units > 0) m.fast_splits = splits_for(max_fast_tokens);
+    if (slow_units > 0) m.slow_splits = splits_for(max_dense_tokens);
+    m.slots = fast_units * m.fast_splits + slow_units * m.slow_splits;
+    return m;
+}
+
 float resolve_scale(const sfi_attn_shape *s) {
     return s->softmax_scale > 0.f ? s->softmax_scale : 1.0f / std::sqrt((float)s->head_dim);
 }
@@ -283,6 +307,87 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
     maps.comp_k = maps.pool_k;  // unused in dense mode
     maps.comp_v = maps.pool_v;
     return sfi::launch_attention(shape->head_dim, sfi::kModeDense, scores != nullptr, maps, p, batch,
+                                 static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_fast, int32_t n_slow, int32_t max_fast_tokens,
+                                int32_t max_dense_tokens) {
+    if (check_shape(shape) != SFI_OK || n_fast < 0 || n_slow < 0) return 0;
+    const MixedPlan m = plan_mixed((int64_t)n_fast * shape->num_kv_heads, (int64_t)n_slow * shape->num_kv_heads,
+                                   max_fast_tokens, max_dense_tokens, sm_count_current_device());
+    if (m.fast_splits == 1 && m.slow_splits == 1) return 0;
+    return sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim).total;
+}
+
+sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
+                                 int32_t sink, int32_t recent, const void *q, const void *k_new, const void *v_new,
+                                 float *out, float *lse, float *scores, int64_t score_stride, const int32_t *fast_ids,
+                                 int32_t n_fast, const int32_t *slow_ids, int32_t n_slow, int32_t max_fast_tokens,
+                                 int32_t max_dense_tokens, uint32_t flags, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (n_fast < 0 || n_slow < 0 || sink < 0 || recent < 0 || !q || !out || !aligned16(q) || !aligned8(out))
+        return SFI_ERR_INVALID_ARG;
+    if ((n_fast > 0 && !fast_ids) || (n_slow > 0 && !slow_ids)) return SFI_ERR_INVALID_ARG;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return SFI_ERR_INVALID_ARG;
+    if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
+    if (n_fast > 0) {
+        if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity || !compact->count)
+            return SFI_ERR_INVALID_ARG;
+        if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v)) return SFI_ERR_INVALID_ARG;
+        if (compact->total_rows >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
+    }
+    if (n_fast + n_slow == 0) return SFI_OK;
+    AttnParams p{};
+    fill_common(p, shape, kv, q, out, lse, nullptr, sink, recent, dev_status);
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
+    p.scores = scores;
+    p.score_stride = score_stride;
+    if (n_fast > 0) {
+        p.c_row_offset = compact->row_offset;
+        p.c_capacity = compact->capacity;
+        p.c_count = compact->count;
+        p.c_total_rows = compact->total_rows;
+    }
+    const MixedPlan m = plan_mixed((int64_t)n_fast * shape->num_kv_heads, (int64_t)n_slow * shape->num_kv_heads,
+                                   max_fast_tokens, max_dense_tokens, sm_count_current_device());
+    p.fast_ids = fast_ids;
+    p.slow_ids = slow_ids;
+    p.n_fast = n_fast;
+    p.n_slow = n_slow;
+    p.fast_splits = m.fast_splits;
+    p.slow_splits = m.slow_splits;
+    p.splits = std::max(m.fast_splits, m.slow_splits);  // > 1: partial states go through the workspace
+    if (p.splits > 1) {
+        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim);
+        if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return SFI_ERR_WORKSPACE;
+        char *base = static_cast<char *>(workspace);
+        p.ws_count = reinterpret_cast<int32_t *>(base + l.count_off);
+        p.ws_ml = reinterpret_cast<float *>(base + l.ml_off);
+        p.ws_part = reinterpret_cast<float *>(base + l.part_off);
+    }
+    AttnMaps maps;
+    const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
+    if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.pool_v, kv->v_pool, pool_rows, shape->head_dim))
+        return SFI_ERR_CUDA;
+    if (n_fast > 0) {
+        if (!encode_rows(&maps.comp_k, compact->k, compact->total_rows, shape->head_dim) ||
+            !encode_rows(&maps.comp_v, compact->v, compact->total_rows, shape->head_dim))
+            return SFI_ERR_CUDA;
+    } else {
+        maps.comp_k = maps.pool_k;
+        maps.comp_v = maps.pool_v;
+    }
+    return sfi::launch_attention(shape->head_dim, sfi::kModeMixed, true, maps, p, 0,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SFI_OK
                : SFI_ERR_CUDA;

@@ -23,7 +23,9 @@ constexpr int kAttnCtasPerSm = 2;
 // more splits merge through the global workspace.
 constexpr int kMaxClusterSplits = 8;
 
-enum AttnMode : int { kModeFast = 0, kModeDense = 1 };
+// kModeMixed: one launch where each request is either fast (fast_ids) or slow
+// (slow_ids: dense attention with scores); 1-D grid of work items.
+enum AttnMode : int { kModeFast = 0, kModeDense = 1, kModeMixed = 2 };
 
 struct AttnParams {
     const __nv_bfloat16 *q;  // [B][Hq][D]
@@ -45,6 +47,10 @@ struct AttnParams {
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
     int32_t splits;
+    // mixed mode: request lists and per-mode split counts
+    const int32_t *fast_ids;
+    const int32_t *slow_ids;
+    int32_t n_fast, n_slow, fast_splits, slow_splits;
     int32_t early_prefetch;  // SFI_ATTN_EARLY_KV_PREFETCH: stream KV before the dependency wait
     // fused append of the current token (position L - 1), or null
     const __nv_bfloat16 *k_new;  // [B][Hkv][D]
@@ -67,6 +73,7 @@ struct WorkspaceLayout {
     size_t count_off, ml_off, part_off, total;
 };
 WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim);
+WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim);
 
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream);

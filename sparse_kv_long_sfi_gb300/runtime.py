@@ -11,14 +11,15 @@ orders them on streams with events and keeps the per-request counters.
 """
 from __future__ import annotations
 
-from dataclasses import dataclass, field
-from typing import List, Optional
+from dataclasses import dataclass
+from typing import List, Optional, Sequence
 
 import numpy as np
 import torch
 
-from .api import (SFI_ATTN_EARLY_KV_PREFETCH, AttnShape, CompactKV, PagedKV, alloc_workspace, sfi_compact_gather,
-                  sfi_fast_decode_attn, sfi_paged_kv_append, sfi_select_topk, sfi_slow_dense_attn_with_scores)
+from .api import (SFI_ATTN_EARLY_KV_PREFETCH, AttnShape, CompactKV, PagedKV, alloc_mixed_workspace, alloc_workspace,
+                  sfi_compact_gather, sfi_fast_decode_attn, sfi_mixed_decode_attn, sfi_paged_kv_append,
+                  sfi_select_topk, sfi_slow_dense_attn_with_scores)
 
 
 class SlowFastSchedule:
@@ -117,11 +118,14 @@ class SFIDecoder:
     def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
                  max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
                  main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None,
-                 fuse_append: bool = True):
+                 fuse_append: bool = True, single_launch_mixed: bool = True):
         self.shape, self.layers, self.batch = shape, layers, batch
         # fuse_append: the attention kernels write the current token into the pages
         # themselves (no separate append launch per layer)
         self.fuse_append = bool(fuse_append)
+        # single_launch_mixed: a mixed step runs one attention launch per layer for its
+        # fast and slow requests together (sfi_mixed_decode_attn) instead of two
+        self.single_launch_mixed = bool(single_launch_mixed)
         self.sink, self.recent = int(sink), int(recent)
         self.max_len = int(max_len)
         B = batch.page_table.shape[0]
@@ -129,6 +133,8 @@ class SFIDecoder:
         self.max_dense_tokens = self.max_len + shape.page_size
         self.ws_fast = alloc_workspace(shape, B, self.max_fast_tokens, device=device)
         self.ws_dense = alloc_workspace(shape, B, self.max_dense_tokens, device=device)
+        self.ws_mixed = (alloc_mixed_workspace(shape, B, self.max_fast_tokens, self.max_dense_tokens, device=device)
+                         if single_launch_mixed else None)
         self.dev_status = dev_status if dev_status is not None else torch.zeros(1, dtype=torch.int32, device=device)
         lo, hi = torch.cuda.Stream.priority_range()
         self.main = main_stream or torch.cuda.Stream(device=device, priority=hi)
@@ -184,6 +190,27 @@ class SFIDecoder:
             self.main.wait_event(self.e_aux[i])
             self.pending[i] = False
 
+    def _slow_layer(self, i: int, L: LayerBuffers, kv: PagedKV, io: StepIO, seq_lens: torch.Tensor,
+                    req_ids: Optional[torch.Tensor], n: Optional[int], kn, vn):
+        """Layer i of a slow step: dense attention + masked scores on the main stream,
+        then the Selector and the compaction on the aux stream (Figure 3A)."""
+        self._mark("slow", "start")
+        sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
+                                        None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
+                                        req_ids=req_ids, batch=n, max_tokens=self.max_dense_tokens,
+                                        workspace=self.ws_dense, dev_status=self.dev_status, stream=self.main,
+                                        flags=self.attn_flags)
+        self._mark("slow", "end")
+        self.e_attn[i].record(self.main)
+        self.aux.wait_event(self.e_attn[i])
+        sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent, self.batch.k_per_req,
+                        L.idx, L.compact.count, req_ids=req_ids, batch=n, dev_status=self.dev_status,
+                        stream=self.aux)
+        sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact, req_ids=req_ids, batch=n,
+                           dev_status=self.dev_status, stream=self.aux)
+        self.e_aux[i].record(self.aux)
+        self.pending[i] = True
+
     def slow_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
                   append: bool = True):
         n = None if req_ids is None else req_ids.numel()
@@ -192,32 +219,24 @@ class SFIDecoder:
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
             kn, vn = self._append(i, kv, io, append, req_ids, n)
-            self._mark("slow", "start")
-            sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
-                                            None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
-                                            req_ids=req_ids, batch=n, max_tokens=self.max_dense_tokens,
-                                            workspace=self.ws_dense, dev_status=self.dev_status, stream=self.main,
-                                            flags=self.attn_flags)
-            self._mark("slow", "end")
-            self.e_attn[i].record(self.main)
-            self.aux.wait_event(self.e_attn[i])
-            sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,
-                            self.batch.k_per_req, L.idx, L.compact.count, req_ids=req_ids, batch=n,
-                            dev_status=self.dev_status, stream=self.aux)
-            sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact, req_ids=req_ids,
-                               batch=n, dev_status=self.dev_status, stream=self.aux)
-            self.e_aux[i].record(self.aux)
-            self.pending[i] = True
+            self._slow_layer(i, L, kv, io, seq_lens, req_ids, n, kn, vn)
         self._leave()
 
     def fast_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
-                  append: bool = True):
+                  append: bool = True, refresh_layers: Sequence[int] = ()):
+        """A fast step over all layers. Layers in refresh_layers take the slow path
+        instead (dense attention, scores, Selector, compaction): ASPIRE's intra-draft
+        refresh layer, which keeps one layer's sparse state current at every step."""
         n = None if req_ids is None else req_ids.numel()
+        refresh = set(int(x) for x in refresh_layers)
         self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
             kn, vn = self._append(i, kv, io, append, req_ids, n)
+            if i in refresh:
+                self._slow_layer(i, L, kv, io, seq_lens, req_ids, n, kn, vn)
+                continue
             self._mark("fast", "start")
             sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
                                  None if io.lse is None else io.lse[i], k_new=kn, v_new=vn, req_ids=req_ids,
@@ -227,24 +246,36 @@ class SFIDecoder:
         self._leave()
 
     def mixed_step(self, io: StepIO, seq_lens: torch.Tensor, slow_ids: torch.Tensor, fast_ids: torch.Tensor):
-        """One step where each request is slow or fast (ASPIRE-style mixed batch, two launches per layer)."""
+        """One step where each request is slow or fast (ASPIRE-style mixed batch): one
+        attention launch per layer for both kinds (or two with single_launch_mixed off)."""
         ns, nf = slow_ids.numel(), fast_ids.numel()
         self._enter()
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
             kn, vn = self._append(i, kv, io, True, None, None)
-            if nf:
-                sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
-                                     None if io.lse is None else io.lse[i], k_new=kn, v_new=vn, req_ids=fast_ids,
-                                     batch=nf, max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
-                                     dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
+            lse = None if io.lse is None else io.lse[i]
+            if self.single_launch_mixed:
+                self._mark("mixed", "start")
+                sfi_mixed_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
+                                      fast_ids, slow_ids, lse=lse, scores=L.scores if ns else None, k_new=kn,
+                                      v_new=vn, max_fast_tokens=self.max_fast_tokens,
+                                      max_dense_tokens=self.max_dense_tokens, flags=self.attn_flags,
+                                      workspace=self.ws_mixed, dev_status=self.dev_status, stream=self.main)
+                self._mark("mixed", "end")
+            else:
+                if nf:
+                    sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
+                                         lse, k_new=kn, v_new=vn, req_ids=fast_ids, batch=nf,
+                                         max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
+                                         dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
+                if ns:
+                    sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
+                                                    lse, L.scores, k_new=kn, v_new=vn, req_ids=slow_ids, batch=ns,
+                                                    max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
+                                                    dev_status=self.dev_status, stream=self.main,
+                                                    flags=self.attn_flags)
             if ns:
-                sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
-                                                None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
-                                                req_ids=slow_ids, batch=ns, max_tokens=self.max_dense_tokens,
-                                                workspace=self.ws_dense, dev_status=self.dev_status,
-                                                stream=self.main, flags=self.attn_flags)
                 self.e_attn[i].record(self.main)
                 self.aux.wait_event(self.e_attn[i])
                 sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,

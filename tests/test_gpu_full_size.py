@@ -33,7 +33,7 @@ class Workload:
     new tokens for a few steps."""
 
     def __init__(self, seed, lens, Hq, Hkv, D, S, W, k_per_req, steps=3, layers=1, heavy_frac=0.0,
-                 k_cap=None):
+                 k_cap=None, single_launch_mixed=True):
         import sparse_kv_long_sfi_gb300 as sfi
         self.sfi = sfi
         self.Hq, self.Hkv, self.D, self.P, self.S, self.W = Hq, Hkv, D, 16, S, W
@@ -69,7 +69,8 @@ class Workload:
         self.layers = sfi.allocate_layers(self.shape, layers, num_pages, self.batch, S, device=dev, pool_init=init)
         self.out = torch.zeros((layers, self.B, Hq, D), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((layers, self.B, Hq), dtype=torch.float32, device=dev)
-        self.dec = sfi.SFIDecoder(self.shape, self.layers, self.batch, S, W, max_len=int(self.lens0.max()) + steps + 1)
+        self.dec = sfi.SFIDecoder(self.shape, self.layers, self.batch, S, W, max_len=int(self.lens0.max()) + steps + 1,
+                                  single_launch_mixed=single_launch_mixed)
         self.cur = self.lens0.copy()
 
     def io(self, t):
@@ -144,10 +145,12 @@ def _check_fast(w, t, layer, sampled):
         assert_close(lse[r], l_ref, f"fast lse r={r} t={t}")
 
 
-def _run_schedule(w, modes, sampled, retention=None):
-    """Run len(modes) steps (modes[t][b] = 1 slow / 0 fast) and check every step."""
+def _run_schedule(w, modes, sampled, retention=None, refresh=None):
+    """Run len(modes) steps (modes[t][b] = 1 slow / 0 fast) and check every step.
+    refresh[t]: layers that take the slow path inside an all-fast step t."""
     w.oracle_compact = {}
     for t, m in enumerate(modes):
+        layers_slow = set(refresh[t]) if refresh else set()
         w.cur = w.cur + 1  # the step's token is appended first (fused into the attention kernels)
         w.slow_mask = np.asarray(m, bool)
         if retention is not None:  # k fixed at each slow step from the request's retention ratio
@@ -159,14 +162,17 @@ def _run_schedule(w, modes, sampled, retention=None):
         if w.slow_mask.all():
             w.dec.slow_step(w.io(t), seq)
         elif not w.slow_mask.any():
-            w.dec.fast_step(w.io(t), seq)
+            w.dec.fast_step(w.io(t), seq, refresh_layers=layers_slow)
         else:
             w.dec.mixed_step(w.io(t), seq, torch.as_tensor(np.flatnonzero(w.slow_mask).astype(np.int32)).cuda(),
                              torch.as_tensor(np.flatnonzero(~w.slow_mask).astype(np.int32)).cuda())
         w.dec.join()
+        step_mask = w.slow_mask
         for layer in range(len(w.layers)):
+            w.slow_mask = np.ones_like(step_mask) if layer in layers_slow else step_mask
             _check_slow(w, t, layer, sampled)
             _check_fast(w, t, layer, sampled)
+        w.slow_mask = step_mask
 
 
 def test_qwen3_0_6b_16k_batch16_cycle():
@@ -211,7 +217,8 @@ def test_slow_step_stress_64k_zipf_ties():
     assert any(len(np.unique(sc[r, h, S:S + n])) < n for r in range(8) for h in range(8))
 
 
-def test_ragged_mixed_batch_64_requests():
+@pytest.mark.parametrize("single_launch", [True, False], ids=["one-launch", "two-launch"])
+def test_ragged_mixed_batch_64_requests(single_launch):
     """64 requests, lengths log-uniform in [4096, 131072], 32 Q / 8 KV heads, shuffled pages,
     per-request retention from {3, 12.5, 25}%, boundary process p = 0.06 with a forced
     refresh every 32 steps (the first step is slow)."""
@@ -221,7 +228,8 @@ def test_ragged_mixed_batch_64_requests():
     S, W = 64, 256
     k0 = [syn.retention_budget(ret[r], int(lens[r]) + 1, S, W) for r in range(64)]
     k_cap = max(syn.retention_budget(ret[r], int(lens[r]) + 8, S, W) for r in range(64))
-    w = Workload(5, lens, 32, 8, 128, S, W, k0, steps=4, layers=1, heavy_frac=0.02, k_cap=k_cap)
+    w = Workload(5, lens, 32, 8, 128, S, W, k0, steps=4, layers=1, heavy_frac=0.02, k_cap=k_cap,
+                 single_launch_mixed=single_launch)
     from sparse_kv_long_sfi_gb300 import SlowFastSchedule
     sched = SlowFastSchedule(64, 32)
     b = syn.boundary_draws(syn.rng(5, 1), 4, 64, 0.3)  # a high rate so that a short run mixes modes
@@ -230,3 +238,12 @@ def test_ragged_mixed_batch_64_requests():
     short, long_ = int(np.argmin(lens)), int(np.argmax(lens))
     slow_then_fast = int(np.flatnonzero(modes[1] == 0)[0])
     _run_schedule(w, modes, sampled=sorted({short, long_, slow_then_fast}), retention=ret)
+
+
+def test_refresh_layer_inside_fast_steps():
+    """ASPIRE's intra-draft refresh layer: layer 1 runs the slow path (dense attention,
+    scores, Selector, compaction) inside fast steps; the step after uses its fresh
+    selection while layer 0 keeps the one of the first slow step."""
+    k = syn.retention_budget(0.125, 4096, 64, 256)
+    w = Workload(6, [4095] * 4, 16, 8, 128, 64, 256, [k] * 4, steps=4, layers=2, heavy_frac=0.02)
+    _run_schedule(w, [[1] * 4, [0] * 4, [0] * 4, [0] * 4], sampled=[0, 3], refresh=[(), (1,), (), (1,)])

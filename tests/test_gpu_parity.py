@@ -529,3 +529,70 @@ def test_early_prefetch_flag_gives_identical_results():
 
     for a, b in zip(run(0), run(sfi.SFI_ATTN_EARLY_KV_PREFETCH)):
         np.testing.assert_array_equal(a, b)
+
+
+def test_mixed_launch_matches_oracle():
+    """One launch serving fast and slow requests of one batch, the current token fused:
+    fast requests against the oracle's fast step, slow ones against dense attention and
+    the masked scores. The slow requests are long enough to be split, so their partial
+    states merge through the workspace."""
+    sfi = _sfi()
+    S, W, k = 4, 32, 64
+    lens = [4000, 1200, 3000, 600, 2500, 40]
+    prob = Problem(seed=91, lens=lens, Hq=16, Hkv=8, D=128, S=S, W=W, extra_tokens=16,
+                   heavy_frac=0.02).to_device()
+    fast, slow = [1, 3, 5], [0, 2, 4]
+    # an earlier slow step for the fast requests' compact buffers
+    stride = int(prob.lens.max()) + 16
+    scores0 = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores0)
+    comp = _compact_buffers(prob, [k] * prob.B)
+    idx = torch.zeros((prob.B, prob.Hkv, k), dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_topk(scores0, prob.Hkv, prob.d_kv.seq_lens, S, W, dev_i32([k] * prob.B), idx, comp.count,
+                        dev_status=st)
+    sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
+    torch.cuda.synchronize()
+    ref_idx, ref_count = run_oracle_selection(prob, scores0.cpu().numpy(), [k] * prob.B, k)
+    cap = comp.capacity.cpu().numpy()
+    compacts = {r: oracle_compact_request(prob, r, ref_idx[r], ref_count[r], cap[r]) for r in fast}
+    # the mixed step, one token later
+    kn, vn = _grow(prob, syn.rng(403, 1))
+    q = syn.normal_bf16(syn.rng(404, 1), (prob.B, 16, 128))
+    out = torch.full((prob.B, 16, 128), float("nan"), device="cuda")
+    lse = torch.full((prob.B, 16), float("nan"), device="cuda")
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    mf, md = S + k + W + 32, int(prob.lens.max()) + 16
+    ws = sfi.alloc_mixed_workspace(prob.shape, prob.B, mf, md)
+    assert sfi.sfi_mixed_workspace_size(prob.shape, len(fast), len(slow), mf, md) > 0  # slow units are split
+    sfi.sfi_mixed_decode_attn(prob.shape, prob.d_kv, comp, S, W, dev_bf16(q), out, dev_i32(fast), dev_i32(slow),
+                              lse=lse, scores=scores, k_new=dev_bf16(kn), v_new=dev_bf16(vn), max_fast_tokens=mf,
+                              max_dense_tokens=md, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    assert counters_zero(ws, prob.B * prob.Hkv)
+    for r in range(prob.B):
+        oracle.paged_append(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], prob.lens[r], kn[r], vn[r],
+                            prob.Hkv, prob.D, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
+    prob.q = q
+    o, l, sc = out.cpu().numpy(), lse.cpu().numpy(), scores.cpu().numpy()
+    for r in fast:
+        rk, rv = compacts[r]
+        if prob.lens[r] <= S:
+            rk[:, prob.lens[r] - 1], rv[:, prob.lens[r] - 1] = kn[r], vn[r]
+        o_ref, l_ref = oracle.fast_attn(q[r], rk, rv, ref_count[r], prob.kv.k_pool, prob.kv.v_pool,
+                                        prob.kv.page_table[r], prob.lens[r], S, W, 16, 8, 128, 16)
+        assert_close(o[r], o_ref, f"mixed fast r={r}")
+        assert_close(l[r], l_ref, f"mixed fast lse r={r}")
+        assert np.isnan(sc[r]).all(), "fast requests write no scores"
+    for r in slow:
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(o[r], o_ref, f"mixed slow r={r}")
+        assert_close(l[r], l_ref, f"mixed slow lse r={r}")
+        L = prob.lens[r]
+        ref = prob.oracle_scores(r, stride)
+        masked = np.isneginf(ref[:, :L])
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+        err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
+        assert (err <= prob.score_bound(r, stride)[:, :L][~masked]).all()
