@@ -55,8 +55,14 @@ def _load(path: str):
     L.oracle_split_merge_attn.argtypes = [P, I, P, P, P, P, I, I, I, I, Dd, P, P]
     L.oracle_paged_append.argtypes = [P, P, P, I, P, P, I, I, I]
     L.oracle_schedule.argtypes = [P, I, I, I, P]
+    L.oracle_verify_attn.argtypes = [P, P, P, P, I, I, I, I, I, I, Dd, P, P]
+    L.oracle_fast_multi_attn.argtypes = [P, P, P, I, I, P, P, P, I, I, I, I, I, I, I, I, Dd, P, P]
+    L.oracle_verify_scores.argtypes = [P, P, P, I, I, I, I, I, I, I, I, Dd, P, ctypes.c_long]
+    L.oracle_paged_append_tokens.argtypes = [P, P, P, I, I, P, P, I, I, I]
     for f in (L.oracle_dense_attn, L.oracle_index_attn, L.oracle_group_scores, L.oracle_compact,
-              L.oracle_fast_attn, L.oracle_split_merge_attn, L.oracle_paged_append, L.oracle_schedule):
+              L.oracle_fast_attn, L.oracle_split_merge_attn, L.oracle_paged_append, L.oracle_schedule,
+              L.oracle_verify_attn, L.oracle_fast_multi_attn, L.oracle_verify_scores,
+              L.oracle_paged_append_tokens):
         f.restype = None
     return L
 
@@ -201,3 +207,44 @@ def schedule(boundary, interval):
     modes = np.zeros_like(boundary)
     lib().oracle_schedule(_p(boundary), steps, batch, int(interval), _p(modes))
     return modes
+
+
+def verify_attn(q, k_pool, v_pool, page_row, L, T, Hq, Hkv, D, P, scale=0.0):
+    """Causal attention of T drafted tokens: q uint16 [T][Hq][D] -> (out [T][Hq][D], lse [T][Hq])."""
+    q, k_pool, v_pool, page_row = _u16(q), _u16(k_pool), _u16(v_pool), _i32(page_row)
+    out = np.zeros((T, Hq, D), np.float64)
+    lse = np.zeros((T, Hq), np.float64)
+    lib().oracle_verify_attn(_p(q), _p(k_pool), _p(v_pool), _p(page_row), int(L), int(T), Hq, Hkv, D, P,
+                             float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def fast_multi_attn(q, ck, cv, count, k_pool, v_pool, page_row, L, T, S, W, Hq, Hkv, D, P, scale=0.0):
+    """T query tokens over the sparse state: q uint16 [T][Hq][D] -> (out [T][Hq][D], lse [T][Hq])."""
+    q, ck, cv = _u16(q), _u16(ck), _u16(cv)
+    k_pool, v_pool, page_row = _u16(k_pool), _u16(v_pool), _i32(page_row)
+    cap = ck.shape[1]
+    out = np.zeros((T, Hq, D), np.float64)
+    lse = np.zeros((T, Hq), np.float64)
+    lib().oracle_fast_multi_attn(_p(q), _p(ck), _p(cv), cap, int(count), _p(k_pool), _p(v_pool), _p(page_row),
+                                 int(L), int(T), int(S), int(W), Hq, Hkv, D, P, float(scale), _p(out), _p(lse))
+    return out, lse
+
+
+def verify_scores(q, k_pool, page_row, L, T, S, W, Hq, Hkv, D, P, scale=0.0, stride=None, fill=np.nan):
+    """Verification statistics: float32 [Hkv][stride] (group- and token-summed masked logits)."""
+    q, k_pool, page_row = _u16(q), _u16(k_pool), _i32(page_row)
+    stride = int(L) if stride is None else int(stride)
+    scores = np.full((Hkv, stride), fill, np.float32)
+    lib().oracle_verify_scores(_p(q), _p(k_pool), _p(page_row), int(L), int(T), int(S), int(W), Hq, Hkv, D, P,
+                               float(scale), _p(scores), stride)
+    return scores
+
+
+def paged_append_tokens(k_pool, v_pool, page_row, L, T, k_new, v_new, Hkv, D, P):
+    """In-place append of T tokens (positions L - T .. L - 1) into uint16 pools; k_new [T][Hkv][D]."""
+    assert k_pool.dtype == np.uint16 and k_pool.flags["C_CONTIGUOUS"]
+    assert v_pool.dtype == np.uint16 and v_pool.flags["C_CONTIGUOUS"]
+    page_row, k_new, v_new = _i32(page_row), _u16(k_new), _u16(v_new)
+    lib().oracle_paged_append_tokens(_p(k_pool), _p(v_pool), _p(page_row), int(L), int(T), _p(k_new), _p(v_new),
+                                     Hkv, D, P)

@@ -380,6 +380,91 @@ ORACLE_EXPORT void oracle_paged_append(uint16_t *k_pool, uint16_t *v_pool, const
 }
 
 /*
+ * Verification of T drafted tokens ("A Sparse Glimpse of the Whole: Train-Free
+ * Self-Speculative Decoding", abstract: drafts come from the sparse, recallable KV
+ * state; full-context verification produces the per-head attention statistics that
+ * are recycled as the importance signal). The T tokens occupy positions
+ * L - T .. L - 1 (L counts them); query token t attends causally to positions
+ * [0, L - T + t]. q: [T][Hq][D]; out: [T][Hq][D]; lse: [T][Hq].
+ */
+ORACLE_EXPORT void oracle_verify_attn(const uint16_t *q, const uint16_t *k_pool, const uint16_t *v_pool,
+                                      const int32_t *page_row, int L, int T, int Hq, int Hkv, int D, int P,
+                                      double scale, double *out, double *lse)
+{
+    for (int t = 0; t < T; ++t)
+        oracle_dense_attn(q + (size_t)t * Hq * D, k_pool, v_pool, page_row, L - T + t + 1, Hq, Hkv, D, P, scale,
+                          out + (size_t)t * Hq * D, lse + (size_t)t * Hq);
+}
+
+/*
+ * T query tokens over the sparse state (drafting several tokens in one pass): token
+ * t sees what a fast step at length L_t = L - T + t + 1 sees, the compact rows and
+ * the recent window [max(S, L_t - W), L_t). q: [T][Hq][D]; out: [T][Hq][D];
+ * lse: [T][Hq]. A non-empty selection needs L - T + 1 >= S.
+ */
+ORACLE_EXPORT void oracle_fast_multi_attn(const uint16_t *q, const uint16_t *ck, const uint16_t *cv, int cap,
+                                          int count, const uint16_t *k_pool, const uint16_t *v_pool,
+                                          const int32_t *page_row, int L, int T, int S, int W, int Hq, int Hkv,
+                                          int D, int P, double scale, double *out, double *lse)
+{
+    for (int t = 0; t < T; ++t)
+        oracle_fast_attn(q + (size_t)t * Hq * D, ck, cv, cap, count, k_pool, v_pool, page_row, L - T + t + 1, S, W,
+                         Hq, Hkv, D, P, scale, out + (size_t)t * Hq * D, lse + (size_t)t * Hq);
+}
+
+/*
+ * Statistics of a verification: for every KV head kv and candidate j in
+ * C = [S, L - W), the scaled logit summed over the G query heads of the group and
+ * over the query tokens t that see j (j <= L - T + t); -inf at the other positions
+ * below L. Formed in double, rounded once to float. Rows have stride `stride`.
+ */
+ORACLE_EXPORT void oracle_verify_scores(const uint16_t *q, const uint16_t *k_pool, const int32_t *page_row, int L,
+                                        int T, int S, int W, int Hq, int Hkv, int D, int P, double scale,
+                                        float *scores, long stride)
+{
+    int G = Hq / Hkv;
+    scale = default_scale(scale, D);
+    double *qd = (double *)malloc((size_t)T * G * D * sizeof(double));
+    for (int kv = 0; kv < Hkv; ++kv) {
+        for (int t = 0; t < T; ++t)
+            for (int g = 0; g < G; ++g)
+                widen_query(q + ((size_t)t * Hq + (size_t)(kv * G + g)) * D, D, qd + ((size_t)t * G + g) * D);
+        float *row = scores + (size_t)kv * (size_t)stride;
+        for (int j = 0; j < L; ++j) {
+            if (j < S || j >= L - W) {
+                row[j] = -INFINITY;
+                continue;
+            }
+            const uint16_t *k = paged_row(k_pool, page_row, j, kv, Hkv, P, D);
+            double sigma = 0.0;
+            for (int t = 0; t < T; ++t) {
+                if (j > L - T + t) continue; /* not visible to query token t */
+                for (int g = 0; g < G; ++g) {
+                    double acc = 0.0;
+                    for (int d = 0; d < D; ++d) acc += qd[((size_t)t * G + g) * D + d] * widen_bf16(k[d]);
+                    sigma += scale * acc;
+                }
+            }
+            row[j] = (float)sigma;
+        }
+    }
+    free(qd);
+}
+
+/*
+ * Append of T tokens: request positions L - T .. L - 1 (L counts them) receive
+ * k_new[t], v_new[t] ([T][Hkv][D]).
+ */
+ORACLE_EXPORT void oracle_paged_append_tokens(uint16_t *k_pool, uint16_t *v_pool, const int32_t *page_row, int L,
+                                              int T, const uint16_t *k_new, const uint16_t *v_new, int Hkv, int D,
+                                              int P)
+{
+    for (int t = 0; t < T; ++t)
+        oracle_paged_append(k_pool, v_pool, page_row, L - T + t + 1, k_new + (size_t)t * Hkv * D,
+                            v_new + (size_t)t * Hkv * D, Hkv, D, P);
+}
+
+/*
  * Slow/fast schedule (Figure 2 caption: a slow step fires on a boundary token or
  * when a fixed refresh interval is reached). For each request, step t is slow if
  * it is the request's first step, if boundary[t][b] is set, or if `interval`

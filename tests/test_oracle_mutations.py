@@ -54,6 +54,19 @@ MUTATIONS = [
      [lambda: pins.test_split_merge_equals_one_pass(O, 3)]),
     ("append one slot late", "int pos = L - 1;", "int pos = L;",
      [lambda: pins.test_append_writes_only_the_last_slot(O)]),
+    ("verification not causal", "page_row, L - T + t + 1, Hq, Hkv", "page_row, L, Hq, Hkv",
+     [lambda: pins.test_verify_is_causal_prefix_mean(O, 40, 3)]),
+    ("verification shifted by one position", "page_row, L - T + t + 1, Hq, Hkv", "page_row, L - T + t, Hq, Hkv",
+     [lambda: pins.test_verify_is_causal_prefix_mean(O, 40, 3)]),
+    ("multi-token draft shares the last token's window", "page_row, L - T + t + 1, S, W,", "page_row, L, S, W,",
+     [lambda: pins.test_fast_multi_attends_each_tokens_sparse_state(O, 203, 4, 4, 32, [5, 9, 100, 166])]),
+    ("verification statistic ignores causality", "if (j > L - T + t) continue;", "if (j > L) continue;",
+     [lambda: pins.test_verify_scores_closed_form_and_mask(O, 5, 2)]),
+    ("verification statistic from the last token only", "for (int t = 0; t < T; ++t) {\n                if (j >",
+     "for (int t = T - 1; t < T; ++t) {\n                if (j >",
+     [lambda: pins.test_verify_scores_closed_form_and_mask(O, 4, 40)]),
+    ("token append one slot early", "page_row, L - T + t + 1, k_new", "page_row, L - T + t, k_new",
+     [lambda: pins.test_append_tokens_writes_exactly_the_last_t_slots(O)]),
     ("refresh interval off by one", "(t - last_slow >= interval)", "(t - last_slow > interval)",
      [lambda: pins.test_schedule_interval_and_boundaries(O)]),
 ]

@@ -408,3 +408,164 @@ def test_schedule_interval_and_boundaries(oracle_lib):
     assert np.flatnonzero(m[:, 0]).tolist() == [0, 16, 32, 48, 64]
     assert np.flatnonzero(m[:, 1]).tolist() == [0, 5, 6, 22, 38, 54]
     assert np.flatnonzero(m[:, 2]).tolist() == [0, 16, 32, 40, 56]
+
+
+# ---------------------------------------------------------------------------
+# Several query tokens: draft over the sparse state, verification over the whole
+# context ("A Sparse Glimpse of the Whole", abstract; the T tokens sit at positions
+# L - T .. L - 1 and token t sees the context up to its own position)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("L,T", [(203, 1), (203, 5), (40, 3), (16, 16), (37, 9)])
+def test_verify_is_causal_prefix_mean(oracle_lib, L, T):
+    """Zero logits and position-coded V: token t averages positions 0 .. L - T + t."""
+    Hq, Hkv, D, P = 4, 2, 64, 16
+    page_row, kp, vp = _position_coded_kv(L, Hkv, D, P, seed=40 + L + T)
+    out, lse = oracle_lib.verify_attn(np.zeros((T, Hq, D), np.uint16), kp, vp, page_row, L, T, Hq, Hkv, D, P)
+    for t in range(T):
+        n = L - T + t + 1
+        for h in range(Hq):
+            assert out[t, h, 0] == pytest.approx((n - 1) / 2, abs=1e-11)
+            assert out[t, h, 1] == h // 2
+            assert lse[t, h] == pytest.approx(math.log(n), abs=1e-13)
+
+
+def test_verify_tokens_see_nothing_after_themselves(oracle_lib):
+    """Changing K/V after position L - T + t, or another token's query, leaves token t unchanged."""
+    Hq, Hkv, D, P, L, T = 8, 2, 64, 16, 150, 6
+    g = syn.rng(3, 77)
+    kv = syn.make_paged_kv(g, [L], Hkv, D, P)
+    pr = kv.page_table[0]
+    q = syn.normal_bf16(g, (T, Hq, D))
+    base, base_l = oracle_lib.verify_attn(q, kv.k_pool, kv.v_pool, pr, L, T, Hq, Hkv, D, P)
+    t_cut = 2
+    kp, vp = kv.k_pool.copy(), kv.v_pool.copy()
+    for j in range(L - T + t_cut + 1, L):
+        for h in range(Hkv):
+            kp[pr[j // P], h, j % P] = syn.normal_bf16(g, (D,))
+            vp[pr[j // P], h, j % P] = syn.normal_bf16(g, (D,))
+    o2, l2 = oracle_lib.verify_attn(q, kp, vp, pr, L, T, Hq, Hkv, D, P)
+    assert np.array_equal(o2[:t_cut + 1], base[:t_cut + 1]) and np.array_equal(l2[:t_cut + 1], base_l[:t_cut + 1])
+    assert np.abs(o2[t_cut + 1:] - base[t_cut + 1:]).max() > 1e-3
+    q2 = q.copy()
+    q2[4] = syn.normal_bf16(g, (Hq, D))
+    o3, _ = oracle_lib.verify_attn(q2, kv.k_pool, kv.v_pool, pr, L, T, Hq, Hkv, D, P)
+    keep = [t for t in range(T) if t != 4]
+    assert np.array_equal(o3[keep], base[keep]) and np.abs(o3[4] - base[4]).max() > 1e-3
+
+
+@pytest.mark.parametrize("L,T,S,W,sel", [
+    (203, 4, 4, 32, [5, 9, 100, 166]),     # windows shift by one position per token
+    (203, 6, 4, 3, [5, 9, 100]),           # W < T: every token's window is disjoint from the first's
+    (10, 4, 12, 32, []),                   # L - T + 1 < S: the sink grows with the token
+    (12, 12, 4, 6, []),                    # T = L
+])
+def test_fast_multi_attends_each_tokens_sparse_state(oracle_lib, L, T, S, W, sel):
+    """Zero logits and position-coded V: token t averages sink + selection + its own recent window."""
+    Hq, Hkv, D, P = 4, 2, 64, 16
+    page_row, kp, vp = _position_coded_kv(L, Hkv, D, P, seed=60 + L + T)
+    k_eff = len(sel)
+    cap = S + max(k_eff, 1)
+    idx = np.array([sel, sel], np.int32).reshape(Hkv, -1) if k_eff else np.zeros((Hkv, 1), np.int32)
+    ck, cv = oracle_lib.compact(kp, vp, page_row, L, S, idx, k_eff, Hkv, D, P, cap)
+    out, lse = oracle_lib.fast_multi_attn(np.zeros((T, Hq, D), np.uint16), ck, cv, k_eff, kp, vp, page_row, L, T,
+                                          S, W, Hq, Hkv, D, P)
+    for t in range(T):
+        Lt = L - T + t + 1
+        state = sorted(set(range(min(S, Lt))) | set(sel) | set(range(max(S, Lt - W), Lt)))
+        for h in range(Hq):
+            assert out[t, h, 0] == pytest.approx(sum(state) / len(state), abs=1e-11)
+            assert out[t, h, 1] == h // 2
+            assert lse[t, h] == pytest.approx(math.log(len(state)), abs=1e-13)
+
+
+def test_fast_multi_equals_masked_dense_per_token(oracle_lib):
+    """Random data: token t equals dense attention restricted to its explicit position set."""
+    Hq, Hkv, D, P, S, W, L, T, k = 8, 2, 64, 16, 4, 24, 400, 5, 30
+    g = syn.rng(3, 91)
+    kv = syn.make_paged_kv(g, [L], Hkv, D, P)
+    pr = kv.page_table[0]
+    q = syn.normal_bf16(g, (T, Hq, D))
+    L0 = L - T + 1
+    idx = np.stack([np.sort(g.choice(np.arange(S, L0 - W), k, replace=False)) for _ in range(Hkv)]).astype(np.int32)
+    ck, cv = oracle_lib.compact(kv.k_pool, kv.v_pool, pr, L0, S, idx, k, Hkv, D, P, S + k)
+    out, lse = oracle_lib.fast_multi_attn(q, ck, cv, k, kv.k_pool, kv.v_pool, pr, L, T, S, W, Hq, Hkv, D, P)
+    for t in range(T):
+        Lt = L0 + t
+        pos = np.stack([np.concatenate([np.arange(S), idx[h], np.arange(Lt - W, Lt)]) for h in range(Hkv)])
+        mo, ml = oracle_lib.index_attn(q[t], kv.k_pool, kv.v_pool, pr, pos.astype(np.int32), Hq, Hkv, D, P)
+        np.testing.assert_allclose(out[t], mo, rtol=0, atol=1e-12)
+        np.testing.assert_allclose(lse[t], ml, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("which", ["first", "last"])
+def test_fast_multi_full_retention_meets_verify(oracle_lib, which):
+    """Table 1's 100%-retention identity, per token: with every candidate of C(L_t) selected, token t's
+    sparse state is all of [0, L_t), so it equals the verification's token t."""
+    Hq, Hkv, D, P, S, W, L, T = 8, 2, 64, 16, 4, 24, 300, 6
+    g = syn.rng(3, 93)
+    kv = syn.make_paged_kv(g, [L], Hkv, D, P)
+    pr = kv.page_table[0]
+    q = syn.normal_bf16(g, (T, Hq, D))
+    t = 0 if which == "first" else T - 1
+    Lt = L - T + t + 1
+    nC = Lt - W - S
+    idx = np.tile(np.arange(S, Lt - W, dtype=np.int32), (Hkv, 1))
+    ck, cv = oracle_lib.compact(kv.k_pool, kv.v_pool, pr, Lt, S, idx, nC, Hkv, D, P, S + nC)
+    fo, fl = oracle_lib.fast_multi_attn(q, ck, cv, nC, kv.k_pool, kv.v_pool, pr, L, T, S, W, Hq, Hkv, D, P)
+    vo, vl = oracle_lib.verify_attn(q, kv.k_pool, kv.v_pool, pr, L, T, Hq, Hkv, D, P)
+    np.testing.assert_allclose(fo[t], vo[t], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(fl[t], vl[t], rtol=0, atol=1e-12)
+    other = T - 1 - t
+    assert np.abs(fo[other] - vo[other]).max() > 1e-4  # the others miss part of their context
+
+
+@pytest.mark.parametrize("T,W", [(5, 2), (4, 40), (1, 20)])
+def test_verify_scores_closed_form_and_mask(oracle_lib, T, W):
+    """q_{t, kv*G+g} = c_{t,kv,g} e_g and k_j = [j mod 7, 1, 0...]: the statistic of candidate j is
+    (sum over the tokens that see j of c_{t,kv,0} (j mod 7) + c_{t,kv,1}) / 8 on [S, L - W)."""
+    Hq, Hkv, D, P, L, S = 4, 2, 64, 16, 90, 5
+    G = Hq // Hkv
+    g = syn.rng(3, 95 + T)
+    c = np.round(g.standard_normal((T, Hkv, G)) * 4) / 4  # exact in bf16
+    page_row, kp, _ = _position_coded_kv(L, Hkv, D, P, seed=19)
+    for kv in range(Hkv):
+        for j in range(L):
+            row = np.zeros(D)
+            row[0], row[1] = j % 7, 1.0
+            _set_row(kp, page_row, j, kv, P, row)
+    q = np.zeros((T, Hq, D))
+    for t in range(T):
+        for kv in range(Hkv):
+            for gg in range(G):
+                q[t, kv * G + gg, gg] = c[t, kv, gg]
+    stride = 96
+    sc = oracle_lib.verify_scores(syn.bf16_bits(q), kp, page_row, L, T, S, W, Hq, Hkv, D, P, stride=stride)
+    for kv in range(Hkv):
+        for j in range(stride):
+            if j >= L:
+                assert np.isnan(sc[kv, j])
+            elif S <= j < L - W:
+                seers = [t for t in range(T) if j < L - T + t + 1]
+                want = sum(c[t, kv, 0] * (j % 7) + c[t, kv, 1] for t in seers) / 8.0
+                assert sc[kv, j] == np.float32(want)
+            else:
+                assert sc[kv, j] == -np.inf
+    if T == 1:  # one token: the slow step's statistic
+        one = oracle_lib.group_scores(syn.bf16_bits(q[0]), kp, page_row, L, S, W, Hq, Hkv, D, P, stride=stride)
+        np.testing.assert_array_equal(sc, one)
+
+
+def test_append_tokens_writes_exactly_the_last_t_slots(oracle_lib):
+    Hkv, D, P, L, T = 2, 64, 16, 45, 7
+    g = syn.rng(6, 2)
+    kv = syn.make_paged_kv(g, [L - T], Hkv, D, P, capacity_tokens=[64])
+    kp, vp = kv.k_pool.copy(), kv.v_pool.copy()
+    kn, vn = syn.normal_bf16(g, (T, Hkv, D)), syn.normal_bf16(g, (T, Hkv, D))
+    oracle_lib.paged_append_tokens(kp, vp, kv.page_table[0], L, T, kn, vn, Hkv, D, P)
+    for t in range(T):
+        pos = L - T + t
+        page, slot = kv.page_table[0, pos // P], pos % P
+        assert np.array_equal(kp[page, :, slot], kn[t]) and np.array_equal(vp[page, :, slot], vn[t])
+        kp[page, :, slot] = kv.k_pool[page, :, slot]
+        vp[page, :, slot] = kv.v_pool[page, :, slot]
+    assert np.array_equal(kp, kv.k_pool) and np.array_equal(vp, kv.v_pool)
