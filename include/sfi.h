@@ -92,6 +92,10 @@ typedef enum {
  * written, only after it has finished. Without the flag nothing is read before then. */
 #define SFI_ATTN_EARLY_KV_PREFETCH 1u
 
+/* Most query tokens per request in the multi-token calls (tokens x G must also be
+ * <= 16: G = 2 allows 8 tokens, G = 4 four, G = 8 two). */
+#define SFI_MAX_QUERY_TOKENS 16
+
 /* Attention geometry shared by all calls. */
 typedef struct {
     int32_t num_q_heads;  /* Hq */
@@ -228,6 +232,75 @@ SFI_API sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_
  * device (0 when it needs none). */
 SFI_API size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_fast, int32_t n_slow,
                                         int32_t max_fast_tokens, int32_t max_dense_tokens);
+
+/*
+ * Multi-token calls. "A Sparse Glimpse of the Whole: Train-Free Self-Speculative
+ * Decoding" (abstract): drafts come from the target model itself over the sparse,
+ * recallable KV state; a full-context verification checks them and its per-head
+ * attention statistics are recycled as the importance signal, with no extra forward.
+ * Here a request carries T = num_tokens query tokens at positions L - T .. L - 1
+ * (L = seq_lens[r] counts them; their K/V must already be in the pages, e.g. by
+ * sfi_paged_kv_append_tokens). Query token t sees the context as it stands at length
+ * L_t = L - T + t + 1 (causal).
+ *   q   : bf16 [B][T][Hq][D], indexed by request id
+ *   out : fp32 [B][T][Hq][D], 8-byte aligned;  lse : fp32 [B][T][Hq] or NULL
+ * T x G > 16 returns SFI_ERR_UNSUPPORTED.
+ */
+
+/*
+ * sfi_paged_kv_append_tokens - sfi_paged_kv_append for the T newest tokens: token t
+ * of request r goes to position L_r - T + t.
+ *   k_new, v_new : bf16 [B][T][Hkv][D], indexed by request id
+ * Device errors: SFI_DEV_BAD_LEN (L < T), SFI_DEV_BAD_PAGE (that row is skipped).
+ */
+SFI_API sfi_status sfi_paged_kv_append_tokens(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
+                                              const void *v_new, int32_t num_tokens, const int32_t *req_ids,
+                                              int32_t batch, int32_t *dev_status, void *stream);
+
+/*
+ * sfi_dense_verify_attn - verification: token t of each request attends densely to
+ * positions [0, L_t). When scores is non-NULL it writes the recycled statistic, for
+ * every KV head kv:
+ *   scores[r][kv][j] = sum over tokens t with j < L_t, sum_{g < G} of
+ *                      scale * q_{t, kv*G+g} . k_{kv,j}          for j in [S, L - W)
+ *   scores[r][kv][j] = -inf                                      for other j < L
+ * (with T = 1 this is sfi_slow_dense_attn_with_scores). The Selector
+ * (sfi_select_topk) then refreshes the selection from it; run it with the accepted
+ * length, whose candidate set [S, L' - W) lies inside the scored one.
+ *   scores, score_stride : as for sfi_slow_dense_attn_with_scores
+ *   max_tokens : an upper bound on L + P over the batch (split planning only)
+ *   num_splits, flags : as for sfi_fast_decode_attn
+ *   workspace  : at least sfi_multi_workspace_size(shape, batch, T, max_tokens,
+ *                num_splits) bytes, zero-filled before first use (kept so).
+ * Device errors: SFI_DEV_BAD_LEN (also L < T, or L > score_stride), SFI_DEV_BAD_PAGE,
+ * SFI_DEV_TIMEOUT.
+ */
+SFI_API sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
+                                         int32_t recent, const void *q, int32_t num_tokens, float *out, float *lse,
+                                         float *scores, int64_t score_stride, const int32_t *req_ids, int32_t batch,
+                                         int32_t max_tokens, int32_t num_splits, uint32_t flags, void *workspace,
+                                         size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/*
+ * sfi_sparse_draft_attn - T draft tokens over the sparse state in one pass: token t
+ * sees exactly what sfi_fast_decode_attn at length L_t sees, compact rows
+ * [0, min(S, L_t) + count[r]) and the recent window [max(S, L_t - W), L_t); so the
+ * result equals T single-token fast steps. A non-empty selection (count[r] > 0)
+ * needs L - T + 1 >= S (else SFI_DEV_K_OVERFLOW).
+ *   max_tokens : an upper bound on S + max count + W + T + P (split planning only)
+ *   num_splits, flags, workspace : as for sfi_dense_verify_attn
+ * Device errors: those of sfi_fast_decode_attn.
+ */
+SFI_API sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
+                                         const sfi_compact_kv *compact, int32_t sink, int32_t recent, const void *q,
+                                         int32_t num_tokens, float *out, float *lse, const int32_t *req_ids,
+                                         int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
+                                         void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
+
+/* Workspace bytes the two multi-token attention calls need on the current device
+ * (0 when none; 0 also on invalid input). */
+SFI_API size_t sfi_multi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t num_tokens,
+                                        int32_t max_tokens, int32_t num_splits);
 
 /*
  * sfi_select_topk - the Selector (Figure 2 caption): for every (request r, KV

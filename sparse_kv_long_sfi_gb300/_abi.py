@@ -34,6 +34,7 @@ SFI_OK, SFI_ERR_INVALID_ARG, SFI_ERR_UNSUPPORTED, SFI_ERR_WORKSPACE, SFI_ERR_CUD
 SFI_DEV_BAD_PAGE, SFI_DEV_BAD_LEN, SFI_DEV_K_OVERFLOW = 1, 2, 4
 SFI_DEV_BAD_INDEX, SFI_DEV_TIMEOUT, SFI_DEV_BAD_COMPACT = 8, 16, 32
 SFI_ATTN_EARLY_KV_PREFETCH = 1
+SFI_MAX_QUERY_TOKENS = 16
 
 P_SHAPE = ctypes.POINTER(sfi_attn_shape)
 P_PAGED = ctypes.POINTER(sfi_paged_kv)
@@ -50,6 +51,12 @@ PROTOTYPES = {
                                       c_vp, c_i64, c_vp, c_i32, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_sz,
                                       c_vp, c_vp]),
     "sfi_mixed_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32, c_i32]),
+    "sfi_paged_kv_append_tokens": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp]),
+    "sfi_dense_verify_attn": (c_i32, [P_SHAPE, P_PAGED, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp,
+                                      c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_sparse_draft_attn": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp,
+                                      c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_multi_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32, c_i32]),
     "sfi_select_topk": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp,
                                 c_vp]),
     "sfi_compact_gather": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_i32, c_i32, P_COMPACT, c_vp, c_i32, c_vp,

@@ -17,6 +17,7 @@ from . import _abi
 
 
 SFI_ATTN_EARLY_KV_PREFETCH = _abi.SFI_ATTN_EARLY_KV_PREFETCH
+SFI_MAX_QUERY_TOKENS = _abi.SFI_MAX_QUERY_TOKENS
 
 
 class SFIError(RuntimeError):
@@ -198,6 +199,62 @@ def alloc_mixed_workspace(shape: AttnShape, batch: int, max_fast_tokens: int, ma
     fast and slow subsets."""
     n = max([256] + [sfi_mixed_workspace_size(shape, batch - ns, ns, max_fast_tokens, max_dense_tokens)
                      for ns in range(batch + 1)])
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def sfi_paged_kv_append_tokens(shape: AttnShape, kv: PagedKV, k_new: torch.Tensor, v_new: torch.Tensor,
+                               num_tokens: int, req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None,
+                               dev_status: Optional[torch.Tensor] = None, stream=None):
+    st = _abi.lib().sfi_paged_kv_append_tokens(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(v_new, torch.bfloat16, "v_new"), int(num_tokens), _ptr(req_ids, torch.int32, "req_ids"),
+        _batch(batch, req_ids, kv.seq_lens), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_paged_kv_append_tokens")
+
+
+def sfi_dense_verify_attn(shape: AttnShape, kv: PagedKV, sink: int, recent: int, q: torch.Tensor, num_tokens: int,
+                          out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          scores: Optional[torch.Tensor] = None, req_ids: Optional[torch.Tensor] = None,
+                          batch: Optional[int] = None, max_tokens: int = 0, num_splits: int = 0,
+                          workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
+                          stream=None, flags: int = 0):
+    ws = _ptr(workspace, torch.uint8, "workspace")
+    stride = 0 if scores is None else int(scores.shape[-1])
+    st = _abi.lib().sfi_dense_verify_attn(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), int(sink), int(recent), _ptr(q, torch.bfloat16, "q"),
+        int(num_tokens), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        _ptr(scores, torch.float32, "scores"), stride, _ptr(req_ids, torch.int32, "req_ids"),
+        _batch(batch, req_ids, kv.seq_lens), int(max_tokens), int(num_splits), int(flags), ws,
+        0 if workspace is None else workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_dense_verify_attn")
+
+
+def sfi_sparse_draft_attn(shape: AttnShape, kv: PagedKV, compact: CompactKV, sink: int, recent: int,
+                          q: torch.Tensor, num_tokens: int, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
+                          req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None, max_tokens: int = 0,
+                          num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
+                          dev_status: Optional[torch.Tensor] = None, stream=None, flags: int = 0):
+    ws = _ptr(workspace, torch.uint8, "workspace")
+    st = _abi.lib().sfi_sparse_draft_attn(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), ctypes.byref(compact.c()), int(sink), int(recent),
+        _ptr(q, torch.bfloat16, "q"), int(num_tokens), _ptr(out, torch.float32, "out"),
+        _ptr(lse, torch.float32, "lse"), _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens),
+        int(max_tokens), int(num_splits), int(flags), ws, 0 if workspace is None else workspace.numel(),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_sparse_draft_attn")
+
+
+def sfi_multi_workspace_size(shape: AttnShape, batch: int, num_tokens: int, max_tokens: int,
+                             num_splits: int = 0) -> int:
+    return int(_abi.lib().sfi_multi_workspace_size(ctypes.byref(shape.c()), int(batch), int(num_tokens),
+                                                   int(max_tokens), int(num_splits)))
+
+
+def alloc_multi_workspace(shape: AttnShape, batch: int, num_tokens: int, max_tokens: int, num_splits: int = 0,
+                          device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for the multi-token calls, valid for every batch size 1..batch."""
+    n = max([256] + [sfi_multi_workspace_size(shape, b, num_tokens, max_tokens, num_splits)
+                     for b in range(1, batch + 1)])
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 

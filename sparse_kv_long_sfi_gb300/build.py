@@ -15,8 +15,8 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(ROOT, "_build")
 LIB = os.path.join(HERE, "libsfi.so")
-SOURCES = ["attn_decode.cu", "select_topk.cu", "kv_copy.cu", "sfi_api.cu", "attn_noalloc.cu"]
-HEADERS = ["sfi_device.cuh", "sfi_internal.h"]
+SOURCES = ["attn_decode.cu", "attn_multi.cu", "select_topk.cu", "kv_copy.cu", "sfi_api.cu", "attn_noalloc.cu"]
+HEADERS = ["attn_kernel.cuh", "sfi_device.cuh", "sfi_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
                      "-I", os.path.join(ROOT, "include")]

@@ -1,0 +1,902 @@
+// Split-KV decode attention for SFI on sm_103a (kernel template, included by the
+// translation units that instantiate it): the fast step over the two-segment sparse
+// state, the slow step's dense attention with masked group-summed logits, the dense
+// full-KV baseline, and their multi-token forms (several query tokens per request:
+// drafting over the sparse state, verification over the whole context).
+//
+// Method: Slow-Fast Inference (Xie et al., 2026), Figure 2 caption (fast steps over
+// sink + selected + recent; slow steps run dense attention and collect masked
+// logits over the candidate set) and Figure 3 caption (B) (sink + selected packed
+// in a contiguous compact buffer, recent tokens read in place from paged KV). The
+// multi-token forms follow "A Sparse Glimpse of the Whole: Train-Free Self-Speculative
+// Decoding", abstract (drafts from the sparse, recallable KV state; full-context
+// verification whose per-head statistics are recycled as the importance signal).
+//
+// Design (HBM-bound: every K/V byte is read once per step):
+//  * Grid (split, KV head, request), two CTAs per SM. A (request, KV head) unit's
+//    token stream is cut into 16-token sub-blocks: compact rows first (fast mode),
+//    then the pages of the recent window (fast) or of [0, L) (dense). Split c owns a
+//    contiguous range of sub-blocks.
+//  * One producer warp issues TMA tensor loads (2-D tiled, 128-byte swizzle, L2
+//    evict-first) of K and V sub-blocks into a 96 KB ring of shared-memory stages;
+//    completion is tracked by mbarriers (transaction bytes). Page ids are fetched a
+//    chunk of 32 sub-blocks ahead by the whole producer warp.
+//  * Four consumer warps each own one sub-block per stage. QK^T and PV run on the
+//    tensor cores with mma.sync m16n8k16 (bf16 in, fp32 accumulate): the G <= 8
+//    query rows of the KV head form the M = 16 tile, so K and V never pass through
+//    CUDA-core unpacking. Online softmax in fp32 on the C fragments. The multi-token
+//    form (MQ) fills all 16 rows with T tokens x G heads (row = t * G + g), each row
+//    with its own causal / window bounds, at the same number of mma instructions.
+//  * The slow step sums the C fragments over the group's rows with warp shuffles and
+//    writes the fp32 masked scores.
+//  * With k_new/v_new the consumer warp owning position L - 1 writes the current token
+//    into its tile and into the page (the append fused into the attention).
+//  * Warps merge through shared memory. Splits of a unit merge in-kernel: with up to
+//    8 splits the unit's CTAs form one thread-block cluster and rank 0 reads the
+//    others' partial (m, l, o) states through distributed shared memory; with more,
+//    the last CTA of the unit (atomic counter, self-resetting) merges them from a
+//    global workspace.
+//  * Every wait on the pipeline or on a peer CTA is bounded and reports
+//    SFI_DEV_TIMEOUT instead of hanging.
+#pragma once
+
+#include <atomic>
+
+#include "sfi_device.cuh"
+#include "sfi_internal.h"
+
+namespace sfi {
+
+template <int D>
+struct AttnTile {
+    static constexpr int kBoxes = D / 64;                        // 128-byte boxes per row
+    static constexpr int kSubBytes = kSubTokens * D * 2;         // K (or V) of one sub-block
+    static constexpr int kStageBytes = kConsumerWarps * 2 * kSubBytes;
+    static constexpr int kRingBytes = 96 * 1024;                 // two CTAs per SM
+    static constexpr int kStages = kRingBytes / kStageBytes;
+    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    static constexpr int kKSteps = D / 16;                       // mma k-steps of QK^T
+    static constexpr int kNTiles = D / 8;                        // mma n-tiles of PV
+    static constexpr int kMergeStride = D + 4;                   // padded rows of the warp-merge scratch
+};
+
+constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+constexpr float kLn2 = 0.6931471805599453f;
+
+__device__ __forceinline__ void consumer_bar_sync() {
+    asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Geometry of one (request, KV head) unit's token stream.
+struct UnitStream {
+    int L;         // current length (all query tokens appended)
+    int L0;        // length seen by the first query token: L - tokens + 1
+    int cnt;       // selected rows in the compact buffer (fast mode)
+    int n1;        // compact rows streamed (fast mode)
+    int nb1;       // compact sub-blocks (fast mode)
+    int page0;     // first page of the paged segment
+    int lo_pos;    // first valid position of the paged segment
+    int nb;        // total sub-blocks
+    int64_t crow0; // first compact row of this KV head (fast mode)
+    int sb_app;    // sub-block holding position L - 1 (the current token)
+    int row_app;   // its row inside that sub-block
+};
+
+// `lead` marks one CTA per request, which reports the request's errors.
+__device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh, bool fast, bool lead,
+                                            UnitStream &u) {
+    // All per-request metadata is loaded up front, in one round trip.
+    u.L = p.seq_lens[r];
+    u.L0 = u.L - p.tokens + 1;
+    const int cnt = fast ? p.c_count[r] : 0;
+    u.cnt = cnt;
+    const int cap = fast ? p.c_capacity[r] : 0;
+    const int64_t off = fast ? p.c_row_offset[r] : 0;
+    lead = lead && threadIdx.x == 0 && kvh == 0;
+    if (u.L0 < 1 || u.L > p.max_pages * kSubTokens) {
+        if (lead) report(p.dev_status, SFI_DEV_BAD_LEN);
+        return false;
+    }
+    if (fast) {
+        const int ns = min(p.sink, u.L);
+        if (cnt < 0 || cnt > cap - p.sink || (cnt > 0 && u.L0 < p.sink)) {
+            if (lead) report(p.dev_status, SFI_DEV_K_OVERFLOW);
+            return false;
+        }
+        if (off < 0 || off + (int64_t)p.hkv * cap > p.c_total_rows) {
+            if (lead) report(p.dev_status, SFI_DEV_BAD_COMPACT);
+            return false;
+        }
+        u.crow0 = off + (int64_t)kvh * cap;
+        u.n1 = ns + cnt;
+        u.nb1 = (u.n1 + kSubTokens - 1) / kSubTokens;
+        const int rs = max(p.sink, u.L0 - p.recent);  // the first token's window starts lowest
+        if (rs < u.L) {
+            u.lo_pos = rs;
+            u.page0 = rs / kSubTokens;
+            u.nb = u.nb1 + ((u.L - 1) / kSubTokens - u.page0 + 1);
+            u.sb_app = u.nb1 + ((u.L - 1) / kSubTokens - u.page0);  // last page of the recent window
+        } else {
+            u.lo_pos = u.L;
+            u.page0 = 0;
+            u.nb = u.nb1;
+            u.sb_app = (u.L - 1) / kSubTokens;  // L <= S: the current token is a sink row
+        }
+    } else {
+        u.crow0 = 0;
+        u.n1 = 0;
+        u.nb1 = 0;
+        u.lo_pos = 0;
+        u.page0 = 0;
+        u.nb = (u.L + kSubTokens - 1) / kSubTokens;
+        u.sb_app = u.nb - 1;
+    }
+    u.row_app = (u.L - 1) % kSubTokens;
+    return true;
+}
+
+// Process one 16-token sub-block held in shared memory (K at kaddr, V at vaddr,
+// each kBoxes boxes of [16 rows][128 B] with the 128-byte swizzle).
+template <int D, bool SCORES>
+__device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr, int lo, int hi, int pos0,
+                                                  const uint32_t (&qa)[D / 16][2], float (&o)[D / 8][4],
+                                                  float &m_run, float &l_run, const AttnParams &p, float *score_row,
+                                                  int L, int lane) {
+    using T = AttnTile<D>;
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, r8 = lane & 7;
+
+    // S = Q K^T for 16 tokens: two n-tiles (tokens 0-7 and 8-15).
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+        const int tok = ((mi >> 1) << 3) + r8;
+        const uint32_t row_addr = kaddr + tok * 128;
+#pragma unroll
+        for (int ks = 0; ks < T::kKSteps; ++ks) {
+            const int box = ks >> 2;
+            const int chunk = ((ks & 3) << 1) + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
+            mma_bf16_16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
+    }
+    const int tk0 = 2 * t, tk1 = 2 * t + 1, tk2 = 8 + 2 * t, tk3 = 9 + 2 * t;
+
+    if (SCORES) {
+        // Group sum over the 8 query rows (rows >= G hold zero queries, so they add 0).
+        float v0 = s[0][0], v1 = s[0][1], v2 = s[1][0], v3 = s[1][1];
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+            v0 += __shfl_xor_sync(0xffffffffu, v0, off);
+            v1 += __shfl_xor_sync(0xffffffffu, v1, off);
+            v2 += __shfl_xor_sync(0xffffffffu, v2, off);
+            v3 += __shfl_xor_sync(0xffffffffu, v3, off);
+        }
+        if (g == 0 && score_row != nullptr) {
+            const int c_lo = p.sink, c_hi = L - p.recent;
+            const float vv[4] = {v0, v1, v2, v3};
+            const int tk[4] = {tk0, tk1, tk2, tk3};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pos = pos0 + tk[i];
+                if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? vv[i] * p.scale : -INFINITY;
+            }
+        }
+    }
+
+    const bool full = (lo == 0 && hi == kSubTokens);
+    float x0 = s[0][0] * p.scale_log2, x1 = s[0][1] * p.scale_log2;
+    float x2 = s[1][0] * p.scale_log2, x3 = s[1][1] * p.scale_log2;
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (!full) {
+        const bool ok0 = tk0 >= lo && tk0 < hi, ok1 = tk1 >= lo && tk1 < hi;
+        const bool ok2 = tk2 >= lo && tk2 < hi, ok3 = tk3 >= lo && tk3 < hi;
+        x0 = ok0 ? x0 : -INFINITY;
+        x1 = ok1 ? x1 : -INFINITY;
+        x2 = ok2 ? x2 : -INFINITY;
+        x3 = ok3 ? x3 : -INFINITY;
+        // V rows of masked tokens may hold anything (even NaN): zero them in the B fragments.
+        vm0 = (ok0 ? 0x0000ffffu : 0u) | (ok1 ? 0xffff0000u : 0u);
+        vm1 = (ok2 ? 0x0000ffffu : 0u) | (ok3 ? 0xffff0000u : 0u);
+    }
+    float mt = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 1));
+    mt = fmaxf(mt, __shfl_xor_sync(0xffffffffu, mt, 2));
+    const float m_new = fmaxf(m_run, mt);
+    const float base = (m_new == -INFINITY) ? 0.f : m_new;
+    const float alpha = fast_exp2(m_run - base);
+    const float p0 = fast_exp2(x0 - base), p1 = fast_exp2(x1 - base);
+    const float p2 = fast_exp2(x2 - base), p3 = fast_exp2(x3 - base);
+    l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
+    m_run = m_new;
+#pragma unroll
+    for (int nt = 0; nt < T::kNTiles; ++nt) {
+        o[nt][0] *= alpha;
+        o[nt][1] *= alpha;
+    }
+    // P enters the PV product as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), so
+    // the weights carry about 16 significant bits instead of bf16's 8.
+    const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
+    const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
+    const __nv_bfloat162 l01 = __floats2bfloat162_rn(p0 - __low2float(h01), p1 - __high2float(h01));
+    const __nv_bfloat162 l23 = __floats2bfloat162_rn(p2 - __low2float(h23), p3 - __high2float(h23));
+    const uint32_t pa0 = *reinterpret_cast<const uint32_t *>(&h01);
+    const uint32_t pa2 = *reinterpret_cast<const uint32_t *>(&h23);
+    const uint32_t pl0 = *reinterpret_cast<const uint32_t *>(&l01);
+    const uint32_t pl2 = *reinterpret_cast<const uint32_t *>(&l23);
+
+    // O += P V: V sub-block as the B operand via ldmatrix.trans.
+    {
+        const int tok = ((mi & 1) << 3) + r8;
+        const uint32_t row_addr = vaddr + tok * 128;
+#pragma unroll
+        for (int j = 0; j < T::kNTiles / 2; ++j) {
+            const int box = j >> 2;
+            const int chunk = ((j & 3) << 1) + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
+            if (!full) {
+                b0 &= vm0;
+                b1 &= vm1;
+                b2 &= vm0;
+                b3 &= vm1;
+            }
+            mma_bf16_16816(o[2 * j], pa0, 0u, pa2, 0u, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], pa0, 0u, pa2, 0u, b2, b3);
+            mma_bf16_16816(o[2 * j], pl0, 0u, pl2, 0u, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], pl0, 0u, pl2, 0u, b2, b3);
+        }
+    }
+}
+
+// Bounds [lo, hi) of the tokens of a 16-token sub-block that one query row sees.
+struct RowSpan {
+    int lo, hi;
+};
+
+// Multi-token form of consume_sub_block: all 16 rows of the tile are query rows; this
+// lane holds rows g (span ra) and g + 8 (span rb). `full` (warp-uniform) says every
+// row sees all 16 tokens; [lo, hi) is the union of the rows' spans.
+template <int D, bool SCORES>
+__device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t vaddr, int lo, int hi, bool full,
+                                                     RowSpan ra, RowSpan rb, int pos0,
+                                                     const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
+                                                     float (&m_run)[2], float (&l_run)[2], const AttnParams &p,
+                                                     float *score_row, int L, int lane) {
+    using T = AttnTile<D>;
+    const int g = lane >> 2, t = lane & 3;
+    const int mi = lane >> 3, r8 = lane & 7;
+
+    float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+        const int tok = ((mi >> 1) << 3) + r8;
+        const uint32_t row_addr = kaddr + tok * 128;
+#pragma unroll
+        for (int ks = 0; ks < T::kKSteps; ++ks) {
+            const int box = ks >> 2;
+            const int chunk = ((ks & 3) << 1) + (mi & 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
+            mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        }
+    }
+    // this lane's tokens, and its elements of rows g (xa) and g + 8 (xb)
+    const int tk[4] = {2 * t, 2 * t + 1, 8 + 2 * t, 9 + 2 * t};
+    float xa[4] = {s[0][0], s[0][1], s[1][0], s[1][1]};
+    float xb[4] = {s[0][2], s[0][3], s[1][2], s[1][3]};
+    bool oka[4], okb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        oka[i] = full || (tk[i] >= ra.lo && tk[i] < ra.hi);
+        okb[i] = full || (tk[i] >= rb.lo && tk[i] < rb.hi);
+    }
+
+    if (SCORES) {
+        // Sum over every (token, head) row that sees the position (padding rows hold
+        // zero queries and add 0).
+        float v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) v[i] = (oka[i] ? xa[i] : 0.f) + (okb[i] ? xb[i] : 0.f);
+#pragma unroll
+        for (int off = 4; off < 32; off <<= 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], off);
+        }
+        if (g == 0 && score_row != nullptr) {
+            const int c_lo = p.sink, c_hi = L - p.recent;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const int pos = pos0 + tk[i];
+                if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? v[i] * p.scale : -INFINITY;
+            }
+        }
+    }
+
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        xa[i] = oka[i] ? xa[i] * p.scale_log2 : -INFINITY;
+        xb[i] = okb[i] ? xb[i] * p.scale_log2 : -INFINITY;
+    }
+    uint32_t vm0 = 0xffffffffu, vm1 = 0xffffffffu;
+    if (!full) {
+        // V rows outside every row's span may hold anything (even NaN): zero them.
+        const bool u0 = tk[0] >= lo && tk[0] < hi, u1 = tk[1] >= lo && tk[1] < hi;
+        const bool u2 = tk[2] >= lo && tk[2] < hi, u3 = tk[3] >= lo && tk[3] < hi;
+        vm0 = (u0 ? 0x0000ffffu : 0u) | (u1 ? 0xffff0000u : 0u);
+        vm1 = (u2 ? 0x0000ffffu : 0u) | (u3 ? 0xffff0000u : 0u);
+    }
+    float ma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+    float mb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+    ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+    mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+    const float na = fmaxf(m_run[0], ma), nb = fmaxf(m_run[1], mb);
+    const float ba = (na == -INFINITY) ? 0.f : na, bb = (nb == -INFINITY) ? 0.f : nb;
+    const float alpha_a = fast_exp2(m_run[0] - ba), alpha_b = fast_exp2(m_run[1] - bb);
+    float pa[4], pb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        pa[i] = fast_exp2(xa[i] - ba);
+        pb[i] = fast_exp2(xb[i] - bb);
+    }
+    l_run[0] = l_run[0] * alpha_a + ((pa[0] + pa[1]) + (pa[2] + pa[3]));
+    l_run[1] = l_run[1] * alpha_b + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
+    m_run[0] = na;
+    m_run[1] = nb;
+#pragma unroll
+    for (int nt = 0; nt < T::kNTiles; ++nt) {
+        o[nt][0] *= alpha_a;
+        o[nt][1] *= alpha_a;
+        o[nt][2] *= alpha_b;
+        o[nt][3] *= alpha_b;
+    }
+    // P as two bf16 terms (hi + lo), rows g and g + 8 in the A fragment's halves.
+    uint32_t ph[4], pl[4];
+    {
+        const __nv_bfloat162 ha01 = __floats2bfloat162_rn(pa[0], pa[1]);
+        const __nv_bfloat162 hb01 = __floats2bfloat162_rn(pb[0], pb[1]);
+        const __nv_bfloat162 ha23 = __floats2bfloat162_rn(pa[2], pa[3]);
+        const __nv_bfloat162 hb23 = __floats2bfloat162_rn(pb[2], pb[3]);
+        const __nv_bfloat162 la01 = __floats2bfloat162_rn(pa[0] - __low2float(ha01), pa[1] - __high2float(ha01));
+        const __nv_bfloat162 lb01 = __floats2bfloat162_rn(pb[0] - __low2float(hb01), pb[1] - __high2float(hb01));
+        const __nv_bfloat162 la23 = __floats2bfloat162_rn(pa[2] - __low2float(ha23), pa[3] - __high2float(ha23));
+        const __nv_bfloat162 lb23 = __floats2bfloat162_rn(pb[2] - __low2float(hb23), pb[3] - __high2float(hb23));
+        ph[0] = *reinterpret_cast<const uint32_t *>(&ha01);
+        ph[1] = *reinterpret_cast<const uint32_t *>(&hb01);
+        ph[2] = *reinterpret_cast<const uint32_t *>(&ha23);
+        ph[3] = *reinterpret_cast<const uint32_t *>(&hb23);
+        pl[0] = *reinterpret_cast<const uint32_t *>(&la01);
+        pl[1] = *reinterpret_cast<const uint32_t *>(&lb01);
+        pl[2] = *reinterpret_cast<const uint32_t *>(&la23);
+        pl[3] = *reinterpret_cast<const uint32_t *>(&lb23);
+    }
+    {
+        const int tok = ((mi & 1) << 3) + r8;
+        const uint32_t row_addr = vaddr + tok * 128;
+#pragma unroll
+        for (int j = 0; j < T::kNTiles / 2; ++j) {
+            const int box = j >> 2;
+            const int chunk = ((j & 3) << 1) + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
+            if (!full) {
+                b0 &= vm0;
+                b1 &= vm1;
+                b2 &= vm0;
+                b3 &= vm1;
+            }
+            mma_bf16_16816(o[2 * j], ph[0], ph[1], ph[2], ph[3], b0, b1);
+            mma_bf16_16816(o[2 * j + 1], ph[0], ph[1], ph[2], ph[3], b2, b3);
+            mma_bf16_16816(o[2 * j], pl[0], pl[1], pl[2], pl[3], b0, b1);
+            mma_bf16_16816(o[2 * j + 1], pl[0], pl[1], pl[2], pl[3], b2, b3);
+        }
+    }
+}
+
+// Write the current token's K/V (k_new/v_new of this KV head) into row u.row_app of
+// the swizzled K and V tiles at `tile` and into the paged cache at position L - 1.
+// One 16-byte chunk per lane; the writing lanes then order their generic-proxy
+// shared-memory writes before later TMA (async-proxy) writes into the same stage.
+template <int D>
+__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
+                                                   const UnitStream &u, int lane) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const int64_t src_off = ((int64_t)r * p.hkv + kvh) * D + c * 8;
+        const int4 val = *reinterpret_cast<const int4 *>((is_v ? p.v_new : p.k_new) + src_off);
+        const int row = u.row_app;
+        uint8_t *base = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128) + row * 128;
+        *reinterpret_cast<int4 *>(base + (((c & 7) ^ (row & 7)) << 4)) = val;
+        const int pos = u.L - 1;
+        const int page = p.page_table[(int64_t)r * p.max_pages + pos / kSubTokens];
+        if (page < 0 || page >= p.num_pages) {
+            if (lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
+        } else {
+            __nv_bfloat16 *dst = (is_v ? p.v_pool_w : p.k_pool_w) +
+                                 (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D + c * 8;
+            *reinterpret_cast<int4 *>(dst) = val;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+}
+
+// MQ: p.tokens query tokens per request (rows = tokens x G <= 16), no fused append.
+template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>
+__global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
+    attn_decode_kernel(const __grid_constant__ CUtensorMap tm_pool_k, const __grid_constant__ CUtensorMap tm_pool_v,
+                       const __grid_constant__ CUtensorMap tm_comp_k, const __grid_constant__ CUtensorMap tm_comp_v,
+                       const AttnParams p) {
+    using T = AttnTile<D>;
+    constexpr int kRows = MQ ? kMaxRows : kMaxGroup;  // query rows per unit in the merge buffers
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    __shared__ __align__(8) uint64_t full_bar[T::kStages];
+    __shared__ __align__(8) uint64_t empty_bar[T::kStages];
+    __shared__ __align__(8) uint64_t merge_bar;  // cluster merge handshake
+    __shared__ int2 s_info[T::kStages][kConsumerWarps];
+    __shared__ int s_last;
+    __shared__ int s_timeout;
+
+    // ---- this CTA's work item: (request, KV head, split) and the unit's mode ----
+    int split, kvh, b, splits;
+    bool fast;
+    int64_t unit, slot0;  // merge counter index; first partial slot of the unit
+    const int *ids = p.req_ids;
+    if (MODE == kModeMixed) {
+        // 1-D grid: the slow units' splits first, then the fast units'
+        int item = blockIdx.x;
+        const int n_slow_items = p.n_slow * p.hkv * p.slow_splits;
+        fast = item >= n_slow_items;
+        splits = fast ? p.fast_splits : p.slow_splits;
+        if (fast) item -= n_slow_items;
+        split = item % splits;
+        const int u_local = item / splits;
+        kvh = u_local % p.hkv;
+        b = u_local / p.hkv;
+        ids = fast ? p.fast_ids : p.slow_ids;
+        unit = fast ? (int64_t)p.n_slow * p.hkv + u_local : u_local;
+        slot0 = fast ? (int64_t)p.n_slow * p.hkv * p.slow_splits + (int64_t)u_local * splits : (int64_t)u_local * splits;
+    } else {
+        split = blockIdx.x;
+        kvh = blockIdx.y;
+        b = blockIdx.z;
+        splits = p.splits;
+        fast = MODE == kModeFast;
+        unit = (int64_t)b * p.hkv + kvh;
+        slot0 = unit * splits;
+    }
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        tma_prefetch_desc(&tm_pool_k);
+        tma_prefetch_desc(&tm_pool_v);
+        if (MODE != kModeDense) {
+            tma_prefetch_desc(&tm_comp_k);
+            tma_prefetch_desc(&tm_comp_v);
+        }
+    }
+    // Programmatic dependent launch: this CTA may have started while the previous
+    // kernel in the stream was still running. By default it waits for that kernel
+    // (and its memory) before touching any global data. With early_prefetch the
+    // caller guarantees that kernel writes none of the KV state read below, so only
+    // the consumer warps wait, right before they read q and write anything. The next
+    // kernel is released only after this CTA's wait, so at most two kernels overlap.
+    if (!p.early_prefetch) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
+    const int r = ids ? ids[b] : b;
+
+    UnitStream u;
+    if (!unit_stream(p, r, kvh, fast, split == 0, u)) return;  // uniform across the CTA and its cluster
+    const int per = (u.nb + splits - 1) / splits;
+    const int sb_begin = split * per;
+    const int sb_end = min(u.nb, sb_begin + per);
+    const int n_my = max(0, sb_end - sb_begin);
+    const int n_stages = (n_my + kConsumerWarps - 1) / kConsumerWarps;
+
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < T::kStages; ++i) {
+            mbar_init(&full_bar[i], kConsumerWarps);
+            mbar_init(&empty_bar[i], kConsumerWarps);
+        }
+        if (CLUSTER) mbar_init(&merge_bar, split == 0 ? splits - 1 : 1);
+        s_timeout = 0;
+        fence_barrier_init();
+    }
+    // Every CTA of a cluster reaches this point unconditionally (the only branch
+    // before it depends on the unit's metadata, which all of them read alike): after
+    // it, each CTA's merge barrier is initialised for remote arrivals.
+    if (CLUSTER) cluster_sync_all();
+    else __syncthreads();
+
+    if (warp == kConsumerWarps) {
+        // ---------------- producer warp ----------------
+        const uint64_t policy = l2_policy_evict_first();
+        const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+        // Page id of sub-block sb (-1 for compact sub-blocks and past the end).
+        auto page_of = [&](int sb) -> int {
+            if (sb >= sb_end || sb < u.nb1) return -1;
+            return ptab[u.page0 + (sb - u.nb1)];
+        };
+        int cur = page_of(sb_begin + lane);
+        int nxt = page_of(sb_begin + 32 + lane);
+        for (int st = 0; st < n_stages; ++st) {
+            if (st > 0 && (st & 7) == 0) {  // 8 stages x 4 sub-blocks = 32 page ids per chunk
+                cur = nxt;
+                nxt = page_of(sb_begin + (st / 8 + 1) * 32 + lane);
+            }
+            const int slot = st % T::kStages;
+            if (st >= T::kStages) {
+                if (!mbar_wait_warp(&empty_bar[slot], ((st / T::kStages) - 1) & 1)) {
+                    if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+                    break;
+                }
+            }
+            const int page = __shfl_sync(0xffffffffu, cur, ((st & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
+            if (lane < kConsumerWarps) {
+                const int sb = sb_begin + st * kConsumerWarps + lane;
+                int lo = 0, hi = 0, pos0 = 0;
+                const CUtensorMap *mk = &tm_pool_k;
+                const CUtensorMap *mv = &tm_pool_v;
+                int32_t y = 0;
+                if (sb < sb_end) {
+                    if (sb < u.nb1) {  // compact segment (fast mode only)
+                        mk = &tm_comp_k;
+                        mv = &tm_comp_v;
+                        y = static_cast<int32_t>(u.crow0 + (int64_t)sb * kSubTokens);
+                        hi = min(kSubTokens, u.n1 - sb * kSubTokens);
+                        pos0 = -1;
+                    } else {
+                        const int pg = u.page0 + (sb - u.nb1);
+                        if (page < 0 || page >= p.num_pages) {
+                            report(p.dev_status, SFI_DEV_BAD_PAGE);
+                        } else {
+                            y = (page * p.hkv + kvh) * kSubTokens;
+                            pos0 = pg * kSubTokens;
+                            lo = max(0, u.lo_pos - pos0);
+                            hi = min(kSubTokens, u.L - pos0);
+                        }
+                    }
+                }
+                s_info[slot][lane] = make_int2(lo | (hi << 16), pos0);
+                if (hi > lo) {
+                    uint8_t *kdst = smem + slot * T::kStageBytes + lane * 2 * T::kSubBytes;
+                    uint8_t *vdst = kdst + T::kSubBytes;
+                    mbar_arrive_expect_tx(&full_bar[slot], 2 * T::kSubBytes);
+#pragma unroll
+                    for (int bx = 0; bx < T::kBoxes; ++bx) {
+                        tma_load_2d(kdst + bx * (kSubTokens * 128), mk, bx * 64, y, &full_bar[slot], policy);
+                        tma_load_2d(vdst + bx * (kSubTokens * 128), mv, bx * 64, y, &full_bar[slot], policy);
+                    }
+                } else {
+                    mbar_arrive(&full_bar[slot]);
+                }
+            }
+        }
+        return;  // the producer takes no part in the merges
+    }
+
+    // ---------------- consumer warps ----------------
+    if (p.early_prefetch) {
+        grid_dependency_wait();
+        grid_launch_dependents();
+    }
+    const int g = lane >> 2, t = lane & 3;
+    const int G = p.group;
+    uint32_t qa[D / 16][MQ ? 4 : 2];
+    if constexpr (MQ) {
+        // rows g (A-fragment registers 0, 2) and g + 8 (registers 1, 3); row rho is
+        // query token rho / G, head rho % G of this KV head's group
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int rho = g + 8 * half;
+            const int tok = rho / G;
+            const __nv_bfloat16 *qrow =
+                p.q + (((int64_t)r * p.tokens + tok) * p.hq + (int64_t)kvh * G + (rho - tok * G)) * D;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks) {
+                if (rho < p.rows) {
+                    qa[ks][half] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * t);
+                    qa[ks][2 + half] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * t);
+                } else {
+                    qa[ks][half] = 0u;
+                    qa[ks][2 + half] = 0u;
+                }
+            }
+        }
+    } else {
+        const __nv_bfloat16 *qrow = p.q + ((int64_t)r * p.hq + (int64_t)kvh * G + g) * D;
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks) {
+            if (g < G) {
+                qa[ks][0] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * t);
+                qa[ks][1] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * t);
+            } else {
+                qa[ks][0] = 0u;
+                qa[ks][1] = 0u;
+            }
+        }
+    }
+    // Per-row bounds (MQ): the length token rho / G sees and the start of its recent
+    // window (0 in dense mode). Padding rows take the last token's.
+    int row_len[2] = {u.L, u.L}, row_lo[2] = {0, 0};
+    if constexpr (MQ) {
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int rho = min(g + 8 * half, p.rows - 1);
+            row_len[half] = u.L0 + rho / G;
+            row_lo[half] = fast ? max(p.sink, row_len[half] - p.recent) : 0;
+        }
+    }
+    float o[D / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < D / 8; ++nt) o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // rows g and g + 8 (MQ)
+    float *score_row = nullptr;
+    if (SCORES && p.scores && !fast) {
+        if (u.L <= p.score_stride) {
+            score_row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride;
+        } else if (threadIdx.x == 0 && split == 0) {
+            report(p.dev_status, SFI_DEV_BAD_LEN);  // score row too short: scores not written
+        }
+    }
+
+    bool timed_out = false;
+    for (int st = 0; st < n_stages; ++st) {
+        const int slot = st % T::kStages;
+        if (!mbar_wait_warp(&full_bar[slot], (st / T::kStages) & 1)) {
+            timed_out = true;
+            break;
+        }
+        const int2 in = s_info[slot][warp];
+        const int lo = in.x & 0xffff, hi = in.x >> 16;
+        if (!MQ && p.k_new != nullptr && sb_begin + st * kConsumerWarps + warp == u.sb_app) {
+            // Fused append: the current token's K/V replace row L - 1 of this tile (the
+            // attention sees the cache after the append) and are written to the pages.
+            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane);
+        }
+        if (hi > lo) {
+            const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);
+            if constexpr (MQ) {
+                RowSpan ra, rb;
+                if (in.y >= 0) {  // paged positions pos0 + i
+                    ra = RowSpan{max(lo, row_lo[0] - in.y), min(hi, row_len[0] - in.y)};
+                    rb = RowSpan{max(lo, row_lo[1] - in.y), min(hi, row_len[1] - in.y)};
+                } else {  // compact rows: without a selection they are the sink positions
+                    const int c0 = (sb_begin + st * kConsumerWarps + warp) * kSubTokens;
+                    ra = RowSpan{lo, u.cnt > 0 ? hi : min(hi, row_len[0] - c0)};
+                    rb = RowSpan{lo, u.cnt > 0 ? hi : min(hi, row_len[1] - c0)};
+                }
+                const bool full = __all_sync(0xffffffffu, ra.lo == 0 && ra.hi == kSubTokens && rb.lo == 0 &&
+                                                              rb.hi == kSubTokens);
+                consume_sub_block_mq<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, full, ra, rb, in.y, qa, o,
+                                                m_run, l_run, p, score_row, u.L, lane);
+            } else {
+                consume_sub_block<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, in.y, qa, o, m_run[0], l_run[0],
+                                             p, score_row, u.L, lane);
+            }
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty_bar[slot]);
+    }
+    if (timed_out && lane == 0) {
+        report(p.dev_status, SFI_DEV_TIMEOUT);
+        s_timeout = 1;
+    }
+#pragma unroll
+    for (int half = 0; half < 2; ++half) {
+        l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 1);
+        l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 2);
+    }
+
+    // ---- merge the consumer warps through shared memory (stage buffers are free now) ----
+    consumer_bar_sync();
+    const bool ok = s_timeout == 0;
+    constexpr int MS = T::kMergeStride;
+    float *sm_o = reinterpret_cast<float *>(smem);                  // [warps][kRows][MS]
+    float *sm_m = sm_o + kConsumerWarps * kRows * MS;               // [warps][kRows]
+    float *sm_l = sm_m + kConsumerWarps * kRows;                    // [warps][kRows]
+    float *cp_o = sm_l + kConsumerWarps * kRows;                    // [kRows][D]  this CTA's partial (cluster merge)
+    float *cp_m = cp_o + kRows * D;                                 // [kRows]
+    float *cp_l = cp_m + kRows;                                     // [kRows]
+    if (ok) {
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) {
+            float2 v = make_float2(o[nt][0], o[nt][1]);
+            *reinterpret_cast<float2 *>(&sm_o[(warp * kRows + g) * MS + nt * 8 + 2 * t]) = v;
+            if (MQ) {
+                float2 w = make_float2(o[nt][2], o[nt][3]);
+                *reinterpret_cast<float2 *>(&sm_o[(warp * kRows + g + 8) * MS + nt * 8 + 2 * t]) = w;
+            }
+        }
+        if (t == 0) {
+            sm_m[warp * kRows + g] = m_run[0];
+            sm_l[warp * kRows + g] = l_run[0];
+            if (MQ) {
+                sm_m[warp * kRows + g + 8] = m_run[1];
+                sm_l[warp * kRows + g + 8] = l_run[1];
+            }
+        }
+    }
+    consumer_bar_sync();
+
+    const int ctid = threadIdx.x;  // 0 .. 127
+    const int rows = MQ ? p.rows : G;
+    // output row of tile row `row`: (request, token row / G, head kvh * G + row % G)
+    const int64_t head0 = (int64_t)r * p.hq + (int64_t)kvh * G;
+    auto out_row = [&](int row) -> int64_t {
+        if (!MQ) return head0 + row;
+        const int tok = row / G;
+        return ((int64_t)r * p.tokens + tok) * p.hq + (int64_t)kvh * G + (row - tok * G);
+    };
+    if (ok) {
+        for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
+            const int row = e / D, d = e - (e / D) * D;
+            float M = -INFINITY;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kRows + row]);
+            float acc = 0.f, lsum = 0.f;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float mw = sm_m[w * kRows + row];
+                if (mw != -INFINITY) {
+                    const float f = fast_exp2(mw - M);
+                    acc += sm_o[(w * kRows + row) * MS + d] * f;
+                    lsum += sm_l[w * kRows + row] * f;
+                }
+            }
+            if (splits == 1) {
+                p.out[out_row(row) * D + d] = acc / lsum;
+                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+            } else if (CLUSTER) {
+                cp_o[row * D + d] = acc;
+                if (d == 0) {
+                    cp_m[row] = M;
+                    cp_l[row] = lsum;
+                }
+            } else {
+                const int64_t slot = (slot0 + split) * kRows + row;
+                p.ws_part[slot * D + d] = acc;
+                if (d == 0) {
+                    p.ws_ml[slot * 2 + 0] = M;
+                    p.ws_ml[slot * 2 + 1] = lsum;
+                }
+            }
+        }
+    }
+    if (splits == 1) return;
+
+    if (CLUSTER) {
+        // ---- split merge inside the cluster, through distributed shared memory ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        if (split != 0) {
+            if (ctid == 0) {
+                mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), 0));  // "my partial is ready"
+                // Stay alive (shared memory readable) until rank 0 has read it.
+                if (!mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            }
+            return;
+        }
+        if (ctid == 0) s_last = mbar_wait_cluster_bounded(&merge_bar, 0) ? 1 : 0;
+        consumer_bar_sync();
+        if (s_last && ok) {
+            // Each thread merges pairs of outputs. All loads from the peers' shared
+            // memory are issued before any is used, so their latencies overlap.
+            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+                float2 os[kMaxClusterSplits];
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < splits) {
+                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
+                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
+                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
+                    }
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s)
+                    if (s < splits) M = fmaxf(M, ms[s]);
+                float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < splits && ls[s] > 0.f) {
+                        const float f = fast_exp2(ms[s] - M);
+                        ax += os[s].x * f;
+                        ay += os[s].y * f;
+                        lsum += ls[s] * f;
+                    }
+                }
+                *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
+                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+            }
+        }
+        if (!s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
+        consumer_bar_sync();  // every read of the peers' shared memory is done
+        if (ctid > 0 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
+        return;
+    }
+
+    // ---- split merge by the last CTA of this unit, through the global workspace ----
+    if (!ok) return;
+    __threadfence();
+    consumer_bar_sync();
+    if (ctid == 0) {
+        const int prev = atomicAdd(&p.ws_count[unit], 1);
+        s_last = (prev == splits - 1);
+    }
+    consumer_bar_sync();
+    if (!s_last) return;
+    __threadfence();
+    for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
+        const int row = e / D, d = e - (e / D) * D;
+        float M = -INFINITY;
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[((slot0 + s) * kRows + row) * 2]));
+        float acc = 0.f, lsum = 0.f;
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) {
+            const int64_t slot = (slot0 + s) * kRows + row;
+            const float ls = __ldcg(&p.ws_ml[slot * 2 + 1]);
+            if (ls > 0.f) {
+                const float f = fast_exp2(__ldcg(&p.ws_ml[slot * 2]) - M);
+                acc += __ldcg(&p.ws_part[slot * D + d]) * f;
+                lsum += ls * f;
+            }
+        }
+        p.out[out_row(row) * D + d] = acc / lsum;
+        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+    }
+    if (ctid == 0) p.ws_count[unit] = 0;  // leave the workspace zeroed for the next launch
+}
+
+template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>
+static cudaError_t launch_one(const AttnMaps &maps, const AttnParams &p, int batch, cudaStream_t stream) {
+    using T = AttnTile<D>;
+    auto kern = attn_decode_kernel<D, MODE, SCORES, CLUSTER, MQ>;
+    // The shared-memory opt-in is a per-device function attribute: set it once per device.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
+    cudaLaunchConfig_t cfg = {};
+    if (MODE == kModeMixed)
+        cfg.gridDim = dim3((unsigned)(p.n_slow * p.hkv * p.slow_splits + p.n_fast * p.hkv * p.fast_splits));
+    else
+        cfg.gridDim = dim3(p.splits, p.hkv, batch);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    int n_attr = 1;
+    if (CLUSTER) {
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = p.splits;  // the splits of one unit form one cluster
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        n_attr = 2;
+    }
+    cfg.attrs = attr;
+    cfg.numAttrs = n_attr;
+    e = cudaLaunchKernelEx(&cfg, kern, maps.pool_k, maps.pool_v, maps.comp_k, maps.comp_v, p);
+    if (e != cudaSuccess) return e;
+    return cudaGetLastError();
+}
+
+}  // namespace sfi

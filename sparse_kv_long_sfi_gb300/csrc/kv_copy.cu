@@ -1,4 +1,4 @@
-// Byte-exact KV copies of the SFI path: the paged append of the current token and
+// Byte-exact KV copies of the SFI path: the paged append of the newest token(s) and
 // the compaction gather that packs sink + selected rows into the compact buffer.
 //
 // Method: Slow-Fast Inference (Xie et al., 2026), Figure 3 caption: the dense KV is
@@ -33,28 +33,32 @@ __device__ __forceinline__ void st_v4(void *p, int4 v) {
                  : "memory");
 }
 
+// Append of the p.tokens newest tokens of each request: token t goes to position
+// L - tokens + t (L counts them); k_new/v_new are [request][tokens][Hkv][D].
 template <int D>
 __global__ void __launch_bounds__(kCopyThreads) paged_append_kernel(const CopyParams p) {
     constexpr int kChunks = D / 8;  // 16-byte chunks per row
     const int b = blockIdx.x;
     const int r = p.req_ids ? p.req_ids[b] : b;
     const int L = p.seq_lens[r];
-    if (L < 1 || L > p.max_pages * kSubTokens) {
+    const int T = p.tokens;
+    if (L < T || L > p.max_pages * kSubTokens) {
         if (threadIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_LEN);
         return;
     }
-    const int pos = L - 1;
-    const int page = p.page_table[(int64_t)r * p.max_pages + pos / kSubTokens];
-    if (page < 0 || page >= p.num_pages) {
-        if (threadIdx.x == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
-        return;
-    }
-    const int total = 2 * p.hkv * kChunks;
-    for (int e = threadIdx.x; e < total; e += kCopyThreads) {
-        const bool is_v = e >= p.hkv * kChunks;
-        const int f = is_v ? e - p.hkv * kChunks : e;
+    const int per_token = 2 * p.hkv * kChunks;
+    for (int e = threadIdx.x; e < T * per_token; e += kCopyThreads) {
+        const int tt = e / per_token, f0 = e - tt * per_token;
+        const bool is_v = f0 >= p.hkv * kChunks;
+        const int f = is_v ? f0 - p.hkv * kChunks : f0;
         const int kv = f / kChunks, c = f - (f / kChunks) * kChunks;
-        const __nv_bfloat16 *src = (is_v ? p.v_new : p.k_new) + ((int64_t)r * p.hkv + kv) * D + c * 8;
+        const int pos = L - T + tt;
+        const int page = p.page_table[(int64_t)r * p.max_pages + pos / kSubTokens];
+        if (page < 0 || page >= p.num_pages) {
+            report(p.dev_status, SFI_DEV_BAD_PAGE);
+            continue;
+        }
+        const __nv_bfloat16 *src = (is_v ? p.v_new : p.k_new) + (((int64_t)r * T + tt) * p.hkv + kv) * D + c * 8;
         __nv_bfloat16 *dst = (is_v ? p.v_pool_dst : p.k_pool_dst) +
                              (((int64_t)page * p.hkv + kv) * kSubTokens + pos % kSubTokens) * D + c * 8;
         st_v4(dst, *reinterpret_cast<const int4 *>(src));

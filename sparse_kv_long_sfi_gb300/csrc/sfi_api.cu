@@ -157,6 +157,8 @@ void fill_common(AttnParams &p, const sfi_attn_shape *s, const sfi_paged_kv *kv,
     p.recent = recent;
     p.scale = resolve_scale(s);
     p.scale_log2 = p.scale * 1.4426950408889634f;
+    p.tokens = 1;
+    p.rows = p.group;
     p.dev_status = dev_status;
     p.k_new = nullptr;
     p.v_new = nullptr;
@@ -164,18 +166,44 @@ void fill_common(AttnParams &p, const sfi_attn_shape *s, const sfi_paged_kv *kv,
     p.v_pool_w = static_cast<__nv_bfloat16 *>(kv->v_pool);
 }
 
-sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, size_t ws_bytes) {
+sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, size_t ws_bytes,
+                          int rows = sfi::kMaxGroup) {
     p.ws_count = nullptr;
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
     if (!needs_workspace(p.splits)) return SFI_OK;
-    const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim);
+    const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim, rows);
     if (!ws || ws_bytes < l.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SFI_ERR_WORKSPACE;
     char *base = static_cast<char *>(ws);
     p.ws_count = reinterpret_cast<int32_t *>(base + l.count_off);
     p.ws_ml = reinterpret_cast<float *>(base + l.ml_off);
     p.ws_part = reinterpret_cast<float *>(base + l.part_off);
     return SFI_OK;
+}
+
+sfi_status append_tokens(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new, const void *v_new,
+                         int32_t tokens, const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    sfi::CopyParams p{};
+    p.k_pool_dst = static_cast<__nv_bfloat16 *>(kv->k_pool);
+    p.v_pool_dst = static_cast<__nv_bfloat16 *>(kv->v_pool);
+    p.num_pages = kv->num_pages;
+    p.max_pages = kv->max_pages_per_req;
+    p.page_table = kv->page_table;
+    p.seq_lens = kv->seq_lens;
+    p.hkv = shape->num_kv_heads;
+    p.head_dim = shape->head_dim;
+    p.req_ids = req_ids;
+    p.dev_status = dev_status;
+    p.tokens = tokens;
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
+    return sfi::launch_paged_append(p, batch, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFI_OK
+                                                                                                : SFI_ERR_CUDA;
 }
 
 }  // namespace
@@ -209,26 +237,14 @@ size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t ma
 sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
                                const void *v_new, const int32_t *req_ids, int32_t batch, int32_t *dev_status,
                                void *stream) {
-    sfi_status st = check_shape(shape);
-    if (st != SFI_OK) return st;
-    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
-    if (batch < 0 || !k_new || !v_new || !aligned16(k_new) || !aligned16(v_new)) return SFI_ERR_INVALID_ARG;
-    if (batch == 0) return SFI_OK;
-    sfi::CopyParams p{};
-    p.k_pool_dst = static_cast<__nv_bfloat16 *>(kv->k_pool);
-    p.v_pool_dst = static_cast<__nv_bfloat16 *>(kv->v_pool);
-    p.num_pages = kv->num_pages;
-    p.max_pages = kv->max_pages_per_req;
-    p.page_table = kv->page_table;
-    p.seq_lens = kv->seq_lens;
-    p.hkv = shape->num_kv_heads;
-    p.head_dim = shape->head_dim;
-    p.req_ids = req_ids;
-    p.dev_status = dev_status;
-    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
-    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
-    return sfi::launch_paged_append(p, batch, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFI_OK
-                                                                                                : SFI_ERR_CUDA;
+    return append_tokens(shape, kv, k_new, v_new, 1, req_ids, batch, dev_status, stream);
+}
+
+sfi_status sfi_paged_kv_append_tokens(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
+                                      const void *v_new, int32_t num_tokens, const int32_t *req_ids, int32_t batch,
+                                      int32_t *dev_status, void *stream) {
+    if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return SFI_ERR_INVALID_ARG;
+    return append_tokens(shape, kv, k_new, v_new, num_tokens, req_ids, batch, dev_status, stream);
 }
 
 sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
@@ -389,6 +405,95 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     }
     return sfi::launch_attention(shape->head_dim, sfi::kModeMixed, true, maps, p, 0,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+size_t sfi_multi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t num_tokens, int32_t max_tokens,
+                                int32_t num_splits) {
+    if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return 0;
+    const int32_t s = sfi_plan_splits(shape, batch, max_tokens, num_splits);
+    if (!needs_workspace(s)) return 0;
+    return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, s, shape->head_dim, sfi::kMaxRows).total;
+}
+
+sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink, int32_t recent,
+                                 const void *q, int32_t num_tokens, float *out, float *lse, float *scores,
+                                 int64_t score_stride, const int32_t *req_ids, int32_t batch, int32_t max_tokens,
+                                 int32_t num_splits, uint32_t flags, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned16(q) || !aligned8(out))
+        return SFI_ERR_INVALID_ARG;
+    if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return SFI_ERR_INVALID_ARG;
+    if (num_tokens * (shape->num_q_heads / shape->num_kv_heads) > sfi::kMaxRows) return SFI_ERR_UNSUPPORTED;
+    if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    AttnParams p{};
+    fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.tokens = num_tokens;
+    p.rows = num_tokens * p.group;
+    p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
+    p.scores = scores;
+    p.score_stride = score_stride;
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
+        return st;
+    AttnMaps maps;
+    const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
+    if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.pool_v, kv->v_pool, pool_rows, shape->head_dim))
+        return SFI_ERR_CUDA;
+    maps.comp_k = maps.pool_k;  // unused in dense mode
+    maps.comp_v = maps.pool_v;
+    return sfi::launch_attention_multi(shape->head_dim, sfi::kModeDense, maps, p, batch,
+                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
+sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
+                                 int32_t sink, int32_t recent, const void *q, int32_t num_tokens, float *out,
+                                 float *lse, const int32_t *req_ids, int32_t batch, int32_t max_tokens,
+                                 int32_t num_splits, uint32_t flags, void *workspace, size_t workspace_bytes,
+                                 int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (batch < 0 || sink < 0 || recent < 0 || num_splits < 0 || !q || !out || !aligned16(q) || !aligned8(out))
+        return SFI_ERR_INVALID_ARG;
+    if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return SFI_ERR_INVALID_ARG;
+    if (num_tokens * (shape->num_q_heads / shape->num_kv_heads) > sfi::kMaxRows) return SFI_ERR_UNSUPPORTED;
+    if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity || !compact->count)
+        return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v)) return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows >= (int64_t(1) << 31)) return SFI_ERR_UNSUPPORTED;
+    if (batch == 0) return SFI_OK;
+    AttnParams p{};
+    fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
+    p.tokens = num_tokens;
+    p.rows = num_tokens * p.group;
+    p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
+    p.c_row_offset = compact->row_offset;
+    p.c_capacity = compact->capacity;
+    p.c_count = compact->count;
+    p.c_total_rows = compact->total_rows;
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
+        return st;
+    AttnMaps maps;
+    const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
+    if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.pool_v, kv->v_pool, pool_rows, shape->head_dim) ||
+        !encode_rows(&maps.comp_k, compact->k, compact->total_rows, shape->head_dim) ||
+        !encode_rows(&maps.comp_v, compact->v, compact->total_rows, shape->head_dim))
+        return SFI_ERR_CUDA;
+    return sfi::launch_attention_multi(shape->head_dim, sfi::kModeFast, maps, p, batch,
+                                       static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SFI_OK
                : SFI_ERR_CUDA;
 }

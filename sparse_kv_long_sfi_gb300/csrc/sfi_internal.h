@@ -17,6 +17,9 @@ constexpr int kSubTokens = 16;
 constexpr int kConsumerWarps = 4;
 // Rows of the query tile handled per (request, KV head): G <= 8 query heads share a KV head.
 constexpr int kMaxGroup = 8;
+// Query rows of one (request, KV head) unit in the multi-token kernels: tokens x G <= 16
+// fill the whole M = 16 tile.
+constexpr int kMaxRows = 16;
 // Attention CTAs resident per SM (shared memory sized for this).
 constexpr int kAttnCtasPerSm = 2;
 // Splits of one unit that merge inside a thread-block cluster (portable cluster size);
@@ -28,9 +31,9 @@ constexpr int kMaxClusterSplits = 8;
 enum AttnMode : int { kModeFast = 0, kModeDense = 1, kModeMixed = 2 };
 
 struct AttnParams {
-    const __nv_bfloat16 *q;  // [B][Hq][D]
-    float *out;              // [B][Hq][D]
-    float *lse;              // [B][Hq] or null
+    const __nv_bfloat16 *q;  // [B][tokens][Hq][D]
+    float *out;              // [B][tokens][Hq][D]
+    float *lse;              // [B][tokens][Hq] or null
     float *scores;           // [B][Hkv][score_stride] or null
     int64_t score_stride;
     const int32_t *page_table;
@@ -47,6 +50,8 @@ struct AttnParams {
     float scale;       // softmax scale
     float scale_log2;  // scale * log2(e)
     int32_t splits;
+    // query tokens per request (positions L - tokens .. L - 1) and tile rows tokens x group
+    int32_t tokens, rows;
     // mixed mode: request lists and per-mode split counts
     const int32_t *fast_ids;
     const int32_t *slow_ids;
@@ -58,8 +63,8 @@ struct AttnParams {
     __nv_bfloat16 *k_pool_w;     // the paged pools, for the append's writes
     __nv_bfloat16 *v_pool_w;
     int32_t *ws_count;  // [units]
-    float *ws_ml;       // [units][splits][8][2]
-    float *ws_part;     // [units][splits][8][D]
+    float *ws_ml;       // [units][splits][rows per slot][2]
+    float *ws_part;     // [units][splits][rows per slot][D]
     int32_t *dev_status;
 };
 
@@ -72,11 +77,16 @@ struct AttnMaps {
 struct WorkspaceLayout {
     size_t count_off, ml_off, part_off, total;
 };
-WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim);
-WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim);
+// Single-token launches keep kMaxGroup rows per partial slot, multi-token ones kMaxRows.
+WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int rows = kMaxGroup);
+WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows = kMaxGroup);
 
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream);
+// Multi-token launch: mode kModeFast (draft over the sparse state) or kModeDense
+// (verification; scores written when p.scores is set).
+cudaError_t launch_attention_multi(int head_dim, int mode, const AttnMaps &maps, const AttnParams &p, int batch,
+                                   cudaStream_t stream);
 
 struct TopkParams {
     const float *scores;
@@ -104,7 +114,8 @@ struct CopyParams {
     int32_t hkv, head_dim;
     const int32_t *req_ids;
     int32_t *dev_status;
-    // append
+    // append of the `tokens` newest tokens
+    int32_t tokens;
     const __nv_bfloat16 *k_new;
     const __nv_bfloat16 *v_new;
     // compaction
