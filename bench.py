@@ -50,7 +50,7 @@ def parse_args():
     ap.add_argument("--steps", type=int, default=50)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["sfi", "reference"], default="sfi")
-    ap.add_argument("--no-sweep", action="store_true", help="skip the retention sweep")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the retention and speculative sweeps")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU-oracle baseline leg")
     ap.add_argument("--layers", type=int, default=WL["layers"])
     ap.add_argument("--batch", type=int, default=WL["batch"])
@@ -179,8 +179,9 @@ def append_bytes(B, Hkv, D):
 # kernel at the benchmark's per-launch shape (16 requests x 8 KV heads at KV 16K; the
 # summaries under profiles/ give the commands). They describe the kernel built from
 # the sources whose hash is recorded here and are dropped (null) once those change.
-PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_decode.cu", "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh",
-                    "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h", "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
+PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
+                    "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
+                    "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
 PROFILED_TRAFFIC = {"sha256_16": "15a63691a9426cf2", "fast": 68_328_704 + 1_067_264, "slow": 1_073_999_000 + 6_049_536}
 
 
@@ -391,6 +392,8 @@ def run_gpu(args, ranks: Ranks):
     if not args.no_sweep:
         result["retention_sweep"] = retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps,
                                                     NL, B, Hq, Hkv, D, P, L0, S, dev, peak)
+        result["speculative_sweep"] = speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv,
+                                                        D, P, L0, S, W, k_main, dev, peak, seed0)
     return result
 
 
@@ -522,6 +525,94 @@ def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_s
             "dense_frac_of_peak": round(NL * by_dense / (us_dense * 1e-6) / 1e9 / peak, 3),
             "points": rows, "note": "fast and dense steps include the (fused) paged append; 28 layers per step; "
                                     "Table 1 speedups are the paper's (hardware unstated), context only"}
+
+
+def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak,
+                      seed0):
+    """Self-speculative decoding's two passes over all layers ("A Sparse Glimpse of the
+    Whole", abstract): verification of T tokens (T-token append + causal dense
+    attention + the recycled statistic) and a T-token draft pass over the sparse state
+    at the main workload's retention, each as one graph of NL layers."""
+    import torch
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    reps = 20
+
+    def time_graph(fn):
+        with torch.cuda.stream(dec.main):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=dec.main):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(dec.main):
+            for _ in range(3):
+                g.replay()
+            e0.record(dec.main)
+            for _ in range(reps):
+                g.replay()
+            e1.record(dec.main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    # the main workload's selection (k_main at L0) in every layer's compact buffer
+    kreq = torch.full((B,), k_main, dtype=torch.int32, device=dev)
+    scratch = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    for i, Lb in enumerate(layers):
+        kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq_steps[0])
+        sfi.sfi_slow_dense_attn_with_scores(shape, kv, S, W, q_all[0, i], scratch, None, Lb.scores,
+                                            max_tokens=L0 + P, workspace=dec.ws_dense, stream=dec.main)
+        sfi.sfi_select_topk(Lb.scores, Hkv, seq_steps[0], S, W, kreq, Lb.idx, Lb.compact.count, stream=dec.main)
+        sfi.sfi_compact_gather(shape, kv, Lb.idx, Lb.compact.count, S, Lb.compact, stream=dec.main)
+    torch.cuda.synchronize()
+    rows = []
+    for T in (1, 2, 4, 8):
+        L = L0 + T
+        seq = torch.full((B,), L, dtype=torch.int32, device=dev)
+        q = torch.empty((NL, B, T, Hq, D), dtype=torch.bfloat16, device=dev)
+        kn = torch.empty((NL, B, T, Hkv, D), dtype=torch.bfloat16, device=dev)
+        vn = torch.empty_like(kn)
+        syn.device_normal_bf16_(q, syn.stream_seed(seed0, 30, T))
+        syn.device_normal_bf16_(kn, syn.stream_seed(seed0, 31, T))
+        syn.device_normal_bf16_(vn, syn.stream_seed(seed0, 32, T))
+        o = torch.empty((NL, B, T, Hq, D), dtype=torch.float32, device=dev)
+        ws_v = sfi.alloc_multi_workspace(shape, B, T, L + P, device=dev)
+        max_draft = S + k_main + W + T + 2 * P
+        ws_d = sfi.alloc_multi_workspace(shape, B, T, max_draft, device=dev)
+
+        def verify():
+            for i, Lb in enumerate(layers):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
+                sfi.sfi_paged_kv_append_tokens(shape, kv, kn[i], vn[i], T, stream=dec.main)
+                sfi.sfi_dense_verify_attn(shape, kv, S, W, q[i], T, o[i], None, Lb.scores, max_tokens=L + P,
+                                          workspace=ws_v, stream=dec.main)
+
+        def draft():
+            for i, Lb in enumerate(layers):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
+                sfi.sfi_paged_kv_append_tokens(shape, kv, kn[i], vn[i], T, stream=dec.main)
+                sfi.sfi_sparse_draft_attn(shape, kv, Lb.compact, S, W, q[i], T, o[i], None, max_tokens=max_draft,
+                                          workspace=ws_d, stream=dec.main)
+
+        us_v, us_d = time_graph(verify), time_graph(draft)
+        qo = B * T * Hq * (D * (2 + 4) + 4)
+        app = 2 * 2 * B * T * Hkv * D * 2
+        by_v = NL * (B * Hkv * L * 4 * D + B * math.ceil(L / P) * 4 + B * Hkv * L * 4 + qo + app)
+        by_d = NL * (B * Hkv * (S + k_main + W + T - 1) * 4 * D + qo + app)
+        rows.append({"tokens": T,
+                     "verify_us_per_pass": round(us_v, 2), "verify_us_per_token": round(us_v / T, 2),
+                     "verify_GBps": round(by_v / (us_v * 1e-6) / 1e9, 1),
+                     "verify_frac_of_peak": round(by_v / (us_v * 1e-6) / 1e9 / peak, 3),
+                     "draft_us_per_pass": round(us_d, 2), "draft_us_per_token": round(us_d / T, 2),
+                     "draft_GBps": round(by_d / (us_d * 1e-6) / 1e9, 1),
+                     "draft_frac_of_peak": round(by_d / (us_d * 1e-6) / 1e9 / peak, 3)})
+    dec.pending = [False] * len(layers)
+    return {"points": rows, "retention_pct_of_draft": round(100 * (S + k_main + W) / L0, 2),
+            "note": f"{NL} layers per pass, batch {B}, KV {L0} + T; each pass includes the T-token paged append; "
+                    "verification writes the recycled statistic (masked logits summed over the group and the "
+                    "tokens) for every layer"}
 
 
 # ---------------------------------------------------------------------------

@@ -6,6 +6,9 @@ Slow-Fast Inference (Xie et al., 2026):
     refresh interval is reached; otherwise the step is fast.
   * Figure 3 caption (A): while the main stream computes attention for layer i+1,
     an aux stream runs the Selector and the cache reorganisation of layer i.
+"A Sparse Glimpse of the Whole: Train-Free Self-Speculative Decoding" (abstract):
+drafts over the sparse state, a full-context verification whose per-head statistics
+refresh the selection (verify_step, refresh_selection, draft_step).
 Every device operation of a step is one of libsfi's kernels; this module only
 orders them on streams with events and keeps the per-request counters.
 """
@@ -17,9 +20,11 @@ from typing import List, Optional, Sequence
 import numpy as np
 import torch
 
-from .api import (SFI_ATTN_EARLY_KV_PREFETCH, AttnShape, CompactKV, PagedKV, alloc_mixed_workspace, alloc_workspace,
-                  sfi_compact_gather, sfi_fast_decode_attn, sfi_mixed_decode_attn, sfi_paged_kv_append,
-                  sfi_select_topk, sfi_slow_dense_attn_with_scores)
+from .api import (SFI_ATTN_EARLY_KV_PREFETCH, SFI_MAX_QUERY_TOKENS, AttnShape, CompactKV, PagedKV,
+                  alloc_mixed_workspace, alloc_multi_workspace, alloc_workspace, sfi_compact_gather,
+                  sfi_dense_verify_attn, sfi_fast_decode_attn, sfi_mixed_decode_attn, sfi_paged_kv_append,
+                  sfi_paged_kv_append_tokens, sfi_select_topk, sfi_slow_dense_attn_with_scores,
+                  sfi_sparse_draft_attn)
 
 
 class SlowFastSchedule:
@@ -98,7 +103,9 @@ def compact_layout(shape: AttnShape, sink: int, k_per_req, device="cuda"):
 
 @dataclass
 class StepIO:
-    """Per-step inputs/outputs of all layers (leading dim = layer)."""
+    """Per-step inputs/outputs of all layers (leading dim = layer). Multi-token steps
+    (verify_step, draft_step) carry a token dim after the request dim:
+    q [NL][B][T][Hq][D], k_new/v_new [NL][B][T][Hkv][D], out [NL][B][T][Hq][D]."""
     q: torch.Tensor           # bf16 [NL][B][Hq][D]
     k_new: torch.Tensor       # bf16 [NL][B][Hkv][D]
     v_new: torch.Tensor
@@ -135,6 +142,8 @@ class SFIDecoder:
         self.ws_dense = alloc_workspace(shape, B, self.max_dense_tokens, device=device)
         self.ws_mixed = (alloc_mixed_workspace(shape, B, self.max_fast_tokens, self.max_dense_tokens, device=device)
                          if single_launch_mixed else None)
+        self.ws_multi = None  # multi-token workspaces, allocated on first use
+        self._device = device
         self.dev_status = dev_status if dev_status is not None else torch.zeros(1, dtype=torch.int32, device=device)
         lo, hi = torch.cuda.Stream.priority_range()
         self.main = main_stream or torch.cuda.Stream(device=device, priority=hi)
@@ -285,6 +294,78 @@ class SFIDecoder:
                                    req_ids=slow_ids, batch=ns, dev_status=self.dev_status, stream=self.aux)
                 self.e_aux[i].record(self.aux)
                 self.pending[i] = True
+        self._leave()
+
+    def _multi_workspaces(self):
+        if self.ws_multi is None:
+            B = self.batch.page_table.shape[0]
+            T = SFI_MAX_QUERY_TOKENS
+            self.ws_multi = (alloc_multi_workspace(self.shape, B, 1, self.max_dense_tokens, device=self._device),
+                             alloc_multi_workspace(self.shape, B, 1, self.max_fast_tokens + T, device=self._device))
+        return self.ws_multi
+
+    def verify_step(self, io: StepIO, seq_lens: torch.Tensor, num_tokens: int,
+                    req_ids: Optional[torch.Tensor] = None, append: bool = True):
+        """Verification of num_tokens drafted tokens over all layers: their K/V go into
+        the pages (overwriting the draft's), causal dense attention runs, and each
+        layer's score rows receive the recycled statistic. seq_lens count the T tokens.
+        The selection is refreshed afterwards, on the accepted lengths, by
+        refresh_selection."""
+        T, n = int(num_tokens), None if req_ids is None else req_ids.numel()
+        ws_v, _ = self._multi_workspaces()
+        self._enter()
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            self._wait_aux(i)
+            if append:
+                sfi_paged_kv_append_tokens(self.shape, kv, io.k_new[i], io.v_new[i], T, req_ids=req_ids, batch=n,
+                                           dev_status=self.dev_status, stream=self.main)
+            self._mark("verify", "start")
+            sfi_dense_verify_attn(self.shape, kv, self.sink, self.recent, io.q[i], T, io.out[i],
+                                  None if io.lse is None else io.lse[i], L.scores, req_ids=req_ids, batch=n,
+                                  max_tokens=self.max_dense_tokens, workspace=ws_v, dev_status=self.dev_status,
+                                  stream=self.main)
+            self._mark("verify", "end")
+        self._leave()
+
+    def refresh_selection(self, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None):
+        """Selector and compaction of every layer from the statistics of the last
+        verify_step, at the accepted lengths seq_lens (at most the verified ones), on
+        the aux stream; the next use of each layer's compact buffer waits for it."""
+        n = None if req_ids is None else req_ids.numel()
+        self._enter()
+        self.aux.wait_stream(self.main)
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent, self.batch.k_per_req,
+                            L.idx, L.compact.count, req_ids=req_ids, batch=n, dev_status=self.dev_status,
+                            stream=self.aux)
+            sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact, req_ids=req_ids,
+                               batch=n, dev_status=self.dev_status, stream=self.aux)
+            self.e_aux[i].record(self.aux)
+            self.pending[i] = True
+        self._leave()
+
+    def draft_step(self, io: StepIO, seq_lens: torch.Tensor, num_tokens: int,
+                   req_ids: Optional[torch.Tensor] = None, append: bool = True):
+        """num_tokens query tokens per request over the sparse state in one pass per
+        layer (token t sees what a fast step at length L - T + t + 1 sees); their K/V
+        go into the pages first. seq_lens count the T tokens."""
+        T, n = int(num_tokens), None if req_ids is None else req_ids.numel()
+        _, ws_d = self._multi_workspaces()
+        self._enter()
+        for i, L in enumerate(self.layers):
+            kv = self.kv(i, seq_lens)
+            self._wait_aux(i)
+            if append:
+                sfi_paged_kv_append_tokens(self.shape, kv, io.k_new[i], io.v_new[i], T, req_ids=req_ids, batch=n,
+                                           dev_status=self.dev_status, stream=self.main)
+            self._mark("draft", "start")
+            sfi_sparse_draft_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], T, io.out[i],
+                                  None if io.lse is None else io.lse[i], req_ids=req_ids, batch=n,
+                                  max_tokens=self.max_fast_tokens + T, workspace=ws_d, dev_status=self.dev_status,
+                                  stream=self.main)
+            self._mark("draft", "end")
         self._leave()
 
     def dense_step(self, io: StepIO, seq_lens: torch.Tensor, append: bool = True):

@@ -247,3 +247,101 @@ def test_refresh_layer_inside_fast_steps():
     k = syn.retention_budget(0.125, 4096, 64, 256)
     w = Workload(6, [4095] * 4, 16, 8, 128, 64, 256, [k] * 4, steps=4, layers=2, heavy_frac=0.02)
     _run_schedule(w, [[1] * 4, [0] * 4, [0] * 4, [0] * 4], sampled=[0, 3], refresh=[(), (1,), (), (1,)])
+
+
+def test_speculative_draft_verify_refresh_16k_batch16():
+    """Self-speculative decoding over the SFI state ("A Sparse Glimpse of the Whole",
+    abstract), Qwen3-0.6B attention at 16K, batch 16, 6.25% retention, two layers:
+    slow step, a 4-token draft pass over the sparse state, verification of the same 4
+    positions (new K/V, causal dense attention, the recycled statistic), acceptance of a
+    seeded number of tokens per request, Selector + compaction from the statistic at the
+    accepted lengths, then a fast step on the refreshed state."""
+    S, W, T, NL, B = 64, 256, 4, 2, 16
+    k = syn.retention_budget(0.0625, 16384, S, W)
+    w = Workload(7, [16383] * B, 16, 8, 128, S, W, [k] * B, steps=2 * T + 2, layers=NL, heavy_frac=0.02)
+    sampled = [1, 14]
+    dev = torch.device("cuda")
+    # step 0: slow
+    _run_schedule(w, [[1] * B], sampled=sampled)
+    oc = dict(w.oracle_compact)
+    # draft pass: T tokens over the sparse state
+    g = syn.rng(7, 50)
+    qd = torch.empty((NL, B, T, 16, 128), dtype=torch.bfloat16, device=dev)
+    kd = torch.empty((NL, B, T, 8, 128), dtype=torch.bfloat16, device=dev)
+    vd = torch.empty_like(kd)
+    for i, t in enumerate((qd, kd, vd)):
+        syn.device_normal_bf16_(t, syn.stream_seed(7, 60, i))
+    od = torch.full((NL, B, T, 16, 128), float("nan"), device=dev)
+    w.cur = w.cur + T
+    w.dec.draft_step(w.sfi.StepIO(qd, kd, vd, od), w.seq_lens(), T)
+    torch.cuda.synchronize()
+    assert w.dec.dev_status.item() == 0
+    for layer in range(NL):
+        o = od[layer].cpu().numpy()
+        for r in sampled:
+            kp, vp, pr = w.host_pages(layer, r)
+            rk, rv, keff = oc[(layer, r)]
+            o_ref, _ = oracle.fast_multi_attn(host_bf16(qd[layer, r]), rk, rv, keff, kp, vp, pr, w.cur[r], T, S, W,
+                                              16, 8, 128, 16)
+            assert_close(o[r], o_ref, f"draft out layer={layer} r={r}")
+    # verification of the same T positions with the full model's K/V and queries
+    qv, kv_, vv = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
+    for i, t in enumerate((qv, kv_, vv)):
+        syn.device_normal_bf16_(t, syn.stream_seed(7, 70, i))
+    ov = torch.full_like(od, float("nan"))
+    lv = torch.full((NL, B, T, 16), float("nan"), device=dev)
+    for L_ in w.layers:
+        L_.scores.fill_(float("nan"))
+    w.dec.verify_step(w.sfi.StepIO(qv, kv_, vv, ov, lv), w.seq_lens(), T)
+    torch.cuda.synchronize()
+    assert w.dec.dev_status.item() == 0
+    for layer in range(NL):
+        o, l = ov[layer].cpu().numpy(), lv[layer].cpu().numpy()
+        sc = w.layers[layer].scores.cpu().numpy()
+        for r in sampled:
+            kp, vp, pr = w.host_pages(layer, r)
+            q = host_bf16(qv[layer, r])
+            o_ref, l_ref = oracle.verify_attn(q, kp, vp, pr, w.cur[r], T, 16, 8, 128, 16)
+            assert_close(o[r], o_ref, f"verify out layer={layer} r={r}")
+            assert_close(l[r], l_ref, f"verify lse layer={layer} r={r}")
+            L = int(w.cur[r])
+            ref = oracle.verify_scores(q, kp, pr, L, T, S, W, 16, 8, 128, 16, stride=sc.shape[-1])
+            masked = np.isneginf(ref[:, :L])
+            assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+            qa = np.abs(syn.bf16_values(q))
+            for h in range(8):
+                rows = np.abs(syn.bf16_values(kp[pr[np.arange(L) // 16], h, np.arange(L) % 16]))
+                mag = (rows @ qa[:, 2 * h:2 * h + 2].reshape(-1, 128).T).sum(1) / math.sqrt(128)
+                bound = 2 * T * 2 * 128 * 2.0 ** -24 * mag + 1e-30
+                ok = ~masked[h]
+                err = np.abs(sc[r, h, :L][ok].astype(np.float64) - ref[h, :L][ok])
+                assert (err <= bound[ok]).all(), (layer, r, h, err.max())
+    # acceptance: a seeded number of the T tokens per request, then the selection refresh
+    accepted = syn.rng(7, 80).integers(0, T + 1, size=B)
+    w.cur = w.cur - T + accepted
+    w.dec.refresh_selection(w.seq_lens())
+    w.dec.join()
+    torch.cuda.synchronize()
+    assert w.dec.dev_status.item() == 0
+    w.oracle_compact = {}
+    for layer in range(NL):
+        Lb = w.layers[layer]
+        sc = Lb.scores.cpu().numpy()
+        idx, count = Lb.idx.cpu().numpy(), Lb.compact.count.cpu().numpy()
+        cap = Lb.compact.capacity.cpu().numpy()
+        for r in range(B):
+            for h in range(8):
+                want = oracle.select_topk(sc[r, h], w.cur[r], S, W, k)
+                assert count[r] == len(want)
+                np.testing.assert_array_equal(idx[r, h, :len(want)], want, err_msg=f"layer={layer} r={r} kv={h}")
+        for r in sampled:
+            kp, vp, pr = w.host_pages(layer, r)
+            rk, rv = oracle.compact(kp, vp, pr, w.cur[r], S, idx[r], count[r], 8, 128, 16, cap[r])
+            w.oracle_compact[(layer, r)] = (rk, rv, count[r])
+    # a fast step on the refreshed state
+    w.cur = w.cur + 1
+    w.slow_mask = np.zeros(B, bool)
+    w.dec.fast_step(w.io(1), w.seq_lens())
+    w.dec.join()
+    for layer in range(NL):
+        _check_fast(w, 1, layer, sampled)
