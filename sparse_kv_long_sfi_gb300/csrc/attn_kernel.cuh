@@ -137,6 +137,9 @@ __device__ __forceinline__ bool unit_stream(const AttnParams &p, int r, int kvh,
 
 // Process one 16-token sub-block held in shared memory (K at kaddr, V at vaddr,
 // each kBoxes boxes of [16 rows][128 B] with the 128-byte swizzle).
+// The G <= 8 query rows sit in rows 0-7 of the M = 16 tile. In PV, rows 8-15 of the A
+// fragment carry the low bf16 part of the same probabilities, so o[nt][0..1] (rows g)
+// accumulate P_hi V and o[nt][2..3] (rows g + 8) P_lo V; the caller adds the halves.
 template <int D, bool SCORES>
 __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr, int lo, int hi, int pos0,
                                                   const uint32_t (&qa)[D / 16][2], float (&o)[D / 8][4],
@@ -146,9 +149,11 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;
 
-    // S = Q K^T for 16 tokens: two n-tiles (tokens 0-7 and 8-15).
+    // S = Q K^T for 16 tokens: two n-tiles (tokens 0-7 and 8-15), each accumulated in
+    // two independent chains (even and odd k-steps) to halve the mma dependency depth.
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
+        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int tok = ((mi >> 1) << 3) + r8;
         const uint32_t row_addr = kaddr + tok * 128;
 #pragma unroll
@@ -159,6 +164,11 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
             ldsm_x4(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
             mma_bf16_16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
             mma_bf16_16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
+        }
+#pragma unroll
+        for (int n = 0; n < 2; ++n) {
+            s[n][0] += s2[n][0];
+            s[n][1] += s2[n][1];
         }
     }
     const int tk0 = 2 * t, tk1 = 2 * t + 1, tk2 = 8 + 2 * t, tk3 = 9 + 2 * t;
@@ -210,13 +220,18 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
     const float p2 = fast_exp2(x2 - base), p3 = fast_exp2(x3 - base);
     l_run = l_run * alpha + ((p0 + p1) + (p2 + p3));
     m_run = m_new;
+    if (__any_sync(0xffffffffu, alpha != 1.f)) {  // the running max moved for some row
 #pragma unroll
-    for (int nt = 0; nt < T::kNTiles; ++nt) {
-        o[nt][0] *= alpha;
-        o[nt][1] *= alpha;
+        for (int nt = 0; nt < T::kNTiles; ++nt) {
+            o[nt][0] *= alpha;
+            o[nt][1] *= alpha;
+            o[nt][2] *= alpha;
+            o[nt][3] *= alpha;
+        }
     }
     // P enters the PV product as two bf16 terms, hi = bf16(p) and lo = bf16(p - hi), so
-    // the weights carry about 16 significant bits instead of bf16's 8.
+    // the weights carry about 16 significant bits instead of bf16's 8; hi fills the A
+    // fragment's rows 0-7, lo its rows 8-15.
     const __nv_bfloat162 h01 = __floats2bfloat162_rn(p0, p1);
     const __nv_bfloat162 h23 = __floats2bfloat162_rn(p2, p3);
     const __nv_bfloat162 l01 = __floats2bfloat162_rn(p0 - __low2float(h01), p1 - __high2float(h01));
@@ -242,10 +257,8 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
                 b2 &= vm0;
                 b3 &= vm1;
             }
-            mma_bf16_16816(o[2 * j], pa0, 0u, pa2, 0u, b0, b1);
-            mma_bf16_16816(o[2 * j + 1], pa0, 0u, pa2, 0u, b2, b3);
-            mma_bf16_16816(o[2 * j], pl0, 0u, pl2, 0u, b0, b1);
-            mma_bf16_16816(o[2 * j + 1], pl0, 0u, pl2, 0u, b2, b3);
+            mma_bf16_16816(o[2 * j], pa0, pl0, pa2, pl2, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], pa0, pl0, pa2, pl2, b2, b3);
         }
     }
 }
@@ -527,6 +540,24 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         };
         int cur = page_of(sb_begin + lane);
         int nxt = page_of(sb_begin + 32 + lane);
+        if (!fast) {
+            // Dense units: L2 prefetch of the stages after the ring's first fill (the rest
+            // of the first chunk of 32 sub-blocks), so the first refills read L2. (Measured:
+            // it shortens the slow step; on short fast-step units it costs more than it saves.)
+            const int page_all = cur;
+            for (int pst = T::kStages; pst < 8 && pst < n_stages; ++pst) {
+                const int page = __shfl_sync(0xffffffffu, page_all, (pst * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
+                const int sb = sb_begin + pst * kConsumerWarps + lane;
+                if (lane < kConsumerWarps && sb < sb_end && page >= 0 && page < p.num_pages) {
+                    const int32_t y = (page * p.hkv + kvh) * kSubTokens;
+#pragma unroll
+                    for (int bx = 0; bx < T::kBoxes; ++bx) {
+                        tma_prefetch_l2_2d(&tm_pool_k, bx * 64, y);
+                        tma_prefetch_l2_2d(&tm_pool_v, bx * 64, y);
+                    }
+                }
+            }
+        }
         for (int st = 0; st < n_stages; ++st) {
             if (st > 0 && (st & 7) == 0) {  // 8 stages x 4 sub-blocks = 32 page ids per chunk
                 cur = nxt;
@@ -709,7 +740,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     if (ok) {
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) {
-            float2 v = make_float2(o[nt][0], o[nt][1]);
+            // one token: rows g + 8 hold the P_lo V half of row g
+            float2 v = MQ ? make_float2(o[nt][0], o[nt][1]) : make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
             *reinterpret_cast<float2 *>(&sm_o[(warp * kRows + g) * MS + nt * 8 + 2 * t]) = v;
             if (MQ) {
                 float2 w = make_float2(o[nt][2], o[nt][3]);
