@@ -54,7 +54,10 @@ struct AttnTile {
     static constexpr int kStageBytes = kConsumerWarps * 2 * kSubBytes;
     static constexpr int kRingBytes = 96 * 1024;                 // two CTAs per SM
     static constexpr int kStages = kRingBytes / kStageBytes;
-    static constexpr int kSmemBytes = kStages * kStageBytes + 1024;  // + alignment slack
+    // After the ring: where the other CTAs of a cluster push their partial results.
+    static constexpr int kRecvOffset = kStages * kStageBytes;
+    static constexpr int kRecvBytes = 13 * 1024;
+    static constexpr int kSmemBytes = kRecvOffset + kRecvBytes + 1024;  // + alignment slack
     static constexpr int kKSteps = D / 16;                       // mma k-steps of QK^T
     static constexpr int kNTiles = D / 8;                        // mma n-tiles of PV
     static constexpr int kMergeStride = D + 4;                   // padded rows of the warp-merge scratch
@@ -413,21 +416,44 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
 // the swizzled K and V tiles at `tile` and into the paged cache at position L - 1.
 // One 16-byte chunk per lane; the writing lanes then order their generic-proxy
 // shared-memory writes before later TMA (async-proxy) writes into the same stage.
+// Start the loads fuse_current_token needs (the current token's K/V chunks and its page
+// id) as asynchronous copies into shared memory, so their latency overlaps the stages
+// before the one holding position L - 1.
 template <int D>
-__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
-                                                   const UnitStream &u, int lane) {
-    using T = AttnTile<D>;
+__device__ __forceinline__ void stage_current_token(const AttnParams &p, int r, int kvh, const UnitStream &u,
+                                                    int lane, int4 *s_val, int *s_page) {
     constexpr int kChunks = D / 8;
     if (lane < 2 * kChunks) {
         const bool is_v = lane >= kChunks;
         const int c = is_v ? lane - kChunks : lane;
-        const int64_t src_off = ((int64_t)r * p.hkv + kvh) * D + c * 8;
-        const int4 val = *reinterpret_cast<const int4 *>((is_v ? p.v_new : p.k_new) + src_off);
+        const __nv_bfloat16 *src = (is_v ? p.v_new : p.k_new) + ((int64_t)r * p.hkv + kvh) * D + c * 8;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 16;" ::"r"(smem_u32(&s_val[lane])), "l"(src)
+                     : "memory");
+    }
+    if (lane == 0) {
+        const int32_t *src = p.page_table + (int64_t)r * p.max_pages + (u.L - 1) / kSubTokens;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s_page)), "l"(src) : "memory");
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
+                                                   const UnitStream &u, int lane, const int4 *s_val,
+                                                   const int *s_page) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
+    // the copies issued by stage_current_token have landed (each lane waits for its own)
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const int4 val = s_val[lane];
         const int row = u.row_app;
         uint8_t *base = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128) + row * 128;
         *reinterpret_cast<int4 *>(base + (((c & 7) ^ (row & 7)) << 4)) = val;
         const int pos = u.L - 1;
-        const int page = p.page_table[(int64_t)r * p.max_pages + pos / kSubTokens];
+        const int page = *s_page;
         if (page < 0 || page >= p.num_pages) {
             if (lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
         } else {
@@ -438,6 +464,19 @@ __device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnPara
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
+}
+
+// Floats of one pushed partial in the receive region: o [rows][D], m [rows], l [rows],
+// padded to 16 bytes.
+template <int D>
+__host__ __device__ constexpr int cluster_slot_floats(int rows) {
+    return (rows * (D + 2) + 3) & ~3;
+}
+
+// Whether the partials of `splits` CTAs with `rows` query rows fit rank 0's receive region.
+template <int D>
+__host__ __device__ constexpr bool cluster_push_fits(int splits, int rows) {
+    return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= AttnTile<D>::kRecvBytes;
 }
 
 // MQ: p.tokens query tokens per request (rows = tokens x G <= 16), no fused append.
@@ -456,6 +495,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __shared__ int2 s_info[T::kStages][kConsumerWarps];
     __shared__ int s_last;
     __shared__ int s_timeout;
+    __shared__ __align__(16) int4 s_app_val[32];  // the current token's K/V chunks (fused append)
+    __shared__ int s_app_page;
 
     // ---- this CTA's work item: (request, KV head, split) and the unit's mode ----
     int split, kvh, b, splits;
@@ -519,7 +560,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             mbar_init(&full_bar[i], kConsumerWarps);
             mbar_init(&empty_bar[i], kConsumerWarps);
         }
-        if (CLUSTER) mbar_init(&merge_bar, split == 0 ? splits - 1 : 1);
+        // push merge: every consumer thread of every other CTA arrives once at rank 0
+        if (CLUSTER)
+            mbar_init(&merge_bar, split != 0 ? 1u
+                                  : cluster_push_fits<D>(splits, MQ ? p.rows : p.group)
+                                      ? (uint32_t)(splits - 1) * kConsumerWarps * 32
+                                      : (uint32_t)(splits - 1));
         s_timeout = 0;
         fence_barrier_init();
     }
@@ -679,6 +725,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
     }
 
+    if (!MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end &&
+        (u.sb_app - sb_begin) % kConsumerWarps == warp)
+        stage_current_token<D>(p, r, kvh, u, lane, s_app_val, &s_app_page);
     bool timed_out = false;
     for (int st = 0; st < n_stages; ++st) {
         const int slot = st % T::kStages;
@@ -688,10 +737,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
         const int2 in = s_info[slot][warp];
         const int lo = in.x & 0xffff, hi = in.x >> 16;
-        if (!MQ && p.k_new != nullptr && sb_begin + st * kConsumerWarps + warp == u.sb_app) {
+        if (!MQ && p.k_new != nullptr && u.sb_app < sb_end && sb_begin + st * kConsumerWarps + warp == u.sb_app) {
             // Fused append: the current token's K/V replace row L - 1 of this tile (the
             // attention sees the cache after the append) and are written to the pages.
-            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane);
+            // Only the split that owns that sub-block does it (a stage's padding slots
+            // past sb_end may carry the same index).
+            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane,
+                                  s_app_val, &s_app_page);
         }
         if (hi > lo) {
             const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);
@@ -805,8 +857,72 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     }
     if (splits == 1) return;
 
+    if (CLUSTER && cluster_push_fits<D>(splits, rows)) {
+        // ---- split merge inside the cluster: the other CTAs push their partials into
+        // rank 0's receive region (distributed shared-memory stores), rank 0 merges them
+        // from its own shared memory ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        const int slot_f = cluster_slot_floats<D>(rows);
+        float *recv = reinterpret_cast<float *>(smem + T::kRecvOffset);  // [splits - 1][slot_f]
+        if (split != 0) {
+            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * slot_f) * 4u;
+            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
+                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
+            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
+                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
+                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
+            }
+            mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), 0));  // release: my stores above
+            // Rank 0 signals once every push has landed; only then may this CTA exit.
+            if (ctid == 0 && !mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+        const bool got = mbar_wait_cluster_bounded(&merge_bar, 0);  // acquire: the peers' pushes
+        if (got && ctid >= 1 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
+        if (!got) {
+            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+        if (!ok) return;
+        for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+            const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+            float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+            float2 os[kMaxClusterSplits];
+            ms[0] = cp_m[row];
+            ls[0] = cp_l[row];
+            os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
+#pragma unroll
+            for (int s = 1; s < kMaxClusterSplits; ++s) {
+                if (s < splits) {
+                    const float *src = recv + (s - 1) * slot_f;
+                    ms[s] = src[rows * D + row];
+                    ls[s] = src[rows * D + rows + row];
+                    os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s)
+                if (s < splits) M = fmaxf(M, ms[s]);
+            float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s < splits && ls[s] > 0.f) {
+                    const float f = fast_exp2(ms[s] - M);
+                    ax += os[s].x * f;
+                    ay += os[s].y * f;
+                    lsum += ls[s] * f;
+                }
+            }
+            *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
+            if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+        }
+        return;
+    }
+
     if (CLUSTER) {
-        // ---- split merge inside the cluster, through distributed shared memory ----
+        // ---- split merge inside the cluster, pulled by rank 0 from the other CTAs'
+        // shared memory (when their partials do not fit rank 0's receive region) ----
         consumer_bar_sync();  // this CTA's partial is complete in its shared memory
         if (split != 0) {
             if (ctid == 0) {
