@@ -18,7 +18,7 @@ namespace sfi {
 constexpr int kCopyThreads = 256;
 constexpr int kCompactRowsPerCta = 64;
 // Requests handled by one compaction launch (the chunk prefix lives in shared memory).
-constexpr int kCompactMaxBatch = 2048;
+constexpr int kCompactMaxBatch = 512;
 
 __device__ __forceinline__ int4 ld_nc_v4(const void *p) {
     int4 v;
@@ -92,7 +92,7 @@ __device__ __forceinline__ int compact_rows(const CopyParams &p, int r, uint32_t
 // counts (an exclusive prefix over the launch's requests, in shared memory) and walks
 // it with a grid stride, so the work follows the rows actually selected, not k_cap.
 template <int D>
-__global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const CopyParams p, int b_begin, int nb) {
+__global__ void __launch_bounds__(kCopyThreads, 4) compact_gather_kernel(const CopyParams p, int b_begin, int nb) {
     constexpr int kChunks = D / 8;
     constexpr int kThreadsPerRow = 2 * kChunks;  // K chunks then V chunks
     constexpr int kRowsPerIter = kCopyThreads / kThreadsPerRow;
@@ -100,6 +100,10 @@ __global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const Copy
     constexpr int kWarps = kCopyThreads / 32;
     __shared__ int s_prefix[kCompactMaxBatch];  // first chunk of each request entry
     __shared__ int s_rows[kCompactMaxBatch];    // rows per KV head of each request entry
+    __shared__ int s_len[kCompactMaxBatch];     // L, selected count and capacity of each entry
+    __shared__ int s_cnt[kCompactMaxBatch];
+    __shared__ int s_cap[kCompactMaxBatch];
+    __shared__ long long s_off[kCompactMaxBatch];
     __shared__ int s_warp[kWarps];
     __shared__ int s_total;
 
@@ -137,6 +141,13 @@ __global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const Copy
         if (b < nb) {
             s_prefix[b] = carry + s_warp[warp] + incl - c;
             s_rows[b] = rows;
+            if (rows > 0) {  // compact_rows has validated these
+                const int r = p.req_ids ? p.req_ids[b_begin + b] : b_begin + b;
+                s_len[b] = p.seq_lens[r];
+                s_cnt[b] = p.count[r];
+                s_cap[b] = p.c_capacity[r];
+                s_off[b] = p.c_row_offset[r];
+            }
         }
         carry += s_total;
         __syncthreads();
@@ -164,11 +175,11 @@ __global__ void __launch_bounds__(kCopyThreads) compact_gather_kernel(const Copy
         const int within = work - s_prefix[b];
         const int kvh = within / per_head;
         const int row0 = (within - kvh * per_head) * kCompactRowsPerCta;
-        const int L = p.seq_lens[r];
+        const int L = s_len[b];
         const int ns = min(p.sink, L);
-        const int cnt = p.count[r];
-        const int cap = p.c_capacity[r];
-        const int64_t off = p.c_row_offset[r];
+        const int cnt = s_cnt[b];
+        const int cap = s_cap[b];
+        const int64_t off = s_off[b];
         __nv_bfloat16 *dst_base = (is_v ? p.cv : p.ck) + (off + (int64_t)kvh * cap) * D + chunk * 8;
         const int32_t *sel = p.idx + ((int64_t)r * p.hkv + kvh) * p.k_cap;
         const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
@@ -216,11 +227,15 @@ cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t str
 
 cudaError_t launch_compact_gather(const CopyParams &p, int batch, int max_rows, cudaStream_t stream) {
     (void)max_rows;  // the grid follows the device counts
-    int dev = 0, sms = 0;
+    int dev = 0, sms = 0, per_sm = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e == cudaSuccess)
+        e = p.head_dim == 128
+                ? cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_gather_kernel<128>, kCopyThreads, 0)
+                : cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, compact_gather_kernel<64>, kCopyThreads, 0);
     if (e != cudaSuccess) return e;
-    const int grid = sms * 6;  // enough 32 KB chunks in flight to saturate HBM
+    const int grid = sms * (per_sm > 0 ? per_sm : 1);  // one resident wave of persistent CTAs
     for (int b0 = 0; b0 < batch; b0 += kCompactMaxBatch) {
         const int nb = batch - b0 < kCompactMaxBatch ? batch - b0 : kCompactMaxBatch;
         if (p.head_dim == 128)

@@ -9,9 +9,11 @@
 //    -inf).
 //  * The candidates are walked in rounds of 16384 positions; in a round, warp w owns
 //    the contiguous positions [512 w, 512 w + 512) and lane l holds positions
-//    512 w + 32 j + l, j < 16, loaded together (16 independent coalesced loads per
-//    thread). With at most one round (|C| <= 16384) the keys stay in registers for
-//    the whole selection: the scores are read from memory once.
+//    512 w + 32 j + l, j < 16. With at most one round (|C| <= 16384) the whole score
+//    row is first moved into shared memory by one TMA bulk copy (many small loads per
+//    thread would be limited by the SM's outstanding misses), and the keys stay in
+//    registers for the whole selection: the scores are read from memory once. Longer
+//    rows are read round by round with 16 independent coalesced loads per thread.
 //  * Radix select, 4 passes of 8 bits from the top: a 256-bin shared histogram of the
 //    keys that share the current prefix (warp-aggregated atomics via match.any),
 //    then one warp scans the bins from the top to find the bin holding the k-th key.
@@ -20,6 +22,8 @@
 //  * Output in ascending position order without sorting: per (round, warp) counts of
 //    keys above / equal to tau, an exclusive scan over (round, warp) in position
 //    order, then each warp writes its taken positions with ballot/popc ranks.
+#include <atomic>
+
 #include "sfi_device.cuh"
 #include "sfi_internal.h"
 
@@ -64,7 +68,12 @@ __device__ __forceinline__ void histogram_round(const uint32_t (&key)[kTopkPerTh
     }
 }
 
+// Dynamic shared memory: one round of scores.
+constexpr int kTopkSmemBytes = kTopkRound * 4;
+
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p) {
+    extern __shared__ __align__(16) float s_keys[];
+    __shared__ __align__(8) uint64_t s_bar;
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_bin, s_rem;
     __shared__ int32_t s_gt[kTopkMaxRounds * kTopkWarps], s_eq[kTopkMaxRounds * kTopkWarps];
@@ -95,7 +104,36 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     }
 
     uint32_t key[kTopkPerThread];
-    if (rounds == 1) load_round(row, n, 0, warp, lane, key);  // resident for the whole selection
+    if (rounds == 1) {  // resident for the whole selection
+        // Bulk copy [a0, a1) of the row: a0 = its start rounded up, a1 = its end rounded
+        // down to 16 bytes (the copy never leaves the row); the few floats outside are
+        // read directly.
+        const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+        const uintptr_t a0 = (a + 15) & ~uintptr_t(15);
+        const uintptr_t a1 = (a + 4 * (uintptr_t)n) & ~uintptr_t(15);
+        const int lo_i = (int)((a0 - a) >> 2);                    // row[i], lo_i <= i < hi_i, is s_keys[i - lo_i]
+        const int hi_i = a1 > a0 ? (int)((a1 - a) >> 2) : lo_i;
+        if (tid == 0) {
+            mbar_init(&s_bar, 1);
+            fence_barrier_init();
+            if (a1 > a0) {
+                mbar_arrive_expect_tx(&s_bar, (uint32_t)(a1 - a0));
+                bulk_load_1d(s_keys, reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0), &s_bar);
+            } else {
+                mbar_arrive(&s_bar);
+            }
+        }
+        __syncthreads();
+        if (!mbar_wait_warp(&s_bar, 0)) {  // bounded; the copy is the same for every warp
+            if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+#pragma unroll
+        for (int j = 0; j < kTopkPerThread; ++j) {
+            const int i = warp * (32 * kTopkPerThread) + 32 * j + lane;
+            key[j] = i < n ? order_key(i >= lo_i && i < hi_i ? s_keys[i - lo_i] : __ldg(row + i)) : kNoKey;
+        }
+    }
 
     // ---- radix select of the keff-th largest key ----
     uint32_t prefix = 0u, mask = 0u;
@@ -215,8 +253,19 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
 }
 
 cudaError_t launch_select_topk(const TopkParams &p, int batch, cudaStream_t stream) {
+    // The shared-memory opt-in is a per-device function attribute: set it once per device.
+    static std::atomic<uint64_t> configured{0};
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
+    if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
+        e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemBytes);
+        if (e != cudaSuccess) return e;
+        configured.fetch_or(bit, std::memory_order_acq_rel);
+    }
     dim3 grid(p.hkv, batch);
-    select_topk_kernel<<<grid, kTopkThreads, 0, stream>>>(p);
+    select_topk_kernel<<<grid, kTopkThreads, kTopkSmemBytes, stream>>>(p);
     return cudaGetLastError();
 }
 

@@ -173,6 +173,16 @@ __device__ __forceinline__ void tma_prefetch_l2_2d(const CUtensorMap *map, int32
                  : "memory");
 }
 
+// 1-D bulk copy global -> shared (both addresses 16-byte aligned, bytes a multiple of
+// 16), completing on an mbarrier.
+__device__ __forceinline__ void bulk_load_1d(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+            smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+
 // L2 policy for data read exactly once by this kernel (KV streams).
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
