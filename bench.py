@@ -331,7 +331,8 @@ def run_gpu(args, ranks: Ranks):
         for kind, a, b in step_marks:
             dur[kind].append(a.elapsed_time(b) * 1e3 / NL)
         timing_method = (f"events at decode-step boundaries (graph nodes), {NL} back-to-back launches per step, "
-                         f"last of {reps} replays after the headline region")
+                         f"last of {reps} replays after the headline region; the fast kernel's average over the "
+                         f"{cyc - 2} fast steps that do not follow the slow step")
     except RuntimeError as exc:
         dur = None
         timing_method = f"unavailable: {exc}"
@@ -349,9 +350,16 @@ def run_gpu(args, ranks: Ranks):
 
     roofline = None
     if dur:
-        t_fast = statistics.mean(dur["fast"]) if dur["fast"] else 0.0
+        # The first fast step after the slow step also waits, layer by layer, for the
+        # side stream's Selector and compaction (the slow step's attention leaves them no
+        # room to run beside it), so the fast kernel's own duration is taken from the
+        # other fast steps; the first one is reported on its own.
+        fast_wait = dur["fast"][:1]
+        fast_clean = dur["fast"][1:] or dur["fast"]
+        t_fast = statistics.mean(fast_clean) if fast_clean else 0.0
+        t_fast_first = statistics.mean(fast_wait) if fast_wait else 0.0
         t_slow = statistics.mean(dur["slow"]) if dur["slow"] else 0.0
-        share_fast = t_fast * (cyc - 1) * NL / (ms_marked * 1e3)
+        share_fast = (t_fast * (cyc - 2) + t_fast_first) * NL / (ms_marked * 1e3)
         share_slow = t_slow * NL / (ms_marked * 1e3)
         if share_slow >= share_fast:
             name, per, tl, sh = "attn_decode_kernel<128,dense,scores> (slow step)", by_slow, t_slow, share_slow
@@ -364,6 +372,8 @@ def run_gpu(args, ranks: Ranks):
                     "time_share": round(sh, 4), "timing": timing_method,
                     "other": {"fast_avg_us": round(t_fast, 3), "fast_GBps": round(by_fast / (t_fast * 1e-6) / 1e9, 1)
                               if t_fast else None, "fast_share": round(share_fast, 4),
+                              "first_fast_step_us_per_layer": round(t_fast_first, 3),
+                              "first_fast_step_note": "waits for the side stream's Selector and compaction",
                               "slow_avg_us": round(t_slow, 3), "slow_GBps": round(by_slow / (t_slow * 1e-6) / 1e9, 1)
                               if t_slow else None, "slow_share": round(share_slow, 4)}}
 

@@ -71,6 +71,17 @@ __device__ __forceinline__ void histogram_round(const uint32_t (&key)[kTopkPerTh
 // Dynamic shared memory: one round of scores.
 constexpr int kTopkSmemBytes = kTopkRound * 4;
 
+// The same histogram with one counter per (bin, lane): hrep[bin * 32 + lane]. One
+// shared atomic per key and no warp aggregation; a warp's 32 atomics go to 32 banks.
+// Cheaper than histogram_round when most keys are in play (the first two passes).
+__device__ __forceinline__ void histogram_lanes(const uint32_t (&key)[kTopkPerThread], uint32_t prefix, uint32_t mask,
+                                                int shift, int lane, uint32_t *hrep) {
+#pragma unroll
+    for (int j = 0; j < kTopkPerThread; ++j) {
+        if (key[j] != kNoKey && (key[j] & mask) == prefix) atomicAdd(&hrep[((key[j] >> shift) & 255u) * 32 + lane], 1u);
+    }
+}
+
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p) {
     extern __shared__ __align__(16) float s_keys[];
     __shared__ __align__(8) uint64_t s_bar;
@@ -133,23 +144,41 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             const int i = warp * (32 * kTopkPerThread) + 32 * j + lane;
             key[j] = i < n ? order_key(i >= lo_i && i < hi_i ? s_keys[i - lo_i] : __ldg(row + i)) : kNoKey;
         }
+        __syncthreads();  // every warp has its keys; s_keys is reused below
     }
+    uint32_t *hrep = reinterpret_cast<uint32_t *>(s_keys);  // [256][32] lane counters (first two passes)
 
     // ---- radix select of the keff-th largest key ----
     uint32_t prefix = 0u, mask = 0u;
     uint32_t rem = (uint32_t)keff;  // how many still to take inside the current prefix
     for (int shift = 24; shift >= 0; shift -= 8) {
-        for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+        const bool lanes = shift >= 16;
+        if (lanes) {
+            for (int i = tid; i < 256 * 32; i += kTopkThreads) hrep[i] = 0u;
+        } else {
+            for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
+        }
         __syncthreads();
         if (rounds == 1) {
-            histogram_round(key, prefix, mask, shift, lane, hist);
+            if (lanes) histogram_lanes(key, prefix, mask, shift, lane, hrep);
+            else histogram_round(key, prefix, mask, shift, lane, hist);
         } else {
             for (int rd = 0; rd < rounds; ++rd) {
                 load_round(row, n, rd * kTopkRound, warp, lane, key);
-                histogram_round(key, prefix, mask, shift, lane, hist);
+                if (lanes) histogram_lanes(key, prefix, mask, shift, lane, hrep);
+                else histogram_round(key, prefix, mask, shift, lane, hist);
             }
         }
         __syncthreads();
+        if (lanes) {  // hist[b] = sum of bin b's 32 lane counters (rotated: a warp's reads hit 32 banks)
+            if (tid < 256) {
+                uint32_t sum = 0u;
+#pragma unroll 8
+                for (int l = 0; l < 32; ++l) sum += hrep[tid * 32 + ((l + tid) & 31)];
+                hist[tid] = sum;
+            }
+            __syncthreads();
+        }
         if (warp == 0) {
             // lane l owns bins 255-8l .. 248-8l (from the top)
             uint32_t c[8];
@@ -231,6 +260,9 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     }
     __syncthreads();
     const uint32_t lt_mask = (1u << lane) - 1u;
+    // With one round the selection (keff < n <= 16384 positions) is assembled in shared
+    // memory (s_keys is free by now) and written out with one coalesced pass.
+    int32_t *dst = rounds == 1 ? reinterpret_cast<int32_t *>(s_keys) : out;
     for (int rd = 0; rd < rounds; ++rd) {
         if (rounds > 1) load_round(row, n, rd * kTopkRound, warp, lane, key);
         int eq_before = s_eq[rd * kTopkWarps + warp];
@@ -244,11 +276,15 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             const bool take = valid && (key[j] > tau || (is_eq && eq_rank < take_eq));
             const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
             if (take)
-                out[out_pos + __popc(take_bal & lt_mask)] =
+                dst[out_pos + __popc(take_bal & lt_mask)] =
                     p.sink + rd * kTopkRound + warp * (32 * kTopkPerThread) + 32 * j + lane;
             out_pos += __popc(take_bal);
             eq_before += __popc(eq_bal);
         }
+    }
+    if (rounds == 1) {
+        __syncthreads();
+        for (int i = tid; i < keff; i += kTopkThreads) out[i] = dst[i];
     }
 }
 
