@@ -339,6 +339,24 @@ SFI_API sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_pag
                               const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream);
 
 /*
+ * sfi_select_compact - sfi_select_topk followed by sfi_compact_gather, in one launch:
+ * the CTA that selects a (request, KV head) also packs its sink and selected rows into
+ * the compact buffer (Figure 2 caption: the Selector refreshes the selected memory;
+ * Figure 3: cache reorganisation into the contiguous compact buffer). The results are
+ * those of the two calls in sequence with count = count_out.
+ *   scores, score_stride, k_per_req, k_cap, idx_out : as for sfi_select_topk
+ *   count_out : int32 [B], normally the same array as compact->count
+ *   kv->seq_lens gives L (as for both calls)
+ * Device errors: those of the two calls (a request with an invalid compact layout
+ * keeps its selection but is not packed).
+ */
+SFI_API sfi_status sfi_select_compact(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const float *scores,
+                                      int64_t score_stride, int32_t sink, int32_t recent, const int32_t *k_per_req,
+                                      int32_t k_cap, int32_t *idx_out, int32_t *count_out,
+                                      const sfi_compact_kv *compact, const int32_t *req_ids, int32_t batch,
+                                      int32_t *dev_status, void *stream);
+
+/*
  * sfi_fast_decode_attn_noalloc - the fast step of sfi_fast_decode_attn for callers
  * that cannot allocate device memory. The paper has no counterpart to this call; it
  * exists for users of this library.

@@ -61,6 +61,8 @@ PROTOTYPES = {
                                 c_vp]),
     "sfi_compact_gather": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_i32, c_i32, P_COMPACT, c_vp, c_i32, c_vp,
                                    c_vp]),
+    "sfi_select_compact": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_i64, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, P_COMPACT,
+                                   c_vp, c_i32, c_vp, c_vp]),
     "sfi_fast_decode_attn_noalloc": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_vp, c_vp, c_vp,
                                              c_vp, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_vp]),
     "sfi_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32]),

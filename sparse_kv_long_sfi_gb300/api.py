@@ -271,6 +271,21 @@ def sfi_select_topk(scores: torch.Tensor, num_kv_heads: int, seq_lens: torch.Ten
     _check(st, "sfi_select_topk")
 
 
+def sfi_select_compact(shape: AttnShape, kv: PagedKV, scores: torch.Tensor, sink: int, recent: int,
+                       k_per_req: torch.Tensor, idx_out: torch.Tensor, compact: CompactKV,
+                       count_out: Optional[torch.Tensor] = None, req_ids: Optional[torch.Tensor] = None,
+                       batch: Optional[int] = None, dev_status: Optional[torch.Tensor] = None, stream=None):
+    """Selector + compaction in one launch; count_out defaults to compact.count."""
+    count_out = compact.count if count_out is None else count_out
+    st = _abi.lib().sfi_select_compact(
+        ctypes.byref(shape.c()), ctypes.byref(kv.c()), _ptr(scores, torch.float32, "scores"), int(scores.shape[-1]),
+        int(sink), int(recent), _ptr(k_per_req, torch.int32, "k_per_req"), int(idx_out.shape[-1]),
+        _ptr(idx_out, torch.int32, "idx_out"), _ptr(count_out, torch.int32, "count_out"), ctypes.byref(compact.c()),
+        _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens),
+        _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
+    _check(st, "sfi_select_compact")
+
+
 def sfi_compact_gather(shape: AttnShape, kv: PagedKV, idx: torch.Tensor, count: torch.Tensor, sink: int,
                        compact: CompactKV, req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None,
                        dev_status: Optional[torch.Tensor] = None, stream=None):

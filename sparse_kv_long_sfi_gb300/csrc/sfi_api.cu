@@ -560,4 +560,53 @@ sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_paged_kv *k
                : SFI_ERR_CUDA;
 }
 
+sfi_status sfi_select_compact(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const float *scores,
+                              int64_t score_stride, int32_t sink, int32_t recent, const int32_t *k_per_req,
+                              int32_t k_cap, int32_t *idx_out, int32_t *count_out, const sfi_compact_kv *compact,
+                              const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream) {
+    sfi_status st = check_shape(shape);
+    if (st != SFI_OK) return st;
+    if ((st = check_paged(shape, kv)) != SFI_OK) return st;
+    if (!scores || !k_per_req || !idx_out || !count_out) return SFI_ERR_INVALID_ARG;
+    if (score_stride <= 0 || sink < 0 || recent < 0 || k_cap < 0 || batch < 0) return SFI_ERR_INVALID_ARG;
+    if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity)
+        return SFI_ERR_INVALID_ARG;
+    if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v)) return SFI_ERR_INVALID_ARG;
+    if ((int64_t)sink + k_cap >= (int64_t(1) << 31)) return SFI_ERR_INVALID_ARG;
+    if (batch == 0) return SFI_OK;
+    sfi::TopkParams p{};
+    p.scores = scores;
+    p.score_stride = score_stride;
+    p.hkv = shape->num_kv_heads;
+    p.seq_lens = kv->seq_lens;
+    p.sink = sink;
+    p.recent = recent;
+    p.k_per_req = k_per_req;
+    p.k_cap = k_cap;
+    p.idx_out = idx_out;
+    p.count_out = count_out;
+    p.req_ids = req_ids;
+    p.dev_status = dev_status;
+    sfi::CopyParams c{};
+    c.k_pool_src = static_cast<const __nv_bfloat16 *>(kv->k_pool);
+    c.v_pool_src = static_cast<const __nv_bfloat16 *>(kv->v_pool);
+    c.num_pages = kv->num_pages;
+    c.max_pages = kv->max_pages_per_req;
+    c.page_table = kv->page_table;
+    c.seq_lens = kv->seq_lens;
+    c.hkv = shape->num_kv_heads;
+    c.head_dim = shape->head_dim;
+    c.req_ids = req_ids;
+    c.dev_status = dev_status;
+    c.k_cap = k_cap;
+    c.sink = sink;
+    c.ck = static_cast<__nv_bfloat16 *>(compact->k);
+    c.cv = static_cast<__nv_bfloat16 *>(compact->v);
+    c.c_total_rows = compact->total_rows;
+    c.c_row_offset = compact->row_offset;
+    c.c_capacity = compact->capacity;
+    return sfi::launch_select_compact(p, c, batch, static_cast<cudaStream_t>(stream)) == cudaSuccess ? SFI_OK
+                                                                                                    : SFI_ERR_CUDA;
+}
+
 }  // extern "C"

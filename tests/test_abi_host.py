@@ -143,3 +143,18 @@ def test_multi_token_calls_validate_on_the_host(libsfi):
     assert libsfi.sfi_paged_kv_append_tokens(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, 5, None, 0, None,
                                              None) == 0
     assert libsfi.sfi_multi_workspace_size(ctypes.byref(sh), 4, 0, 1024, 0) == 0
+
+
+def test_select_compact_validates_on_the_host(libsfi):
+    from sparse_kv_long_sfi_gb300 import _abi
+    sh, kv = _shape(), _paged()
+    comp = _abi.sfi_compact_kv(4096, 4096, 100, 4096, 4096, 4096)
+
+    def call(scores=4096, stride=16, k=4096, idx=4096, cnt=4096, c=comp, batch=1, sink=4):
+        return libsfi.sfi_select_compact(ctypes.byref(sh), ctypes.byref(kv), scores, stride, sink, 32, k, 8, idx, cnt,
+                                         c and ctypes.byref(c), None, batch, None, None)
+
+    assert call(scores=None) == 1 and call(stride=0) == 1 and call(k=None) == 1 and call(idx=None) == 1
+    assert call(cnt=None) == 1 and call(c=None) == 1 and call(sink=-1) == 1
+    assert call(c=_abi.sfi_compact_kv(4097, 4096, 100, 4096, 4096, 4096)) == 1  # unaligned compact K
+    assert call(batch=0) == 0

@@ -596,3 +596,77 @@ def test_mixed_launch_matches_oracle():
         assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
         err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
         assert (err <= prob.score_bound(r, stride)[:, :L][~masked]).all()
+
+
+# ---------------------------------------------------------------------------
+# Selector + compaction in one launch (sfi_select_compact)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("D,Hq,Hkv,lens,k_per_req,k_cap", [
+    (64, 8, 2, [1024, 777, 36, 3, 40], [64, 100, 64, 8, 64], 128),          # L < S, L < S + W, keff < k
+    (128, 16, 8, [300, 21000, 530], [400, 1500, 10], 1600),                  # keff == |C|; |C| > 16384 (rounds)
+    (128, 32, 8, [4096, 2048], [256, 128], 256),
+])
+def test_select_compact_bit_exact(D, Hq, Hkv, lens, k_per_req, k_cap):
+    """The fused Selector + compaction equals the oracle Selector (on the GPU-written scores)
+    followed by the oracle compaction, byte for byte, and leaves the same counts."""
+    sfi = _sfi()
+    S, W = 4, 32
+    prob = Problem(seed=700 + D + len(lens), lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, heavy_frac=0.03).to_device()
+    stride = int(max(lens)) + 8
+    scores = torch.full((prob.B, Hkv, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    comp = _compact_buffers(prob, [k_cap] * prob.B)
+    idx = torch.full((prob.B, Hkv, k_cap), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_compact(prob.shape, prob.d_kv, scores, S, W, dev_i32(k_per_req), idx, comp, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    sc = scores.cpu().numpy()
+    ref_idx, ref_count = run_oracle_selection(prob, sc, k_per_req, k_cap)
+    got_idx, got_count = idx.cpu().numpy(), comp.count.cpu().numpy()
+    np.testing.assert_array_equal(got_count, ref_count)
+    ck, cv = host_bf16(comp.k), host_bf16(comp.v)
+    off, cap = comp.row_offset.cpu().numpy(), comp.capacity.cpu().numpy()
+    for r in range(prob.B):
+        keff = ref_count[r]
+        np.testing.assert_array_equal(got_idx[r, :, :keff], ref_idx[r, :, :keff])
+        assert (got_idx[r, :, keff:] == -7).all(), "entries past k_eff must not be written"
+        rk, rv = oracle_compact_request(prob, r, ref_idx[r], keff, cap[r])
+        ns = min(S, lens[r])
+        for kvh in range(Hkv):
+            base = off[r] + kvh * cap[r]
+            for lo, hi in ((0, ns), (S, S + keff)):
+                np.testing.assert_array_equal(ck[base + lo:base + hi], rk[kvh, lo:hi], err_msg=f"K r={r} kv={kvh}")
+                np.testing.assert_array_equal(cv[base + lo:base + hi], rv[kvh, lo:hi], err_msg=f"V r={r} kv={kvh}")
+
+
+def test_select_compact_subset_and_bad_capacity():
+    """A request subset is handled alone; a request whose capacity is below S + k_eff keeps its
+    selection, is not packed, and is reported."""
+    sfi = _sfi()
+    S, W = 4, 32
+    prob = Problem(seed=720, lens=[800, 900, 1000], Hq=8, Hkv=2, D=128, S=S, W=W).to_device()
+    stride = 1008
+    scores = torch.full((prob.B, 2, stride), float("nan"), device="cuda")
+    _dense(prob, scores=scores)
+    comp = _compact_buffers(prob, [64, 8, 64])  # request 1: capacity S + 8 < S + 64
+    idx = torch.full((prob.B, 2, 64), -7, dtype=torch.int32, device="cuda")
+    st = _status()
+    sfi.sfi_select_compact(prob.shape, prob.d_kv, scores, S, W, dev_i32([64, 64, 64]), idx, comp,
+                           req_ids=dev_i32([2, 1]), dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 4  # SFI_DEV_K_OVERFLOW for request 1
+    sc = scores.cpu().numpy()
+    ref_idx, ref_count = run_oracle_selection(prob, sc, [64, 64, 64], 64)
+    got_idx = idx.cpu().numpy()
+    for r in (1, 2):
+        np.testing.assert_array_equal(got_idx[r], ref_idx[r])
+    assert (got_idx[0] == -7).all()
+    ck = host_bf16(comp.k)
+    off, cap = comp.row_offset.cpu().numpy(), comp.capacity.cpu().numpy()
+    rk, _ = oracle_compact_request(prob, 2, ref_idx[2], 64, cap[2])
+    for kvh in range(2):
+        base = off[2] + kvh * cap[2]
+        np.testing.assert_array_equal(ck[base:base + S + 64], rk[kvh, :S + 64])
+        base1 = off[1] + kvh * cap[1]
+        assert not ck[base1:base1 + cap[1]].any(), "the request with too small a capacity is not packed"
