@@ -404,6 +404,7 @@ def run_gpu(args, ranks: Ranks):
                                                     NL, B, Hq, Hkv, D, P, L0, S, dev, peak)
         result["speculative_sweep"] = speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv,
                                                         D, P, L0, S, W, k_main, dev, peak, seed0)
+        result["other_workloads"] = other_workloads(dev, peak, seed0)
     return result
 
 
@@ -623,6 +624,117 @@ def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hk
             "note": f"{NL} layers per pass, batch {B}, KV {L0} + T; each pass includes the T-token paged append; "
                     "verification writes the recycled statistic (masked logits summed over the group and the "
                     "tokens) for every layer"}
+
+
+OTHER_WORKLOADS = [
+    dict(workload="qwen3-8b-attn kv32k b32", num_q_heads=32, num_kv_heads=8, kv_len=32768, batch=32,
+         retention=0.0625, fast=True),
+    dict(workload="64q/8kv-heads kv64k b8 top-4096", num_q_heads=64, num_kv_heads=8, kv_len=65536, batch=8, k=4096,
+         fast=False),
+]
+
+
+def other_workloads(dev, peak, seed0, layers=4, reps=10):
+    """Per-launch times of the larger workloads: the slow step's three kernels and (where
+    the workload has one) the fast step, each as a graph over `layers` distinct layers
+    (every layer's KV exceeds L2), with the append fused as in the decode cycle."""
+    import torch
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    S, W, D, P = 64, 256, 128, 16
+    stream = torch.cuda.Stream(device=dev)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=stream):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            g.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                g.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps / layers
+
+    out_rows = []
+    for cfg in OTHER_WORKLOADS:
+        Hq, Hkv, L0, B = cfg["num_q_heads"], cfg["num_kv_heads"], cfg["kv_len"], cfg["batch"]
+        shape = sfi.AttnShape(Hq, Hkv, D, P)
+        k = cfg.get("k") or syn.retention_budget(cfg["retention"], L0, S, W)
+        g = syn.rng(seed0, 40, Hq)
+        table, num_pages = syn.make_page_table(g, [L0 + 2] * B, P, shuffle=True)
+        pt = torch.as_tensor(table).to(dev)
+        off, cap = sfi.compact_layout(shape, S, [k] * B, device=dev)
+        batch = sfi.DecodeBatch(pt, off, cap, torch.full((B,), k, dtype=torch.int32, device=dev), k,
+                                score_stride=L0 + 2)
+
+        def init(i, kp, vp):
+            syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 41, Hq, i))
+            syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 42, Hq, i))
+
+        lays = sfi.allocate_layers(shape, layers, num_pages, batch, S, device=dev, pool_init=init)
+        q = torch.empty((layers, B, Hq, D), dtype=torch.bfloat16, device=dev)
+        kn = torch.empty((layers, B, Hkv, D), dtype=torch.bfloat16, device=dev)
+        vn = torch.empty_like(kn)
+        for t, tag in ((q, 43), (kn, 44), (vn, 45)):
+            syn.device_normal_bf16_(t, syn.stream_seed(seed0, tag, Hq))
+        o = torch.empty((layers, B, Hq, D), dtype=torch.float32, device=dev)
+        seq0 = torch.full((B,), L0, dtype=torch.int32, device=dev)
+        seq1 = torch.full((B,), L0 + 1, dtype=torch.int32, device=dev)
+        ws_d = sfi.alloc_workspace(shape, B, L0 + 2 * P, device=dev)
+        max_fast = S + k + W + 2 * P
+        ws_f = sfi.alloc_workspace(shape, B, max_fast, device=dev)
+        flags = sfi.SFI_ATTN_EARLY_KV_PREFETCH
+
+        def slow():
+            for i, Lb in enumerate(lays):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, pt, seq0)
+                sfi.sfi_slow_dense_attn_with_scores(shape, kv, S, W, q[i], o[i], None, Lb.scores, max_tokens=L0 + 2 * P,
+                                                    workspace=ws_d, stream=stream, flags=flags)
+
+        def select():
+            for i, Lb in enumerate(lays):
+                sfi.sfi_select_topk(Lb.scores, Hkv, seq0, S, W, batch.k_per_req, Lb.idx, Lb.compact.count,
+                                    stream=stream)
+
+        def compact():
+            for i, Lb in enumerate(lays):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, pt, seq0)
+                sfi.sfi_compact_gather(shape, kv, Lb.idx, Lb.compact.count, S, Lb.compact, stream=stream)
+
+        def fast():
+            for i, Lb in enumerate(lays):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, pt, seq1)
+                sfi.sfi_fast_decode_attn(shape, kv, Lb.compact, S, W, q[i], o[i], None, k_new=kn[i], v_new=vn[i],
+                                         max_tokens=max_fast, workspace=ws_f, stream=stream, flags=flags)
+
+        t_slow, t_sel, t_cmp = timed(slow), timed(select), timed(compact)
+        nC = L0 - S - W
+        by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True)
+        row = {"workload": cfg["workload"], "k": k, "layers_timed": layers,
+               "slow_us_per_launch": round(t_slow, 2), "slow_GBps": round(by_slow / (t_slow * 1e-6) / 1e9, 1),
+               "slow_frac_of_peak": round(by_slow / (t_slow * 1e-6) / 1e9 / peak, 3),
+               "select_us_per_launch": round(t_sel, 2), "compact_us_per_launch": round(t_cmp, 2),
+               "compact_GBps": round(compact_bytes(B, Hkv, D, S, k) / (t_cmp * 1e-6) / 1e9, 1)}
+        if cfg["fast"]:
+            t_fast = timed(fast)
+            by_fast = fast_bytes(B, Hq, Hkv, D, P, S + k + W, W) + append_bytes(B, Hkv, D)
+            row.update({"fast_us_per_launch": round(t_fast, 2),
+                        "fast_GBps": round(by_fast / (t_fast * 1e-6) / 1e9, 1),
+                        "fast_frac_of_peak": round(by_fast / (t_fast * 1e-6) / 1e9 / peak, 3),
+                        "dense_over_fast": round(t_slow / t_fast, 2)})
+        out_rows.append(row)
+        del lays, q, kn, vn, o, ws_d, ws_f
+        torch.cuda.empty_cache()
+    return {"points": out_rows, "note": "per launch = one layer; slow = dense attention + masked scores (no append), "
+                                        "fast = the sparse step with the fused append; Selector and compaction as in "
+                                        "the slow step; bytes as in the main workload's roofline"}
 
 
 # ---------------------------------------------------------------------------
