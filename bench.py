@@ -182,7 +182,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "d2ac0c4b26af87fd", "fast": 68_327_168 + 1_054_720, "slow": 1_074_307_000 + 6_511_360}
+PROFILED_TRAFFIC = {"sha256_16": "fe148a0a14c8b7fa", "fast": 68_343_040 + 1_088_000, "slow": 1_074_230_000 + 6_153_472}
 
 
 def profiled_traffic(kind):
