@@ -9,11 +9,10 @@
 //    -inf).
 //  * The candidates are walked in rounds of 16384 positions; in a round, warp w owns
 //    the contiguous positions [512 w, 512 w + 512) and lane l holds positions
-//    512 w + 32 j + l, j < 16. With at most one round (|C| <= 16384) the whole score
-//    row is first moved into shared memory by one TMA bulk copy (many small loads per
-//    thread would be limited by the SM's outstanding misses), and the keys stay in
-//    registers for the whole selection: the scores are read from memory once. Longer
-//    rows are read round by round with 16 independent coalesced loads per thread.
+//    512 w + 32 j + l, j < 16. Rounds reach shared memory through TMA bulk copies
+//    (many small loads per thread would be limited by the SM's outstanding misses):
+//    with one round the keys then stay in registers for the whole selection, with two
+//    both rounds stay in shared memory, with more they stream through two buffers.
 //  * Radix select, 4 passes of 8 bits from the top: a 256-bin shared histogram of the
 //    keys that share the current prefix (warp-aggregated atomics via match.any),
 //    then one warp scans the bins from the top to find the bin holding the k-th key.
@@ -43,16 +42,6 @@ __device__ __forceinline__ uint32_t order_key(float x) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// Keys of one round for this thread: position base + 512 * warp + 32 * j + lane.
-__device__ __forceinline__ void load_round(const float *row, int n, int base, int warp, int lane,
-                                           uint32_t (&key)[kTopkPerThread]) {
-#pragma unroll
-    for (int j = 0; j < kTopkPerThread; ++j) {
-        const int i = base + warp * (32 * kTopkPerThread) + 32 * j + lane;
-        key[j] = i < n ? order_key(__ldg(row + i)) : kNoKey;
-    }
-}
-
 // Add this thread's keys that share `prefix` under `mask` to the histogram of bits [shift, shift+8).
 __device__ __forceinline__ void histogram_round(const uint32_t (&key)[kTopkPerThread], uint32_t prefix, uint32_t mask,
                                                 int shift, int lane, uint32_t *hist) {
@@ -68,8 +57,8 @@ __device__ __forceinline__ void histogram_round(const uint32_t (&key)[kTopkPerTh
     }
 }
 
-// Dynamic shared memory: one round of scores.
-constexpr int kTopkSmemBytes = kTopkRound * 4;
+// Dynamic shared memory: two round buffers of scores, then the lane-replicated histogram.
+constexpr int kTopkSmemBytes = 2 * kTopkRound * 4 + 256 * 32 * 4;
 
 // The same histogram with one counter per (bin, lane): hrep[bin * 32 + lane]. One
 // shared atomic per key and no warp aggregation; a warp's 32 atomics go to 32 banks.
@@ -150,7 +139,7 @@ __device__ __forceinline__ void gather_compact(const CopyParams &c, int r, int k
 template <int D>
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p, const CopyParams c) {
     extern __shared__ __align__(16) float s_keys[];
-    __shared__ __align__(8) uint64_t s_bar;
+    __shared__ __align__(8) uint64_t s_bar[2];
     __shared__ uint32_t hist[256];
     __shared__ uint32_t s_bin, s_rem;
     __shared__ int32_t s_gt[kTopkMaxRounds * kTopkWarps], s_eq[kTopkMaxRounds * kTopkWarps];
@@ -184,39 +173,65 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
         return;
     }
 
-    uint32_t key[kTopkPerThread];
-    if (rounds == 1) {  // resident for the whole selection
-        // Bulk copy [a0, a1) of the row: a0 = its start rounded up, a1 = its end rounded
-        // down to 16 bytes (the copy never leaves the row); the few floats outside are
-        // read directly.
-        const uintptr_t a = reinterpret_cast<uintptr_t>(row);
+    // Rounds of 16384 candidates come into shared memory by TMA bulk copies (each
+    // copy covers the round's 16-byte-aligned interior and never leaves the row; the
+    // few floats outside are read directly). One round: its keys stay in registers for
+    // the whole selection. Two rounds: both stay in the two buffers. More: every use of
+    // a round (4 radix passes, the counts, the output) streams through the two buffers,
+    // the next copy in flight while the current round is read.
+    float *const sbuf = s_keys;                                             // [2][kTopkRound]
+    uint32_t *hrep = reinterpret_cast<uint32_t *>(s_keys + 2 * kTopkRound);  // [256][32] lane counters
+    const int total_uses = 6 * rounds;
+    auto issue = [&](int b, int rd) {  // thread 0: copy round rd into buffer b
+        const int base = rd * kTopkRound, len = min(kTopkRound, n - base);
+        const uintptr_t a = reinterpret_cast<uintptr_t>(row + base);
         const uintptr_t a0 = (a + 15) & ~uintptr_t(15);
-        const uintptr_t a1 = (a + 4 * (uintptr_t)n) & ~uintptr_t(15);
-        const int lo_i = (int)((a0 - a) >> 2);                    // row[i], lo_i <= i < hi_i, is s_keys[i - lo_i]
+        const uintptr_t a1 = (a + 4 * (uintptr_t)len) & ~uintptr_t(15);
+        if (a1 > a0) {
+            mbar_arrive_expect_tx(&s_bar[b], (uint32_t)(a1 - a0));
+            bulk_load_1d(sbuf + b * kTopkRound, reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0), &s_bar[b]);
+        } else {
+            mbar_arrive(&s_bar[b]);
+        }
+    };
+    uint32_t key[kTopkPerThread];
+    auto fetch = [&](int u) -> bool {  // this thread's keys of use u: round u % rounds, buffer u & 1
+        const int rd = u % rounds, b = u & 1, base = rd * kTopkRound, len = min(kTopkRound, n - base);
+        if ((rounds != 2 || u < 2) && !mbar_wait_warp(&s_bar[b], (u >> 1) & 1)) return false;
+        const uintptr_t a = reinterpret_cast<uintptr_t>(row + base);
+        const uintptr_t a0 = (a + 15) & ~uintptr_t(15);
+        const uintptr_t a1 = (a + 4 * (uintptr_t)len) & ~uintptr_t(15);
+        const int lo_i = (int)((a0 - a) >> 2);  // row[base + i], lo_i <= i < hi_i, is sbuf[b][i - lo_i]
         const int hi_i = a1 > a0 ? (int)((a1 - a) >> 2) : lo_i;
-        if (tid == 0) {
-            mbar_init(&s_bar, 1);
-            fence_barrier_init();
-            if (a1 > a0) {
-                mbar_arrive_expect_tx(&s_bar, (uint32_t)(a1 - a0));
-                bulk_load_1d(s_keys, reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0), &s_bar);
-            } else {
-                mbar_arrive(&s_bar);
-            }
-        }
-        __syncthreads();
-        if (!mbar_wait_warp(&s_bar, 0)) {  // bounded; the copy is the same for every warp
-            if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
+        const float *bb = sbuf + b * kTopkRound;
 #pragma unroll
         for (int j = 0; j < kTopkPerThread; ++j) {
             const int i = warp * (32 * kTopkPerThread) + 32 * j + lane;
-            key[j] = i < n ? order_key(i >= lo_i && i < hi_i ? s_keys[i - lo_i] : __ldg(row + i)) : kNoKey;
+            key[j] = i < len ? order_key(i >= lo_i && i < hi_i ? bb[i - lo_i] : __ldg(row + base + i)) : kNoKey;
         }
-        __syncthreads();  // every warp has its keys; s_keys is reused below
+        return true;
+    };
+    auto release = [&](int u) {  // every thread has read use u: refill its buffer with use u + 2
+        if (rounds >= 3 && u + 2 < total_uses) {
+            __syncthreads();
+            if (tid == 0) issue(u & 1, (u + 2) % rounds);
+        }
+    };
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        fence_barrier_init();
+        issue(0, 0);
+        if (rounds > 1) issue(1, 1);
     }
-    uint32_t *hrep = reinterpret_cast<uint32_t *>(s_keys);  // [256][32] lane counters (first two passes)
+    __syncthreads();
+    int use = 0;
+    if (rounds == 1) {  // resident in registers for the whole selection
+        if (!fetch(use++)) {
+            if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+    }
 
     // ---- radix select of the keff-th largest key ----
     uint32_t prefix = 0u, mask = 0u;
@@ -234,9 +249,13 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             else histogram_round(key, prefix, mask, shift, lane, hist);
         } else {
             for (int rd = 0; rd < rounds; ++rd) {
-                load_round(row, n, rd * kTopkRound, warp, lane, key);
+                if (!fetch(use)) {
+                    if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+                    return;
+                }
                 if (lanes) histogram_lanes(key, prefix, mask, shift, lane, hrep);
                 else histogram_round(key, prefix, mask, shift, lane, hist);
+                release(use++);
             }
         }
         __syncthreads();
@@ -291,7 +310,10 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
 
     // ---- ascending output: counts per (round, warp), scan, then ranked writes ----
     for (int rd = 0; rd < rounds; ++rd) {
-        if (rounds > 1) load_round(row, n, rd * kTopkRound, warp, lane, key);
+        if (rounds > 1 && !fetch(use)) {
+            if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
         int gt = 0, eq = 0;
 #pragma unroll
         for (int j = 0; j < kTopkPerThread; ++j) {
@@ -302,6 +324,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             s_gt[rd * kTopkWarps + warp] = gt;
             s_eq[rd * kTopkWarps + warp] = eq;
         }
+        if (rounds > 1) release(use++);
     }
     __syncthreads();
     if (warp == 0) {  // exclusive scan over (round, warp) in position order
@@ -334,7 +357,10 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     // memory (s_keys is free by now) and written out with one coalesced pass.
     int32_t *dst = rounds == 1 ? reinterpret_cast<int32_t *>(s_keys) : out;
     for (int rd = 0; rd < rounds; ++rd) {
-        if (rounds > 1) load_round(row, n, rd * kTopkRound, warp, lane, key);
+        if (rounds > 1 && !fetch(use)) {
+            if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
         int eq_before = s_eq[rd * kTopkWarps + warp];
         int out_pos = s_gt[rd * kTopkWarps + warp] + min(eq_before, take_eq);
 #pragma unroll
@@ -351,6 +377,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             out_pos += __popc(take_bal);
             eq_before += __popc(eq_bal);
         }
+        if (rounds > 1) release(use++);
     }
     __syncthreads();  // the selection is complete (in shared memory, or in `out` for long rows)
     if (rounds == 1)
