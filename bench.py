@@ -596,16 +596,16 @@ def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hk
         def verify():
             for i, Lb in enumerate(layers):
                 kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
-                sfi.sfi_paged_kv_append_tokens(shape, kv, kn[i], vn[i], T, stream=dec.main)
                 sfi.sfi_dense_verify_attn(shape, kv, S, W, q[i], T, o[i], None, Lb.scores, max_tokens=L + P,
-                                          workspace=ws_v, stream=dec.main)
+                                          workspace=ws_v, stream=dec.main, flags=dec.attn_flags, k_new=kn[i],
+                                          v_new=vn[i])
 
         def draft():
             for i, Lb in enumerate(layers):
                 kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
-                sfi.sfi_paged_kv_append_tokens(shape, kv, kn[i], vn[i], T, stream=dec.main)
                 sfi.sfi_sparse_draft_attn(shape, kv, Lb.compact, S, W, q[i], T, o[i], None, max_tokens=max_draft,
-                                          workspace=ws_d, stream=dec.main)
+                                          workspace=ws_d, stream=dec.main, flags=dec.attn_flags, k_new=kn[i],
+                                          v_new=vn[i])
 
         us_v, us_d = time_graph(verify), time_graph(draft)
         qo = B * T * Hq * (D * (2 + 4) + 4)
@@ -621,7 +621,8 @@ def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hk
                      "draft_frac_of_peak": round(by_d / (us_d * 1e-6) / 1e9 / peak, 3)})
     dec.pending = [False] * len(layers)
     return {"points": rows, "retention_pct_of_draft": round(100 * (S + k_main + W) / L0, 2),
-            "note": f"{NL} layers per pass, batch {B}, KV {L0} + T; each pass includes the T-token paged append; "
+            "note": f"{NL} layers per pass, batch {B}, KV {L0} + T; each pass includes the T-token paged append "
+                    "(fused into the attention kernel); "
                     "verification writes the recycled statistic (masked logits summed over the group and the "
                     "tokens) for every layer"}
 

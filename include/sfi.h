@@ -239,10 +239,14 @@ SFI_API size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_f
  * recallable KV state; a full-context verification checks them and its per-head
  * attention statistics are recycled as the importance signal, with no extra forward.
  * Here a request carries T = num_tokens query tokens at positions L - T .. L - 1
- * (L = seq_lens[r] counts them; their K/V must already be in the pages, e.g. by
- * sfi_paged_kv_append_tokens). Query token t sees the context as it stands at length
+ * (L = seq_lens[r] counts them). Query token t sees the context as it stands at length
  * L_t = L - T + t + 1 (causal).
  *   q   : bf16 [B][T][Hq][D], indexed by request id
+ *   k_new, v_new : bf16 [B][T][Hkv][D] or both NULL. When given, the call first does
+ *         what sfi_paged_kv_append_tokens does (the T tokens go to their page slots)
+ *         and attends to the cache after that append; otherwise their K/V must already
+ *         be in the pages. In the draft call the T positions must lie past the sink
+ *         (L - T >= S): the compact buffer is not written.
  *   out : fp32 [B][T][Hq][D], 8-byte aligned;  lse : fp32 [B][T][Hq] or NULL
  * T x G > 16 returns SFI_ERR_UNSUPPORTED.
  */
@@ -269,14 +273,16 @@ SFI_API sfi_status sfi_paged_kv_append_tokens(const sfi_attn_shape *shape, const
  * length, whose candidate set [S, L' - W) lies inside the scored one.
  *   scores, score_stride : as for sfi_slow_dense_attn_with_scores
  *   max_tokens : an upper bound on L + P over the batch (split planning only)
- *   num_splits, flags : as for sfi_fast_decode_attn
+ *   num_splits, flags : as for sfi_fast_decode_attn (with k_new/v_new the append is
+ *                part of the call, so SFI_ATTN_EARLY_KV_PREFETCH remains valid)
  *   workspace  : at least sfi_multi_workspace_size(shape, batch, T, max_tokens,
  *                num_splits) bytes, zero-filled before first use (kept so).
  * Device errors: SFI_DEV_BAD_LEN (also L < T, or L > score_stride), SFI_DEV_BAD_PAGE,
  * SFI_DEV_TIMEOUT.
  */
 SFI_API sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink,
-                                         int32_t recent, const void *q, int32_t num_tokens, float *out, float *lse,
+                                         int32_t recent, const void *q, int32_t num_tokens, const void *k_new,
+                                         const void *v_new, float *out, float *lse,
                                          float *scores, int64_t score_stride, const int32_t *req_ids, int32_t batch,
                                          int32_t max_tokens, int32_t num_splits, uint32_t flags, void *workspace,
                                          size_t workspace_bytes, int32_t *dev_status, void *stream);
@@ -293,7 +299,8 @@ SFI_API sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_
  */
 SFI_API sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv,
                                          const sfi_compact_kv *compact, int32_t sink, int32_t recent, const void *q,
-                                         int32_t num_tokens, float *out, float *lse, const int32_t *req_ids,
+                                         int32_t num_tokens, const void *k_new, const void *v_new, float *out,
+                                         float *lse, const int32_t *req_ids,
                                          int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
                                          void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 

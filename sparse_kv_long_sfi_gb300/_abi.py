@@ -52,10 +52,10 @@ PROTOTYPES = {
                                       c_vp, c_vp]),
     "sfi_mixed_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32, c_i32]),
     "sfi_paged_kv_append_tokens": (c_i32, [P_SHAPE, P_PAGED, c_vp, c_vp, c_i32, c_vp, c_i32, c_vp, c_vp]),
-    "sfi_dense_verify_attn": (c_i32, [P_SHAPE, P_PAGED, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_i64, c_vp,
-                                      c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
-    "sfi_sparse_draft_attn": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp,
-                                      c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_dense_verify_attn": (c_i32, [P_SHAPE, P_PAGED, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp, c_vp,
+                                      c_i64, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
+    "sfi_sparse_draft_attn": (c_i32, [P_SHAPE, P_PAGED, P_COMPACT, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_vp,
+                                      c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_sz, c_vp, c_vp]),
     "sfi_multi_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32, c_i32]),
     "sfi_select_topk": (c_i32, [c_vp, c_i64, c_i32, c_vp, c_i32, c_i32, c_vp, c_i32, c_vp, c_vp, c_vp, c_i32, c_vp,
                                 c_vp]),

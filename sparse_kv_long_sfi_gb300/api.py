@@ -217,12 +217,14 @@ def sfi_dense_verify_attn(shape: AttnShape, kv: PagedKV, sink: int, recent: int,
                           scores: Optional[torch.Tensor] = None, req_ids: Optional[torch.Tensor] = None,
                           batch: Optional[int] = None, max_tokens: int = 0, num_splits: int = 0,
                           workspace: Optional[torch.Tensor] = None, dev_status: Optional[torch.Tensor] = None,
-                          stream=None, flags: int = 0):
+                          stream=None, flags: int = 0, k_new: Optional[torch.Tensor] = None,
+                          v_new: Optional[torch.Tensor] = None):
     ws = _ptr(workspace, torch.uint8, "workspace")
     stride = 0 if scores is None else int(scores.shape[-1])
     st = _abi.lib().sfi_dense_verify_attn(
         ctypes.byref(shape.c()), ctypes.byref(kv.c()), int(sink), int(recent), _ptr(q, torch.bfloat16, "q"),
-        int(num_tokens), _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
+        int(num_tokens), _ptr(k_new, torch.bfloat16, "k_new"), _ptr(v_new, torch.bfloat16, "v_new"),
+        _ptr(out, torch.float32, "out"), _ptr(lse, torch.float32, "lse"),
         _ptr(scores, torch.float32, "scores"), stride, _ptr(req_ids, torch.int32, "req_ids"),
         _batch(batch, req_ids, kv.seq_lens), int(max_tokens), int(num_splits), int(flags), ws,
         0 if workspace is None else workspace.numel(), _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))
@@ -233,11 +235,13 @@ def sfi_sparse_draft_attn(shape: AttnShape, kv: PagedKV, compact: CompactKV, sin
                           q: torch.Tensor, num_tokens: int, out: torch.Tensor, lse: Optional[torch.Tensor] = None,
                           req_ids: Optional[torch.Tensor] = None, batch: Optional[int] = None, max_tokens: int = 0,
                           num_splits: int = 0, workspace: Optional[torch.Tensor] = None,
-                          dev_status: Optional[torch.Tensor] = None, stream=None, flags: int = 0):
+                          dev_status: Optional[torch.Tensor] = None, stream=None, flags: int = 0,
+                          k_new: Optional[torch.Tensor] = None, v_new: Optional[torch.Tensor] = None):
     ws = _ptr(workspace, torch.uint8, "workspace")
     st = _abi.lib().sfi_sparse_draft_attn(
         ctypes.byref(shape.c()), ctypes.byref(kv.c()), ctypes.byref(compact.c()), int(sink), int(recent),
-        _ptr(q, torch.bfloat16, "q"), int(num_tokens), _ptr(out, torch.float32, "out"),
+        _ptr(q, torch.bfloat16, "q"), int(num_tokens), _ptr(k_new, torch.bfloat16, "k_new"),
+        _ptr(v_new, torch.bfloat16, "v_new"), _ptr(out, torch.float32, "out"),
         _ptr(lse, torch.float32, "lse"), _ptr(req_ids, torch.int32, "req_ids"), _batch(batch, req_ids, kv.seq_lens),
         int(max_tokens), int(num_splits), int(flags), ws, 0 if workspace is None else workspace.numel(),
         _ptr(dev_status, torch.int32, "dev_status"), _stream(stream))

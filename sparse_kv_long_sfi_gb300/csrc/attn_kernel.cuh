@@ -266,6 +266,38 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
     }
 }
 
+// Multi-token form of the fused append: the query tokens at positions [L - T, L) that
+// fall in this paged sub-block (positions [pos0, pos0 + 16)) replace their rows of the
+// tile and are written to the page (k_new/v_new: [request][T][Hkv][D]).
+template <int D>
+__device__ __forceinline__ void fuse_tokens(uint8_t *tile, const AttnParams &p, int r, int kvh, int L, int pos0,
+                                            int lane) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
+    const int ntok = p.tokens;
+    const int first = max(L - ntok, pos0), last = min(L, pos0 + kSubTokens);
+    const int page = p.page_table[(int64_t)r * p.max_pages + pos0 / kSubTokens];
+    const bool page_ok = page >= 0 && page < p.num_pages;
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const __nv_bfloat16 *src0 = (is_v ? p.v_new : p.k_new) + (int64_t)kvh * D + c * 8;
+        __nv_bfloat16 *dst0 = (is_v ? p.v_pool_w : p.k_pool_w) + ((int64_t)page * p.hkv + kvh) * kSubTokens * D + c * 8;
+        uint8_t *base0 = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128);
+#pragma unroll 4
+        for (int pos = first; pos < last; ++pos) {
+            const int tok = pos - (L - ntok);
+            const int4 val = *reinterpret_cast<const int4 *>(src0 + ((int64_t)r * ntok + tok) * p.hkv * D);
+            const int row = pos - pos0;
+            *reinterpret_cast<int4 *>(base0 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
+            if (page_ok) *reinterpret_cast<int4 *>(dst0 + (int64_t)row * D) = val;
+        }
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    if (!page_ok && lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
+    __syncwarp();
+}
+
 // Bounds [lo, hi) of the tokens of a 16-token sub-block that one query row sees.
 struct RowSpan {
     int lo, hi;
@@ -744,6 +776,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             // past sb_end may carry the same index).
             fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane,
                                   s_app_val, &s_app_page);
+        }
+        if (MQ && p.k_new != nullptr && in.y >= 0 && sb_begin + st * kConsumerWarps + warp < sb_end &&
+            in.y + kSubTokens > u.L0 - 1 && in.y < u.L) {
+            // Fused append of the query tokens (positions [L - T, L)) in this paged sub-block.
+            fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane);
         }
         if (hi > lo) {
             const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);

@@ -418,7 +418,8 @@ size_t sfi_multi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int3
 }
 
 sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink, int32_t recent,
-                                 const void *q, int32_t num_tokens, float *out, float *lse, float *scores,
+                                 const void *q, int32_t num_tokens, const void *k_new, const void *v_new, float *out,
+                                 float *lse, float *scores,
                                  int64_t score_stride, const int32_t *req_ids, int32_t batch, int32_t max_tokens,
                                  int32_t num_splits, uint32_t flags, void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, void *stream) {
@@ -429,12 +430,16 @@ sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv
         return SFI_ERR_INVALID_ARG;
     if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return SFI_ERR_INVALID_ARG;
     if (num_tokens * (shape->num_q_heads / shape->num_kv_heads) > sfi::kMaxRows) return SFI_ERR_UNSUPPORTED;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return SFI_ERR_INVALID_ARG;
     if (scores && score_stride <= 0) return SFI_ERR_INVALID_ARG;
     if (batch == 0) return SFI_OK;
     AttnParams p{};
     fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
     p.tokens = num_tokens;
     p.rows = num_tokens * p.group;
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
     p.scores = scores;
     p.score_stride = score_stride;
@@ -456,8 +461,8 @@ sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv
 }
 
 sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
-                                 int32_t sink, int32_t recent, const void *q, int32_t num_tokens, float *out,
-                                 float *lse, const int32_t *req_ids, int32_t batch, int32_t max_tokens,
+                                 int32_t sink, int32_t recent, const void *q, int32_t num_tokens, const void *k_new,
+                                 const void *v_new, float *out, float *lse, const int32_t *req_ids, int32_t batch, int32_t max_tokens,
                                  int32_t num_splits, uint32_t flags, void *workspace, size_t workspace_bytes,
                                  int32_t *dev_status, void *stream) {
     sfi_status st = check_shape(shape);
@@ -467,6 +472,8 @@ sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv
         return SFI_ERR_INVALID_ARG;
     if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return SFI_ERR_INVALID_ARG;
     if (num_tokens * (shape->num_q_heads / shape->num_kv_heads) > sfi::kMaxRows) return SFI_ERR_UNSUPPORTED;
+    if ((k_new == nullptr) != (v_new == nullptr) || (k_new && (!aligned16(k_new) || !aligned16(v_new))))
+        return SFI_ERR_INVALID_ARG;
     if (!compact || !compact->k || !compact->v || !compact->row_offset || !compact->capacity || !compact->count)
         return SFI_ERR_INVALID_ARG;
     if (compact->total_rows <= 0 || !aligned16(compact->k) || !aligned16(compact->v)) return SFI_ERR_INVALID_ARG;
@@ -476,6 +483,8 @@ sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     fill_common(p, shape, kv, q, out, lse, req_ids, sink, recent, dev_status);
     p.tokens = num_tokens;
     p.rows = num_tokens * p.group;
+    p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
+    p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
     p.c_row_offset = compact->row_offset;
     p.c_capacity = compact->capacity;

@@ -186,6 +186,17 @@ class SFIDecoder:
                             dev_status=self.dev_status, stream=self.main)
         return None, None
 
+    def _append_tokens(self, i, kv, io, T, append, req_ids, n):
+        """The T newest tokens of layer i: returned for the multi-token kernel to write
+        (fused), or written now by the T-token append kernel."""
+        if not append:
+            return None, None
+        if self.fuse_append:
+            return io.k_new[i], io.v_new[i]
+        sfi_paged_kv_append_tokens(self.shape, kv, io.k_new[i], io.v_new[i], T, req_ids=req_ids, batch=n,
+                                   dev_status=self.dev_status, stream=self.main)
+        return None, None
+
     def _enter(self):
         """Order the main stream after the caller's stream (inputs such as seq_lens, q or
         k_new may have just been written there; torch streams do not synchronise with
@@ -329,14 +340,12 @@ class SFIDecoder:
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
-            if append:
-                sfi_paged_kv_append_tokens(self.shape, kv, io.k_new[i], io.v_new[i], T, req_ids=req_ids, batch=n,
-                                           dev_status=self.dev_status, stream=self.main)
+            kn, vn = self._append_tokens(i, kv, io, T, append, req_ids, n)
             self._mark("verify", "start")
             sfi_dense_verify_attn(self.shape, kv, self.sink, self.recent, io.q[i], T, io.out[i],
                                   None if io.lse is None else io.lse[i], L.scores, req_ids=req_ids, batch=n,
                                   max_tokens=self.max_dense_tokens, workspace=ws_v, dev_status=self.dev_status,
-                                  stream=self.main)
+                                  stream=self.main, flags=self.attn_flags, k_new=kn, v_new=vn)
             self._mark("verify", "end")
         self._leave()
 
@@ -362,14 +371,12 @@ class SFIDecoder:
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
-            if append:
-                sfi_paged_kv_append_tokens(self.shape, kv, io.k_new[i], io.v_new[i], T, req_ids=req_ids, batch=n,
-                                           dev_status=self.dev_status, stream=self.main)
+            kn, vn = self._append_tokens(i, kv, io, T, append, req_ids, n)
             self._mark("draft", "start")
             sfi_sparse_draft_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], T, io.out[i],
                                   None if io.lse is None else io.lse[i], req_ids=req_ids, batch=n,
                                   max_tokens=self.max_fast_tokens + T, workspace=ws_d, dev_status=self.dev_status,
-                                  stream=self.main)
+                                  stream=self.main, flags=self.attn_flags, k_new=kn, v_new=vn)
             self._mark("draft", "end")
         self._leave()
 

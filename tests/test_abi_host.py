@@ -122,12 +122,12 @@ def test_multi_token_calls_validate_on_the_host(libsfi):
     comp = _abi.sfi_compact_kv(4096, 4096, 100, 4096, 4096, 4096)
 
     def verify(T, batch=1, scores=None, stride=0):
-        return libsfi.sfi_dense_verify_attn(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, T, 8192, None, scores,
-                                            stride, None, batch, 0, 0, 0, None, 0, None, None)
+        return libsfi.sfi_dense_verify_attn(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, T, None, None, 8192, None,
+                                            scores, stride, None, batch, 0, 0, 0, None, 0, None, None)
 
     def draft(T, c=comp, batch=1):
         return libsfi.sfi_sparse_draft_attn(ctypes.byref(sh), ctypes.byref(kv), c and ctypes.byref(c), 4, 32, 4096,
-                                            T, 8192, None, None, batch, 0, 0, 0, None, 0, None, None)
+                                            T, None, None, 8192, None, None, batch, 0, 0, 0, None, 0, None, None)
 
     assert verify(0) == 1 and verify(17) == 1
     assert verify(9) == 2                      # 9 tokens x G = 2 > 16 rows
@@ -136,8 +136,11 @@ def test_multi_token_calls_validate_on_the_host(libsfi):
     assert draft(0) == 1 and draft(9) == 2 and draft(4, c=None) == 1
     assert draft(8, batch=0) == 0
     sh8 = _shape(32, 4)                        # G = 8: two tokens
-    assert libsfi.sfi_dense_verify_attn(ctypes.byref(sh8), ctypes.byref(kv), 4, 32, 4096, 3, 8192, None, None, 0,
-                                        None, 1, 0, 0, 0, None, 0, None, None) == 2
+    assert libsfi.sfi_dense_verify_attn(ctypes.byref(sh8), ctypes.byref(kv), 4, 32, 4096, 3, None, None, 8192, None,
+                                        None, 0, None, 1, 0, 0, 0, None, 0, None, None) == 2
+    # k_new without v_new
+    assert libsfi.sfi_dense_verify_attn(ctypes.byref(sh), ctypes.byref(kv), 4, 32, 4096, 2, 4096, None, 8192, None,
+                                        None, 0, None, 1, 0, 0, 0, None, 0, None, None) == 1
     assert libsfi.sfi_paged_kv_append_tokens(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, 0, None, 1, None,
                                              None) == 1
     assert libsfi.sfi_paged_kv_append_tokens(ctypes.byref(sh), ctypes.byref(kv), 4096, 4096, 5, None, 0, None,

@@ -224,3 +224,90 @@ def test_draft_d64_g4_and_subset():
 
 def test_draft_g8_two_tokens():
     _draft_case(560, [1500, 800, 47], 64, 8, 128, 4, 32, 2, [100, 50, 5], 128, splits=3)
+
+
+@pytest.mark.parametrize("T,splits,flags", [(4, 0, 0), (8, 3, 1), (3, 12, 1), (16, 1, 0)])
+def test_verify_with_fused_append_matches_oracle(T, splits, flags):
+    """k_new/v_new given to the verification: it equals the T-token append followed by the
+    verification, pages included, with and without early KV prefetch."""
+    sfi = _sfi()
+    Hq, Hkv = (8, 8) if T == 16 else (16, 8)
+    prob = Problem(seed=800 + T, lens=[300, 1023, 17, 40], Hq=Hq, Hkv=Hkv, D=128, S=4, W=32,
+                   extra_tokens=T).to_device()
+    g = syn.rng(403, T)
+    kn, vn = syn.normal_bf16(g, (prob.B, T, Hkv, 128)), syn.normal_bf16(g, (prob.B, T, Hkv, 128))
+    lens = prob.lens + T
+    prob.set_lens(lens)
+    q = _queries(810 + T, prob.B, T, Hq, 128)
+    stride = int(lens.max())
+    scores = torch.full((prob.B, Hkv, stride), float("nan"), device="cuda")
+    out = torch.full((prob.B, T, Hq, 128), float("nan"), device="cuda")
+    maxL = stride + 16
+    ws = sfi.alloc_multi_workspace(prob.shape, prob.B, T, maxL, splits)
+    st = _status()
+    sfi.sfi_dense_verify_attn(prob.shape, prob.d_kv, prob.S, prob.W, dev_bf16(q), T, out, None, scores,
+                              max_tokens=maxL, num_splits=splits, workspace=ws, dev_status=st, flags=flags,
+                              k_new=dev_bf16(kn), v_new=dev_bf16(vn))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for r in range(prob.B):
+        oracle.paged_append_tokens(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], lens[r], T, kn[r], vn[r],
+                                   Hkv, 128, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.v_pool), prob.kv.v_pool)
+    o, sc = out.cpu().numpy(), scores.cpu().numpy()
+    for r in range(prob.B):
+        o_ref, _ = oracle.verify_attn(q[r], prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], lens[r], T, Hq, Hkv,
+                                      128, 16)
+        assert_close(o[r], o_ref, f"out r={r}")
+        ref = oracle.verify_scores(q[r], prob.kv.k_pool, prob.kv.page_table[r], lens[r], T, prob.S, prob.W, Hq, Hkv,
+                                   128, 16, stride=stride)
+        L = lens[r]
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), np.isneginf(ref[:, :L]))
+
+
+@pytest.mark.parametrize("T,flags", [(4, 1), (8, 0)])
+def test_draft_with_fused_append_matches_oracle(T, flags):
+    """k_new/v_new given to the draft pass: equals the T-token append followed by the draft."""
+    sfi = _sfi()
+    S, W, Hq, Hkv, D = 4, 32, 16, 8, 128
+    lens_slow = [1024, 530, 36]
+    k_per_req, k_cap = [64, 100, 5], 128
+    prob = Problem(seed=820 + T, lens=lens_slow, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, extra_tokens=T,
+                   heavy_frac=0.02).to_device()
+    stride = int(max(lens_slow))
+    scores = torch.full((prob.B, Hkv, stride), float("nan"), device="cuda")
+    st = _status()
+    ws1 = sfi.alloc_workspace(prob.shape, prob.B, stride + 16)
+    o1 = torch.empty((prob.B, Hq, D), device="cuda")
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, S, W, prob.d_q, o1, None, scores,
+                                        max_tokens=stride + 16, workspace=ws1, dev_status=st)
+    comp = _compact_buffers(prob, k_per_req)
+    idx = torch.zeros((prob.B, Hkv, k_cap), dtype=torch.int32, device="cuda")
+    sfi.sfi_select_compact(prob.shape, prob.d_kv, scores, S, W, dev_i32(k_per_req), idx, comp, dev_status=st)
+    torch.cuda.synchronize()
+    ref_idx, ref_count = run_oracle_selection(prob, scores.cpu().numpy(), k_per_req, k_cap)
+    cap = comp.capacity.cpu().numpy()
+    ref_compact = [oracle_compact_request(prob, r, ref_idx[r], ref_count[r], cap[r]) for r in range(prob.B)]
+    g = syn.rng(404, T)
+    kn, vn = syn.normal_bf16(g, (prob.B, T, Hkv, D)), syn.normal_bf16(g, (prob.B, T, Hkv, D))
+    lens = prob.lens + T
+    prob.set_lens(lens)
+    q = _queries(830 + T, prob.B, T, Hq, D)
+    out = torch.full((prob.B, T, Hq, D), float("nan"), device="cuda")
+    max_tokens = S + k_cap + W + T + 32
+    ws = sfi.alloc_multi_workspace(prob.shape, prob.B, T, max_tokens)
+    sfi.sfi_sparse_draft_attn(prob.shape, prob.d_kv, comp, S, W, dev_bf16(q), T, out, None, max_tokens=max_tokens,
+                              workspace=ws, dev_status=st, flags=flags, k_new=dev_bf16(kn), v_new=dev_bf16(vn))
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    for r in range(prob.B):
+        oracle.paged_append_tokens(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], lens[r], T, kn[r], vn[r],
+                                   Hkv, D, 16)
+    np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
+    o = out.cpu().numpy()
+    for r in range(prob.B):
+        rk, rv = ref_compact[r]
+        o_ref, _ = oracle.fast_multi_attn(q[r], rk, rv, ref_count[r], prob.kv.k_pool, prob.kv.v_pool,
+                                          prob.kv.page_table[r], lens[r], T, S, W, Hq, Hkv, D, 16)
+        assert_close(o[r], o_ref, f"draft out r={r}")
