@@ -405,6 +405,7 @@ def run_gpu(args, ranks: Ranks):
         result["speculative_sweep"] = speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv,
                                                         D, P, L0, S, W, k_main, dev, peak, seed0)
         result["other_workloads"] = other_workloads(dev, peak, seed0)
+        result["ragged_mixed_step"] = ragged_mixed_step(dev, peak, seed0)
     return result
 
 
@@ -736,6 +737,109 @@ def other_workloads(dev, peak, seed0, layers=4, reps=10):
     return {"points": out_rows, "note": "per launch = one layer; slow = dense attention + masked scores (no append), "
                                         "fast = the sparse step with the fused append; Selector and compaction as in "
                                         "the slow step; bytes as in the main workload's roofline"}
+
+
+def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
+    """One decode step of a ragged batch where a few requests take the slow step and the
+    rest the fast step (ASPIRE's mixed forward; SFI's per-request boundaries): 64
+    requests with lengths log-uniform in [4096, 131072], 32 Q / 8 KV heads, retention
+    per request from {3, 12.5, 25}%, `n_slow` slow requests. Times the attention of the
+    step (appends fused) as one mixed launch and as two launches."""
+    import numpy as np
+    import torch
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    B, Hq, Hkv, D, P, S, W = 64, 32, 8, 128, 16, 64, 256
+    shape = sfi.AttnShape(Hq, Hkv, D, P)
+    g = syn.rng(seed0, 50)
+    lens = syn.log_uniform_lengths(g, B, 4096, 131072)
+    ret = g.choice([0.03, 0.125, 0.25], size=B)
+    ks = [syn.retention_budget(ret[r], int(lens[r]), S, W) for r in range(B)]
+    k_cap = max(ks)
+    table, num_pages = syn.make_page_table(g, lens + 2, P, shuffle=True)
+    pt = torch.as_tensor(table).to(dev)
+    off, cap = sfi.compact_layout(shape, S, ks, device=dev)
+    batch = sfi.DecodeBatch(pt, off, cap, torch.as_tensor(np.asarray(ks, np.int32)).to(dev), k_cap,
+                            score_stride=int(lens.max()) + 2)
+
+    def init(i, kp, vp):
+        syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 51))
+        syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 52))
+
+    (lay,) = sfi.allocate_layers(shape, 1, num_pages, batch, S, device=dev, pool_init=init)
+    q = torch.empty((B, Hq, D), dtype=torch.bfloat16, device=dev)
+    kn = torch.empty((B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vn = torch.empty_like(kn)
+    for t, tag in ((q, 53), (kn, 54), (vn, 55)):
+        syn.device_normal_bf16_(t, syn.stream_seed(seed0, tag))
+    o = torch.empty((B, Hq, D), dtype=torch.float32, device=dev)
+    seq0 = torch.as_tensor(lens.astype(np.int32)).to(dev)
+    seq1 = seq0 + 1
+    max_dense = int(lens.max()) + 2 * P
+    max_fast = S + k_cap + W + 2 * P
+    stream = torch.cuda.Stream(device=dev)
+    # every request's selection from a slow step at its length
+    ws_d = sfi.alloc_workspace(shape, B, max_dense, device=dev)
+    with torch.cuda.stream(stream):
+        kv0 = sfi.PagedKV(lay.k_pool, lay.v_pool, pt, seq0)
+        sfi.sfi_slow_dense_attn_with_scores(shape, kv0, S, W, q, o, None, lay.scores, max_tokens=max_dense,
+                                            workspace=ws_d, stream=stream)
+        sfi.sfi_select_compact(shape, kv0, lay.scores, S, W, batch.k_per_req, lay.idx, lay.compact, stream=stream)
+    torch.cuda.synchronize()
+    slow = np.sort(g.choice(B, size=n_slow, replace=False)).astype(np.int32)
+    fast = np.setdiff1d(np.arange(B, dtype=np.int32), slow)
+    slow_ids, fast_ids = torch.as_tensor(slow).to(dev), torch.as_tensor(fast).to(dev)
+    kv1 = sfi.PagedKV(lay.k_pool, lay.v_pool, pt, seq1)
+    ws_m = sfi.alloc_mixed_workspace(shape, B, max_fast, max_dense, device=dev)
+    ws_f = sfi.alloc_workspace(shape, B, max_fast, device=dev)
+    flags = sfi.SFI_ATTN_EARLY_KV_PREFETCH
+
+    def one_launch():
+        sfi.sfi_mixed_decode_attn(shape, kv1, lay.compact, S, W, q, o, fast_ids, slow_ids, scores=lay.scores,
+                                  k_new=kn, v_new=vn, max_fast_tokens=max_fast, max_dense_tokens=max_dense,
+                                  flags=flags, workspace=ws_m, stream=stream)
+
+    def two_launches():
+        sfi.sfi_fast_decode_attn(shape, kv1, lay.compact, S, W, q, o, None, k_new=kn, v_new=vn, req_ids=fast_ids,
+                                 batch=len(fast), max_tokens=max_fast, workspace=ws_f, stream=stream, flags=flags)
+        sfi.sfi_slow_dense_attn_with_scores(shape, kv1, S, W, q, o, None, lay.scores, k_new=kn, v_new=vn,
+                                            req_ids=slow_ids, batch=len(slow), max_tokens=max_dense,
+                                            workspace=ws_d, stream=stream, flags=flags)
+
+    def timed(fn):
+        with torch.cuda.stream(stream):
+            fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr, stream=stream):
+            fn()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            gr.replay()
+            e0.record(stream)
+            for _ in range(reps):
+                gr.replay()
+            e1.record(stream)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) * 1e3 / reps
+
+    t1, t2 = timed(one_launch), timed(two_launches)
+    by = 0
+    for r in range(B):
+        L = int(lens[r]) + 1
+        if r in set(slow.tolist()):
+            by += dense_bytes(1, Hq, Hkv, D, P, L, scores=True)
+        else:
+            by += fast_bytes(1, Hq, Hkv, D, P, S + ks[r] + W, W)
+        by += append_bytes(1, Hkv, D)
+    del lay
+    torch.cuda.empty_cache()
+    return {"workload": "ragged 64 requests, kv 4K-128K log-uniform, 32q/8kv heads, retention {3,12.5,25}%",
+            "slow_requests": int(n_slow), "total_kv_tokens": int(lens.sum()), "bytes": by,
+            "one_launch_us": round(t1, 2), "one_launch_GBps": round(by / (t1 * 1e-6) / 1e9, 1),
+            "one_launch_frac_of_peak": round(by / (t1 * 1e-6) / 1e9 / peak, 3),
+            "two_launch_us": round(t2, 2), "two_launch_GBps": round(by / (t2 * 1e-6) / 1e9, 1)}
 
 
 # ---------------------------------------------------------------------------

@@ -581,7 +581,18 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
 
     UnitStream u;
     if (!unit_stream(p, r, kvh, fast, split == 0, u)) return;  // uniform across the CTA and its cluster
-    const int per = (u.nb + splits - 1) / splits;
+    int per = (u.nb + splits - 1) / splits;
+    if (MODE == kModeMixed) {
+        const int chunk = fast ? p.fast_chunk_sb : p.slow_chunk_sb;
+        if (chunk > 0) {
+            // Fixed-size chunks (ragged batches): this unit uses ceil(nb / chunk) of the
+            // grid's splits for its mode; the CTAs past them have nothing to do. A unit
+            // longer than the host's bound takes bigger chunks, never more splits.
+            per = max(chunk, (u.nb + splits - 1) / splits);
+            splits = max(1, (u.nb + per - 1) / per);
+            if (split >= splits) return;
+        }
+    }
     const int sb_begin = split * per;
     const int sb_end = min(u.nb, sb_begin + per);
     const int n_my = max(0, sb_end - sb_begin);

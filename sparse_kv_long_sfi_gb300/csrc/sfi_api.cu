@@ -106,26 +106,36 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
 
 bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
 
-// Plan of a mixed launch: every CTA gets about the same number of tokens (one wave of
-// two CTAs per SM over all units), with at least four stages of work per split.
+// Plan of a mixed launch. The host knows only upper bounds of the units' lengths, so
+// each mode is cut into fixed-size chunks of sub-blocks: one wave of two CTAs per SM
+// over the upper-bound work, at most 256 sub-blocks (4096 tokens) per chunk. The grid
+// covers every unit at its upper bound; each CTA finds its unit's real chunk count on
+// the device and exits when it has no chunk (ragged batches stay balanced).
 struct MixedPlan {
     int fast_splits, slow_splits;
+    int fast_chunk_sb, slow_chunk_sb;
     int64_t units, slots;
 };
 
 MixedPlan plan_mixed(int64_t fast_units, int64_t slow_units, int32_t max_fast_tokens, int32_t max_dense_tokens,
                      int sm_count) {
-    MixedPlan m{1, 1, fast_units + slow_units, 0};
+    MixedPlan m{1, 1, 0, 0, fast_units + slow_units, 0};
     const double total = (double)fast_units * std::max(1, max_fast_tokens) +
                          (double)slow_units * std::max(1, max_dense_tokens);
     const double per_cta = std::max(1.0, total / std::max(1, sm_count * sfi::kAttnCtasPerSm));
+    const int chunk = (int)std::min(256.0, std::max(4.0 * sfi::kConsumerWarps, std::ceil(per_cta / sfi::kSubTokens)));
     auto splits_for = [&](int32_t tokens) {
         const int nb = (std::max(1, tokens) + sfi::kSubTokens - 1) / sfi::kSubTokens + 1;
-        const int want = (int)std::ceil(std::max(1, tokens) / per_cta);
-        return std::max(1, std::min({want, std::max(1, nb / (4 * sfi::kConsumerWarps)), 256}));
+        return std::max(1, std::min((nb + chunk - 1) / chunk, 4096));
     };
-    if (fast_units > 0) m.fast_splits = splits_for(max_fast_tokens);
-    if (slow_units > 0) m.slow_splits = splits_for(max_dense_tokens);
+    if (fast_units > 0) {
+        m.fast_splits = splits_for(max_fast_tokens);
+        m.fast_chunk_sb = chunk;
+    }
+    if (slow_units > 0) {
+        m.slow_splits = splits_for(max_dense_tokens);
+        m.slow_chunk_sb = chunk;
+    }
     m.slots = fast_units * m.fast_splits + slow_units * m.slow_splits;
     return m;
 }
@@ -380,6 +390,8 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.n_slow = n_slow;
     p.fast_splits = m.fast_splits;
     p.slow_splits = m.slow_splits;
+    p.fast_chunk_sb = m.fast_chunk_sb;
+    p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);  // > 1: partial states go through the workspace
     if (p.splits > 1) {
         const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim);

@@ -56,6 +56,8 @@ struct AttnParams {
     const int32_t *fast_ids;
     const int32_t *slow_ids;
     int32_t n_fast, n_slow, fast_splits, slow_splits;
+    // sub-blocks per split in mixed mode (0: the mode's units split evenly into *_splits)
+    int32_t fast_chunk_sb, slow_chunk_sb;
     int32_t early_prefetch;  // SFI_ATTN_EARLY_KV_PREFETCH: stream KV before the dependency wait
     // fused append of the current token (position L - 1), or null
     const __nv_bfloat16 *k_new;  // [B][Hkv][D]

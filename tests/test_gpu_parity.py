@@ -531,11 +531,13 @@ def test_early_prefetch_flag_gives_identical_results():
         np.testing.assert_array_equal(a, b)
 
 
-def test_mixed_launch_matches_oracle():
+@pytest.mark.parametrize("bounds", ["tight", "underestimated"])
+def test_mixed_launch_matches_oracle(bounds):
     """One launch serving fast and slow requests of one batch, the current token fused:
     fast requests against the oracle's fast step, slow ones against dense attention and
     the masked scores. The slow requests are long enough to be split, so their partial
-    states merge through the workspace."""
+    states merge through the workspace. Token bounds below the real lengths change the
+    plan, never the results."""
     sfi = _sfi()
     S, W, k = 4, 32, 64
     lens = [4000, 1200, 3000, 600, 2500, 40]
@@ -563,6 +565,8 @@ def test_mixed_launch_matches_oracle():
     lse = torch.full((prob.B, 16), float("nan"), device="cuda")
     scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
     mf, md = S + k + W + 32, int(prob.lens.max()) + 16
+    if bounds == "underestimated":
+        mf, md = 64, 1024
     ws = sfi.alloc_mixed_workspace(prob.shape, prob.B, mf, md)
     assert sfi.sfi_mixed_workspace_size(prob.shape, len(fast), len(slow), mf, md) > 0  # slow units are split
     sfi.sfi_mixed_decode_attn(prob.shape, prob.d_kv, comp, S, W, dev_bf16(q), out, dev_i32(fast), dev_i32(slow),
