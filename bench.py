@@ -793,7 +793,10 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
     kv1 = sfi.PagedKV(lay.k_pool, lay.v_pool, pt, seq1)
     ws_m = sfi.alloc_mixed_workspace(shape, B, max_fast, max_dense, device=dev)
     ws_f = sfi.alloc_workspace(shape, B, max_fast, device=dev)
+    ws_fr = sfi.alloc_ragged_workspace(shape, B, max_fast, device=dev)
+    ws_dr = sfi.alloc_ragged_workspace(shape, B, max_dense, dense=True, device=dev)
     flags = sfi.SFI_ATTN_EARLY_KV_PREFETCH
+    rflags = flags | sfi.SFI_ATTN_RAGGED
 
     def one_launch():
         sfi.sfi_mixed_decode_attn(shape, kv1, lay.compact, S, W, q, o, fast_ids, slow_ids, scores=lay.scores,
@@ -824,7 +827,26 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
         torch.cuda.synchronize()
         return e0.elapsed_time(e1) * 1e3 / reps
 
-    t1, t2 = timed(one_launch), timed(two_launches)
+    def two_launches_ragged():
+        sfi.sfi_fast_decode_attn(shape, kv1, lay.compact, S, W, q, o, None, k_new=kn, v_new=vn, req_ids=fast_ids,
+                                 batch=len(fast), max_tokens=max_fast, workspace=ws_fr, stream=stream, flags=rflags)
+        sfi.sfi_slow_dense_attn_with_scores(shape, kv1, S, W, q, o, None, lay.scores, k_new=kn, v_new=vn,
+                                            req_ids=slow_ids, batch=len(slow), max_tokens=max_dense,
+                                            workspace=ws_dr, stream=stream, flags=rflags)
+
+    # the whole batch in a fast step: the same split count for every request, or
+    # chunks sized by each request's own length (SFI_ATTN_RAGGED)
+    def fast_only_even():
+        sfi.sfi_fast_decode_attn(shape, kv1, lay.compact, S, W, q, o, None, k_new=kn, v_new=vn, max_tokens=max_fast,
+                                 workspace=ws_f, stream=stream, flags=flags)
+
+    def fast_only_ragged():
+        sfi.sfi_fast_decode_attn(shape, kv1, lay.compact, S, W, q, o, None, k_new=kn, v_new=vn, max_tokens=max_fast,
+                                 workspace=ws_fr, stream=stream, flags=rflags)
+
+    t1, t2, t2r = timed(one_launch), timed(two_launches), timed(two_launches_ragged)
+    tf_even, tf_chunk = timed(fast_only_even), timed(fast_only_ragged)
+    by_fast_only = sum(fast_bytes(1, Hq, Hkv, D, P, S + ks[r] + W, W) + append_bytes(1, Hkv, D) for r in range(B))
     by = 0
     for r in range(B):
         L = int(lens[r]) + 1
@@ -839,7 +861,12 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
             "slow_requests": int(n_slow), "total_kv_tokens": int(lens.sum()), "bytes": by,
             "one_launch_us": round(t1, 2), "one_launch_GBps": round(by / (t1 * 1e-6) / 1e9, 1),
             "one_launch_frac_of_peak": round(by / (t1 * 1e-6) / 1e9 / peak, 3),
-            "two_launch_us": round(t2, 2), "two_launch_GBps": round(by / (t2 * 1e-6) / 1e9, 1)}
+            "two_launch_us": round(t2, 2), "two_launch_GBps": round(by / (t2 * 1e-6) / 1e9, 1),
+            "two_launch_ragged_us": round(t2r, 2),
+            "all_fast_bytes": by_fast_only,
+            "all_fast_even_splits_us": round(tf_even, 2),
+            "all_fast_ragged_us": round(tf_chunk, 2),
+            "all_fast_ragged_frac_of_peak": round(by_fast_only / (tf_chunk * 1e-6) / 1e9 / peak, 3)}
 
 
 # ---------------------------------------------------------------------------

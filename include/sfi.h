@@ -91,6 +91,14 @@ typedef enum {
  * preceding kernel has finished; q, k_new and v_new are still read, and every output
  * written, only after it has finished. Without the flag nothing is read before then. */
 #define SFI_ATTN_EARLY_KV_PREFETCH 1u
+/* Flag of sfi_fast_decode_attn and sfi_slow_dense_attn_with_scores: the requests' lengths
+ * differ widely (a ragged batch). The launch is then planned in fixed-size chunks, as
+ * sfi_mixed_decode_attn does (each (request, KV head) gets splits in proportion to its
+ * real length, found on the device), instead of the same number of splits for every
+ * request; num_splits is ignored and the workspace must hold
+ * sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0) bytes for the fast call and
+ * sfi_mixed_workspace_size(shape, 0, batch, 0, max_tokens) for the dense one. */
+#define SFI_ATTN_RAGGED 2u
 
 /* Most query tokens per request in the multi-token calls (tokens x G must also be
  * <= 16: G = 2 allows 8 tokens, G = 4 four, G = 8 two). */
@@ -161,7 +169,7 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  *                is small. It affects speed only, never results.
  *   num_splits : 0 = automatic; otherwise the number of KV splits per
  *                (request, KV head) (clamped to the plan's maximum).
- *   flags      : 0 or SFI_ATTN_EARLY_KV_PREFETCH.
+ *   flags      : 0, SFI_ATTN_EARLY_KV_PREFETCH and/or SFI_ATTN_RAGGED.
  *   workspace  : at least sfi_workspace_size(shape, batch, max_tokens, num_splits)
  *                bytes of device memory, zero-filled before its first use. The
  *                kernels leave it zero-filled again when they finish without a

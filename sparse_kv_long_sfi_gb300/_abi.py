@@ -34,6 +34,7 @@ SFI_OK, SFI_ERR_INVALID_ARG, SFI_ERR_UNSUPPORTED, SFI_ERR_WORKSPACE, SFI_ERR_CUD
 SFI_DEV_BAD_PAGE, SFI_DEV_BAD_LEN, SFI_DEV_K_OVERFLOW = 1, 2, 4
 SFI_DEV_BAD_INDEX, SFI_DEV_TIMEOUT, SFI_DEV_BAD_COMPACT = 8, 16, 32
 SFI_ATTN_EARLY_KV_PREFETCH = 1
+SFI_ATTN_RAGGED = 2
 SFI_MAX_QUERY_TOKENS = 16
 
 P_SHAPE = ctypes.POINTER(sfi_attn_shape)

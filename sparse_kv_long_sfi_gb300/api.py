@@ -18,6 +18,7 @@ from . import _abi
 
 SFI_ATTN_EARLY_KV_PREFETCH = _abi.SFI_ATTN_EARLY_KV_PREFETCH
 SFI_MAX_QUERY_TOKENS = _abi.SFI_MAX_QUERY_TOKENS
+SFI_ATTN_RAGGED = _abi.SFI_ATTN_RAGGED
 
 
 class SFIError(RuntimeError):
@@ -199,6 +200,16 @@ def alloc_mixed_workspace(shape: AttnShape, batch: int, max_fast_tokens: int, ma
     fast and slow subsets."""
     n = max([256] + [sfi_mixed_workspace_size(shape, batch - ns, ns, max_fast_tokens, max_dense_tokens)
                      for ns in range(batch + 1)])
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+def alloc_ragged_workspace(shape: AttnShape, batch: int, max_tokens: int, dense: bool = False,
+                           device="cuda") -> torch.Tensor:
+    """A zero-filled workspace for sfi_fast_decode_attn (dense=False) or
+    sfi_slow_dense_attn_with_scores (dense=True) with SFI_ATTN_RAGGED, valid for every
+    batch size 1..batch."""
+    n = max([256] + [sfi_mixed_workspace_size(shape, 0, b, 0, max_tokens) if dense
+                     else sfi_mixed_workspace_size(shape, b, 0, max_tokens, 0) for b in range(1, batch + 1)])
     return torch.zeros(n, dtype=torch.uint8, device=device)
 
 

@@ -191,6 +191,41 @@ sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, 
     return SFI_OK;
 }
 
+// SFI_ATTN_RAGGED: one mode's launch planned in fixed-size chunks through the mixed
+// kernel (the requests are all fast or all slow; req_ids may be null).
+sfi_status launch_chunked(AttnParams &p, bool fast, const int32_t *req_ids, int32_t batch, int head_dim,
+                          int32_t max_tokens, const AttnMaps &maps, void *workspace, size_t workspace_bytes,
+                          void *stream) {
+    const int64_t units = (int64_t)batch * p.hkv;
+    const MixedPlan m = plan_mixed(fast ? units : 0, fast ? 0 : units, fast ? max_tokens : 0, fast ? 0 : max_tokens,
+                                   sm_count_current_device());
+    p.fast_ids = fast ? req_ids : nullptr;
+    p.slow_ids = fast ? nullptr : req_ids;
+    p.n_fast = fast ? batch : 0;
+    p.n_slow = fast ? 0 : batch;
+    p.fast_splits = m.fast_splits;
+    p.slow_splits = m.slow_splits;
+    p.fast_chunk_sb = m.fast_chunk_sb;
+    p.slow_chunk_sb = m.slow_chunk_sb;
+    p.splits = std::max(m.fast_splits, m.slow_splits);
+    p.ws_count = nullptr;
+    p.ws_ml = nullptr;
+    p.ws_part = nullptr;
+    if (p.splits > 1) {
+        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, head_dim);
+        if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
+            return SFI_ERR_WORKSPACE;
+        char *base = static_cast<char *>(workspace);
+        p.ws_count = reinterpret_cast<int32_t *>(base + l.count_off);
+        p.ws_ml = reinterpret_cast<float *>(base + l.ml_off);
+        p.ws_part = reinterpret_cast<float *>(base + l.part_off);
+    }
+    return sfi::launch_attention(head_dim, sfi::kModeMixed, true, maps, p, 0, static_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? SFI_OK
+               : SFI_ERR_CUDA;
+}
+
 sfi_status append_tokens(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new, const void *v_new,
                          int32_t tokens, const int32_t *req_ids, int32_t batch, int32_t *dev_status, void *stream) {
     sfi_status st = check_shape(shape);
@@ -284,9 +319,6 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
     p.c_capacity = compact->capacity;
     p.c_count = compact->count;
     p.c_total_rows = compact->total_rows;
-    const int64_t units = (int64_t)batch * shape->num_kv_heads;
-    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     AttnMaps maps;
     const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
     if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
@@ -294,6 +326,12 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
         !encode_rows(&maps.comp_k, compact->k, compact->total_rows, shape->head_dim) ||
         !encode_rows(&maps.comp_v, compact->v, compact->total_rows, shape->head_dim))
         return SFI_ERR_CUDA;
+    if (flags & SFI_ATTN_RAGGED)
+        return launch_chunked(p, true, req_ids, batch, shape->head_dim, max_tokens, maps, workspace, workspace_bytes,
+                              stream);
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeFast, false, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SFI_OK
@@ -322,9 +360,6 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
     p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
     p.scores = scores;
     p.score_stride = score_stride;
-    const int64_t units = (int64_t)batch * shape->num_kv_heads;
-    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     AttnMaps maps;
     const int64_t pool_rows = (int64_t)kv->num_pages * shape->num_kv_heads * shape->page_size;
     if (!encode_rows(&maps.pool_k, kv->k_pool, pool_rows, shape->head_dim) ||
@@ -332,6 +367,12 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
         return SFI_ERR_CUDA;
     maps.comp_k = maps.pool_k;  // unused in dense mode
     maps.comp_v = maps.pool_v;
+    if (flags & SFI_ATTN_RAGGED)
+        return launch_chunked(p, false, req_ids, batch, shape->head_dim, max_tokens, maps, workspace,
+                              workspace_bytes, stream);
+    const int64_t units = (int64_t)batch * shape->num_kv_heads;
+    p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeDense, scores != nullptr, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
                ? SFI_OK

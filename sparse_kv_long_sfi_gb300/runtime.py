@@ -20,8 +20,8 @@ from typing import List, Optional, Sequence
 import numpy as np
 import torch
 
-from .api import (SFI_ATTN_EARLY_KV_PREFETCH, SFI_MAX_QUERY_TOKENS, AttnShape, CompactKV, PagedKV,
-                  alloc_mixed_workspace, alloc_multi_workspace, alloc_workspace, sfi_compact_gather,
+from .api import (SFI_ATTN_EARLY_KV_PREFETCH, SFI_ATTN_RAGGED, SFI_MAX_QUERY_TOKENS, AttnShape, CompactKV,
+                  PagedKV, alloc_mixed_workspace, alloc_multi_workspace, alloc_ragged_workspace, alloc_workspace, sfi_compact_gather,
                   sfi_dense_verify_attn, sfi_fast_decode_attn, sfi_mixed_decode_attn, sfi_paged_kv_append,
                   sfi_paged_kv_append_tokens, sfi_select_compact, sfi_select_topk, sfi_slow_dense_attn_with_scores,
                   sfi_sparse_draft_attn)
@@ -125,7 +125,8 @@ class SFIDecoder:
     def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
                  max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
                  main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None,
-                 fuse_append: bool = True, single_launch_mixed: bool = True, fused_select_compact: bool = False):
+                 fuse_append: bool = True, single_launch_mixed: bool = True, fused_select_compact: bool = False,
+                 ragged: bool = False):
         self.shape, self.layers, self.batch = shape, layers, batch
         # fuse_append: the attention kernels write the current token into the pages
         # themselves (no separate append launch per layer)
@@ -140,13 +141,21 @@ class SFIDecoder:
         # decode step 687 -> 698 us at 16K, batch 16). refresh_selection, which runs on
         # an otherwise idle GPU, always uses the fused call.
         self.fused_select_compact = bool(fused_select_compact)
+        # ragged: the requests' lengths differ widely; the single-token fast and slow
+        # launches are planned in fixed-size chunks sized by each request's own length
+        # (SFI_ATTN_RAGGED) rather than with one split count for the whole batch
+        self.ragged = bool(ragged)
         self.sink, self.recent = int(sink), int(recent)
         self.max_len = int(max_len)
         B = batch.page_table.shape[0]
         self.max_fast_tokens = self.sink + int(batch.k_cap) + self.recent + 2 * shape.page_size
         self.max_dense_tokens = self.max_len + shape.page_size
-        self.ws_fast = alloc_workspace(shape, B, self.max_fast_tokens, device=device)
-        self.ws_dense = alloc_workspace(shape, B, self.max_dense_tokens, device=device)
+        if self.ragged:
+            self.ws_fast = alloc_ragged_workspace(shape, B, self.max_fast_tokens, device=device)
+            self.ws_dense = alloc_ragged_workspace(shape, B, self.max_dense_tokens, dense=True, device=device)
+        else:
+            self.ws_fast = alloc_workspace(shape, B, self.max_fast_tokens, device=device)
+            self.ws_dense = alloc_workspace(shape, B, self.max_dense_tokens, device=device)
         self.ws_mixed = (alloc_mixed_workspace(shape, B, self.max_fast_tokens, self.max_dense_tokens, device=device)
                          if single_launch_mixed else None)
         self.ws_multi = None  # multi-token workspaces, allocated on first use
@@ -163,6 +172,8 @@ class SFIDecoder:
         # the previous one finishes. The separate-append path writes the pages right
         # before the attention, so it keeps the conservative launch.
         self.attn_flags = SFI_ATTN_EARLY_KV_PREFETCH if self.fuse_append else 0
+        # flags of the single-token fast and slow launches
+        self.step_flags = self.attn_flags | (SFI_ATTN_RAGGED if self.ragged else 0)
         # Optional instrumentation: called as timer(kind, "start"|"end", stream) around
         # each attention launch (kind "slow", "fast" or "dense"), e.g. to record events.
         self.timer = None
@@ -243,7 +254,7 @@ class SFIDecoder:
                                         None if io.lse is None else io.lse[i], L.scores, k_new=kn, v_new=vn,
                                         req_ids=req_ids, batch=n, max_tokens=self.max_dense_tokens,
                                         workspace=self.ws_dense, dev_status=self.dev_status, stream=self.main,
-                                        flags=self.attn_flags)
+                                        flags=self.step_flags)
         self._mark("slow", "end")
         self.e_attn[i].record(self.main)
         self.aux.wait_event(self.e_attn[i])
@@ -279,7 +290,7 @@ class SFIDecoder:
             sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
                                  None if io.lse is None else io.lse[i], k_new=kn, v_new=vn, req_ids=req_ids,
                                  batch=n, max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
-                                 dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
+                                 dev_status=self.dev_status, stream=self.main, flags=self.step_flags)
             self._mark("fast", "end")
         self._leave()
 
@@ -306,13 +317,13 @@ class SFIDecoder:
                     sfi_fast_decode_attn(self.shape, kv, L.compact, self.sink, self.recent, io.q[i], io.out[i],
                                          lse, k_new=kn, v_new=vn, req_ids=fast_ids, batch=nf,
                                          max_tokens=self.max_fast_tokens, workspace=self.ws_fast,
-                                         dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
+                                         dev_status=self.dev_status, stream=self.main, flags=self.step_flags)
                 if ns:
                     sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
                                                     lse, L.scores, k_new=kn, v_new=vn, req_ids=slow_ids, batch=ns,
                                                     max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
                                                     dev_status=self.dev_status, stream=self.main,
-                                                    flags=self.attn_flags)
+                                                    flags=self.step_flags)
             if ns:
                 self.e_attn[i].record(self.main)
                 self.aux.wait_event(self.e_attn[i])
@@ -390,7 +401,7 @@ class SFIDecoder:
             sfi_slow_dense_attn_with_scores(self.shape, kv, self.sink, self.recent, io.q[i], io.out[i],
                                             None if io.lse is None else io.lse[i], None, k_new=kn, v_new=vn,
                                             max_tokens=self.max_dense_tokens, workspace=self.ws_dense,
-                                            dev_status=self.dev_status, stream=self.main, flags=self.attn_flags)
+                                            dev_status=self.dev_status, stream=self.main, flags=self.step_flags)
             self._mark("dense", "end")
         self._leave()
 

@@ -33,7 +33,7 @@ class Workload:
     new tokens for a few steps."""
 
     def __init__(self, seed, lens, Hq, Hkv, D, S, W, k_per_req, steps=3, layers=1, heavy_frac=0.0,
-                 k_cap=None, single_launch_mixed=True):
+                 k_cap=None, single_launch_mixed=True, ragged=False):
         import sparse_kv_long_sfi_gb300 as sfi
         self.sfi = sfi
         self.Hq, self.Hkv, self.D, self.P, self.S, self.W = Hq, Hkv, D, 16, S, W
@@ -70,7 +70,7 @@ class Workload:
         self.out = torch.zeros((layers, self.B, Hq, D), dtype=torch.float32, device=dev)
         self.lse = torch.zeros((layers, self.B, Hq), dtype=torch.float32, device=dev)
         self.dec = sfi.SFIDecoder(self.shape, self.layers, self.batch, S, W, max_len=int(self.lens0.max()) + steps + 1,
-                                  single_launch_mixed=single_launch_mixed)
+                                  single_launch_mixed=single_launch_mixed, ragged=ragged)
         self.cur = self.lens0.copy()
 
     def io(self, t):
@@ -217,11 +217,13 @@ def test_slow_step_stress_64k_zipf_ties():
     assert any(len(np.unique(sc[r, h, S:S + n])) < n for r in range(8) for h in range(8))
 
 
-@pytest.mark.parametrize("single_launch", [True, False], ids=["one-launch", "two-launch"])
-def test_ragged_mixed_batch_64_requests(single_launch):
+@pytest.mark.parametrize("single_launch,ragged", [(True, False), (False, False), (False, True)],
+                         ids=["one-launch", "two-launch", "two-launch-ragged-flag"])
+def test_ragged_mixed_batch_64_requests(single_launch, ragged):
     """64 requests, lengths log-uniform in [4096, 131072], 32 Q / 8 KV heads, shuffled pages,
     per-request retention from {3, 12.5, 25}%, boundary process p = 0.06 with a forced
-    refresh every 32 steps (the first step is slow)."""
+    refresh every 32 steps (the first step is slow). The ragged-flag variant plans the
+    separate fast and slow launches in length-sized chunks."""
     g = syn.rng(5, 0)
     lens = syn.log_uniform_lengths(g, 64, 4096, 131072) - 1
     ret = g.choice([0.03, 0.125, 0.25], size=64)
@@ -229,7 +231,7 @@ def test_ragged_mixed_batch_64_requests(single_launch):
     k0 = [syn.retention_budget(ret[r], int(lens[r]) + 1, S, W) for r in range(64)]
     k_cap = max(syn.retention_budget(ret[r], int(lens[r]) + 8, S, W) for r in range(64))
     w = Workload(5, lens, 32, 8, 128, S, W, k0, steps=4, layers=1, heavy_frac=0.02, k_cap=k_cap,
-                 single_launch_mixed=single_launch)
+                 single_launch_mixed=single_launch, ragged=ragged)
     from sparse_kv_long_sfi_gb300 import SlowFastSchedule
     sched = SlowFastSchedule(64, 32)
     b = syn.boundary_draws(syn.rng(5, 1), 4, 64, 0.3)  # a high rate so that a short run mixes modes

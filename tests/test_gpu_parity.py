@@ -39,17 +39,20 @@ def counters_zero(ws, units):
     return not ws[:4 * units].any()
 
 
-def _dense(prob, num_splits=0, scores=None, req_ids=None):
+def _dense(prob, num_splits=0, scores=None, req_ids=None, ragged=False, max_tokens=None):
     sfi = _sfi()
     B = prob.B
     out = torch.full((B, prob.Hq, prob.D), float("nan"), device="cuda")
     lse = torch.full((B, prob.Hq), float("nan"), device="cuda")
-    maxL = int(prob.lens.max()) + 16
-    ws = sfi.alloc_workspace(prob.shape, B, maxL, num_splits)
+    maxL = int(prob.lens.max()) + 16 if max_tokens is None else max_tokens
+    if ragged:
+        ws = sfi.alloc_ragged_workspace(prob.shape, B, maxL, dense=True)
+    else:
+        ws = sfi.alloc_workspace(prob.shape, B, maxL, num_splits)
     st = _status()
     sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, lse, scores,
                                         req_ids=req_ids, max_tokens=maxL, num_splits=num_splits, workspace=ws,
-                                        dev_status=st)
+                                        dev_status=st, flags=sfi.SFI_ATTN_RAGGED if ragged else 0)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert counters_zero(ws, B * prob.Hkv), "split counters must be left zeroed"
@@ -250,7 +253,8 @@ def test_append_bit_exact_and_only_the_last_slot():
 # ---------------------------------------------------------------------------
 # Fast step
 # ---------------------------------------------------------------------------
-def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids=None, heavy=0.02):
+def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids=None, heavy=0.02, ragged=False,
+               max_tokens=None):
     """Slow step + Selector + compaction on the GPU, then the fast step at the same length."""
     sfi = _sfi()
     prob = Problem(seed=seed, lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, heavy_frac=heavy).to_device()
@@ -265,11 +269,15 @@ def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids
     sfi.sfi_compact_gather(prob.shape, prob.d_kv, idx, comp.count, S, comp, dev_status=st)
     out = torch.full((prob.B, Hq, D), float("nan"), device="cuda")
     lse = torch.full((prob.B, Hq), float("nan"), device="cuda")
-    max_tokens = S + k_cap + W + 32
-    ws = sfi.alloc_workspace(prob.shape, prob.B, max_tokens, splits)
+    max_tokens = S + k_cap + W + 32 if max_tokens is None else max_tokens
+    if ragged:
+        ws = sfi.alloc_ragged_workspace(prob.shape, prob.B, max_tokens)
+    else:
+        ws = sfi.alloc_workspace(prob.shape, prob.B, max_tokens, splits)
     rid = None if req_ids is None else dev_i32(req_ids)
     sfi.sfi_fast_decode_attn(prob.shape, prob.d_kv, comp, S, W, prob.d_q, out, lse, req_ids=rid,
-                             max_tokens=max_tokens, num_splits=splits, workspace=ws, dev_status=st)
+                             max_tokens=max_tokens, num_splits=splits, workspace=ws, dev_status=st,
+                             flags=sfi.SFI_ATTN_RAGGED if ragged else 0)
     torch.cuda.synchronize()
     assert st.item() == 0
     assert counters_zero(ws, prob.B * Hkv)
@@ -293,6 +301,45 @@ def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids
 def test_fast_step_matches_oracle(splits):
     lens = [1024, 1031, 530, 36, 30, 3, 17]
     _fast_case(21 + splits, lens, 16, 8, 128, 4, 32, [64, 64, 100, 5, 5, 5, 5], 128, splits=splits)
+
+
+@pytest.mark.parametrize("bounds", ["tight", "underestimated"])
+def test_ragged_fast_step_matches_oracle(bounds):
+    """SFI_ATTN_RAGGED: the fast step planned in fixed-size chunks over requests whose
+    selected counts differ by two orders of magnitude (one request past the host's
+    bound when it is underestimated); a subset of the batch by request id."""
+    lens = [9000, 700, 30, 5200, 3, 12000]
+    k_per_req = [2000, 64, 5, 900, 5, 2500]
+    mt = None if bounds == "tight" else 800
+    _fast_case(41, lens, 16, 8, 128, 4, 32, k_per_req, 2560, req_ids=[0, 1, 2, 3, 5] if bounds == "tight" else None,
+               ragged=True, max_tokens=mt)
+
+
+@pytest.mark.parametrize("bounds", ["tight", "underestimated"])
+def test_ragged_dense_with_scores_matches_oracle(bounds):
+    """SFI_ATTN_RAGGED on the slow step: dense attention and the masked scores for a
+    batch whose lengths span 1 to 20000 tokens, by request-id subset; with an
+    underestimated bound the long requests take bigger chunks, same results."""
+    lens = [20000, 1, 700, 4100, 17, 9000]
+    prob = Problem(seed=43, lens=lens, Hq=8, Hkv=2, D=64, S=4, W=32, heavy_frac=0.03).to_device()
+    stride = int(max(lens)) + 8
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    rid = [5, 0, 1, 2, 3] if bounds == "tight" else None
+    out, lse = _dense(prob, scores=scores, req_ids=None if rid is None else dev_i32(rid), ragged=True,
+                      max_tokens=None if bounds == "tight" else 1000)
+    sc = scores.cpu().numpy()
+    for r in (range(prob.B) if rid is None else rid):
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(out[r], o_ref, f"ragged dense out r={r}")
+        assert_close(lse[r], l_ref, f"ragged dense lse r={r}")
+        L = prob.lens[r]
+        ref = prob.oracle_scores(r, stride)
+        masked = np.isneginf(ref[:, :L])
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+        err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
+        assert (err <= prob.score_bound(r, stride)[:, :L][~masked]).all()
+    if rid is not None:
+        assert np.isnan(out[4]).all() and np.isnan(sc[4]).all()
 
 
 def test_fast_step_d64_g4_and_subset():
