@@ -507,8 +507,166 @@ __host__ __device__ constexpr int cluster_slot_floats(int rows) {
 
 // Whether the partials of `splits` CTAs with `rows` query rows fit rank 0's receive region.
 template <int D>
-__host__ __device__ constexpr bool cluster_push_fits(int splits, int rows) {
-    return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= AttnTile<D>::kRecvBytes;
+__host__ __device__ constexpr bool cluster_push_fits(int splits, int rows, int recv_bytes = AttnTile<D>::kRecvBytes) {
+    return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= recv_bytes;
+}
+
+// Split merge of one unit's partial states (m, l, unnormalised o per query row), run by
+// the consumer threads (threadIdx.x < 128) of each of the unit's CTAs once this CTA's
+// partial is complete: in cp_o [rows][D], cp_m, cp_l (shared memory) when the unit's
+// splits form a cluster, in workspace slot (slot0 + split) otherwise. recv is the
+// receive region (recv_bytes) where the other CTAs of a cluster push their partials.
+template <int D, int kRows, bool CLUSTER, typename OutRow>
+__device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, int recv_bytes, uint64_t *merge_bar,
+                                             int *s_last, float *cp_o, float *cp_m, float *cp_l, int rows, int splits,
+                                             int split, int64_t unit, int64_t slot0, bool ok, OutRow out_row) {
+    const int ctid = threadIdx.x;  // 0 .. 127
+    if (CLUSTER && cluster_push_fits<D>(splits, rows, recv_bytes)) {
+        // ---- split merge inside the cluster: the other CTAs push their partials into
+        // rank 0's receive region (distributed shared-memory stores), rank 0 merges them
+        // from its own shared memory ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        const int slot_f = cluster_slot_floats<D>(rows);
+        if (split != 0) {
+            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * slot_f) * 4u;
+            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
+                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
+            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
+                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
+                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
+            }
+            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // release: my stores above
+            // Rank 0 signals once every push has landed; only then may this CTA exit.
+            if (ctid == 0 && !mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+        const bool got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
+        if (got && ctid >= 1 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
+        if (!got) {
+            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+        if (!ok) return;
+        for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+            const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+            float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+            float2 os[kMaxClusterSplits];
+            ms[0] = cp_m[row];
+            ls[0] = cp_l[row];
+            os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
+#pragma unroll
+            for (int s = 1; s < kMaxClusterSplits; ++s) {
+                if (s < splits) {
+                    const float *src = recv + (s - 1) * slot_f;
+                    ms[s] = src[rows * D + row];
+                    ls[s] = src[rows * D + rows + row];
+                    os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
+                }
+            }
+            float M = -INFINITY;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s)
+                if (s < splits) M = fmaxf(M, ms[s]);
+            float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s < splits && ls[s] > 0.f) {
+                    const float f = fast_exp2(ms[s] - M);
+                    ax += os[s].x * f;
+                    ay += os[s].y * f;
+                    lsum += ls[s] * f;
+                }
+            }
+            *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
+            if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+        }
+        return;
+    }
+
+    if (CLUSTER) {
+        // ---- split merge inside the cluster, pulled by rank 0 from the other CTAs'
+        // shared memory (when their partials do not fit rank 0's receive region) ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        if (split != 0) {
+            if (ctid == 0) {
+                mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // "my partial is ready"
+                // Stay alive (shared memory readable) until rank 0 has read it.
+                if (!mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            }
+            return;
+        }
+        if (ctid == 0) *s_last = mbar_wait_cluster_bounded(merge_bar, 0) ? 1 : 0;
+        consumer_bar_sync();
+        if (*s_last && ok) {
+            // Each thread merges pairs of outputs. All loads from the peers' shared
+            // memory are issued before any is used, so their latencies overlap.
+            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+                float2 os[kMaxClusterSplits];
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < splits) {
+                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
+                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
+                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
+                    }
+                }
+                float M = -INFINITY;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s)
+                    if (s < splits) M = fmaxf(M, ms[s]);
+                float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < splits && ls[s] > 0.f) {
+                        const float f = fast_exp2(ms[s] - M);
+                        ax += os[s].x * f;
+                        ay += os[s].y * f;
+                        lsum += ls[s] * f;
+                    }
+                }
+                *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
+                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+            }
+        }
+        if (!*s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
+        consumer_bar_sync();  // every read of the peers' shared memory is done
+        if (ctid > 0 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
+        return;
+    }
+
+    // ---- split merge by the last CTA of this unit, through the global workspace ----
+    if (!ok) return;
+    __threadfence();
+    consumer_bar_sync();
+    if (ctid == 0) {
+        const int prev = atomicAdd(&p.ws_count[unit], 1);
+        *s_last = (prev == splits - 1);
+    }
+    consumer_bar_sync();
+    if (!*s_last) return;
+    __threadfence();
+    for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
+        const int row = e / D, d = e - (e / D) * D;
+        float M = -INFINITY;
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[((slot0 + s) * kRows + row) * 2]));
+        float acc = 0.f, lsum = 0.f;
+#pragma unroll 8
+        for (int s = 0; s < splits; ++s) {
+            const int64_t slot = (slot0 + s) * kRows + row;
+            const float ls = __ldcg(&p.ws_ml[slot * 2 + 1]);
+            if (ls > 0.f) {
+                const float f = fast_exp2(__ldcg(&p.ws_ml[slot * 2]) - M);
+                acc += __ldcg(&p.ws_part[slot * D + d]) * f;
+                lsum += ls * f;
+            }
+        }
+        p.out[out_row(row) * D + d] = acc / lsum;
+        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+    }
+    if (ctid == 0) p.ws_count[unit] = 0;  // leave the workspace zeroed for the next launch
 }
 
 // MQ: p.tokens query tokens per request (rows = tokens x G <= 16), no fused append.
@@ -904,154 +1062,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
     }
     if (splits == 1) return;
-
-    if (CLUSTER && cluster_push_fits<D>(splits, rows)) {
-        // ---- split merge inside the cluster: the other CTAs push their partials into
-        // rank 0's receive region (distributed shared-memory stores), rank 0 merges them
-        // from its own shared memory ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        const int slot_f = cluster_slot_floats<D>(rows);
-        float *recv = reinterpret_cast<float *>(smem + T::kRecvOffset);  // [splits - 1][slot_f]
-        if (split != 0) {
-            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * slot_f) * 4u;
-            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
-                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
-            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
-                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
-                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
-            }
-            mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), 0));  // release: my stores above
-            // Rank 0 signals once every push has landed; only then may this CTA exit.
-            if (ctid == 0 && !mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
-        const bool got = mbar_wait_cluster_bounded(&merge_bar, 0);  // acquire: the peers' pushes
-        if (got && ctid >= 1 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
-        if (!got) {
-            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
-        if (!ok) return;
-        for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-            const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-            float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-            float2 os[kMaxClusterSplits];
-            ms[0] = cp_m[row];
-            ls[0] = cp_l[row];
-            os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
-#pragma unroll
-            for (int s = 1; s < kMaxClusterSplits; ++s) {
-                if (s < splits) {
-                    const float *src = recv + (s - 1) * slot_f;
-                    ms[s] = src[rows * D + row];
-                    ls[s] = src[rows * D + rows + row];
-                    os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
-                }
-            }
-            float M = -INFINITY;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s)
-                if (s < splits) M = fmaxf(M, ms[s]);
-            float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-                if (s < splits && ls[s] > 0.f) {
-                    const float f = fast_exp2(ms[s] - M);
-                    ax += os[s].x * f;
-                    ay += os[s].y * f;
-                    lsum += ls[s] * f;
-                }
-            }
-            *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
-            if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-        }
-        return;
-    }
-
-    if (CLUSTER) {
-        // ---- split merge inside the cluster, pulled by rank 0 from the other CTAs'
-        // shared memory (when their partials do not fit rank 0's receive region) ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        if (split != 0) {
-            if (ctid == 0) {
-                mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), 0));  // "my partial is ready"
-                // Stay alive (shared memory readable) until rank 0 has read it.
-                if (!mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
-            }
-            return;
-        }
-        if (ctid == 0) s_last = mbar_wait_cluster_bounded(&merge_bar, 0) ? 1 : 0;
-        consumer_bar_sync();
-        if (s_last && ok) {
-            // Each thread merges pairs of outputs. All loads from the peers' shared
-            // memory are issued before any is used, so their latencies overlap.
-            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-                float2 os[kMaxClusterSplits];
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < splits) {
-                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
-                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
-                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
-                    }
-                }
-                float M = -INFINITY;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s)
-                    if (s < splits) M = fmaxf(M, ms[s]);
-                float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < splits && ls[s] > 0.f) {
-                        const float f = fast_exp2(ms[s] - M);
-                        ax += os[s].x * f;
-                        ay += os[s].y * f;
-                        lsum += ls[s] * f;
-                    }
-                }
-                *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
-                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-            }
-        }
-        if (!s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
-        consumer_bar_sync();  // every read of the peers' shared memory is done
-        if (ctid > 0 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(&merge_bar), ctid));
-        return;
-    }
-
-    // ---- split merge by the last CTA of this unit, through the global workspace ----
-    if (!ok) return;
-    __threadfence();
-    consumer_bar_sync();
-    if (ctid == 0) {
-        const int prev = atomicAdd(&p.ws_count[unit], 1);
-        s_last = (prev == splits - 1);
-    }
-    consumer_bar_sync();
-    if (!s_last) return;
-    __threadfence();
-    for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
-        const int row = e / D, d = e - (e / D) * D;
-        float M = -INFINITY;
-#pragma unroll 8
-        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[((slot0 + s) * kRows + row) * 2]));
-        float acc = 0.f, lsum = 0.f;
-#pragma unroll 8
-        for (int s = 0; s < splits; ++s) {
-            const int64_t slot = (slot0 + s) * kRows + row;
-            const float ls = __ldcg(&p.ws_ml[slot * 2 + 1]);
-            if (ls > 0.f) {
-                const float f = fast_exp2(__ldcg(&p.ws_ml[slot * 2]) - M);
-                acc += __ldcg(&p.ws_part[slot * D + d]) * f;
-                lsum += ls * f;
-            }
-        }
-        p.out[out_row(row) * D + d] = acc / lsum;
-        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-    }
-    if (ctid == 0) p.ws_count[unit] = 0;  // leave the workspace zeroed for the next launch
+    merge_splits<D, kRows, CLUSTER>(p, reinterpret_cast<float *>(smem + T::kRecvOffset), T::kRecvBytes, &merge_bar,
+                                     &s_last, cp_o, cp_m, cp_l, rows, splits, split, unit, slot0, ok, out_row);
 }
 
 template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>
