@@ -375,6 +375,57 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
         vm0 = (u0 ? 0x0000ffffu : 0u) | (u1 ? 0xffff0000u : 0u);
         vm1 = (u2 ? 0x0000ffffu : 0u) | (u3 ? 0xffff0000u : 0u);
     }
+    if (p.rows <= kMaxGroup) {
+        // At most 8 query rows: rows g + 8 of the tile are padding, so (as in the one-token
+        // consume_sub_block) they carry the low bf16 half of row g's probabilities and one
+        // mma per n-tile computes both halves; the caller adds o[.][0..1] and o[.][2..3].
+        float ma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+        ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+        const float na = fmaxf(m_run[0], ma);
+        const float ba = (na == -INFINITY) ? 0.f : na;
+        const float alpha = fast_exp2(m_run[0] - ba);
+        float pa[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) pa[i] = fast_exp2(xa[i] - ba);
+        l_run[0] = l_run[0] * alpha + ((pa[0] + pa[1]) + (pa[2] + pa[3]));
+        m_run[0] = na;
+        if (__any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll
+            for (int nt = 0; nt < T::kNTiles; ++nt) {
+                o[nt][0] *= alpha;
+                o[nt][1] *= alpha;
+                o[nt][2] *= alpha;
+                o[nt][3] *= alpha;
+            }
+        }
+        const __nv_bfloat162 h01 = __floats2bfloat162_rn(pa[0], pa[1]);
+        const __nv_bfloat162 h23 = __floats2bfloat162_rn(pa[2], pa[3]);
+        const __nv_bfloat162 l01 = __floats2bfloat162_rn(pa[0] - __low2float(h01), pa[1] - __high2float(h01));
+        const __nv_bfloat162 l23 = __floats2bfloat162_rn(pa[2] - __low2float(h23), pa[3] - __high2float(h23));
+        const uint32_t a0 = *reinterpret_cast<const uint32_t *>(&h01);
+        const uint32_t a1 = *reinterpret_cast<const uint32_t *>(&l01);
+        const uint32_t a2 = *reinterpret_cast<const uint32_t *>(&h23);
+        const uint32_t a3 = *reinterpret_cast<const uint32_t *>(&l23);
+        const int tok = ((mi & 1) << 3) + r8;
+        const uint32_t row_addr = vaddr + tok * 128;
+#pragma unroll
+        for (int j = 0; j < T::kNTiles / 2; ++j) {
+            const int box = j >> 2;
+            const int chunk = ((j & 3) << 1) + (mi >> 1);
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_trans(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
+            if (!full) {
+                b0 &= vm0;
+                b1 &= vm1;
+                b2 &= vm0;
+                b3 &= vm1;
+            }
+            mma_bf16_16816(o[2 * j], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(o[2 * j + 1], a0, a1, a2, a3, b2, b3);
+        }
+        return;
+    }
     float ma = fmaxf(fmaxf(xa[0], xa[1]), fmaxf(xa[2], xa[3]));
     float mb = fmaxf(fmaxf(xb[0], xb[1]), fmaxf(xb[2], xb[3]));
     ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
@@ -394,12 +445,14 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
     l_run[1] = l_run[1] * alpha_b + ((pb[0] + pb[1]) + (pb[2] + pb[3]));
     m_run[0] = na;
     m_run[1] = nb;
+    if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f)) {  // some row's running max moved
 #pragma unroll
-    for (int nt = 0; nt < T::kNTiles; ++nt) {
-        o[nt][0] *= alpha_a;
-        o[nt][1] *= alpha_a;
-        o[nt][2] *= alpha_b;
-        o[nt][3] *= alpha_b;
+        for (int nt = 0; nt < T::kNTiles; ++nt) {
+            o[nt][0] *= alpha_a;
+            o[nt][1] *= alpha_a;
+            o[nt][2] *= alpha_b;
+            o[nt][3] *= alpha_b;
+        }
     }
     // P as two bf16 terms (hi + lo), rows g and g + 8 in the A fragment's halves.
     uint32_t ph[4], pl[4];
@@ -817,7 +870,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     break;
                 }
             }
-            const int page = __shfl_sync(0xffffffffu, cur, ((st & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
+            // A stage of compact sub-blocks needs no page id; skipping the shuffle there keeps
+            // the page-table loads off the path of the first TMA copies.
+            const bool paged = sb_begin + (st + 1) * kConsumerWarps > u.nb1;  // warp-uniform
+            const int page =
+                paged ? __shfl_sync(0xffffffffu, cur, ((st & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1))) : -1;
             if (lane < kConsumerWarps) {
                 const int sb = sb_begin + st * kConsumerWarps + lane;
                 int lo = 0, hi = 0, pos0 = 0;
@@ -995,13 +1052,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     float *cp_o = sm_l + kConsumerWarps * kRows;                    // [kRows][D]  this CTA's partial (cluster merge)
     float *cp_m = cp_o + kRows * D;                                 // [kRows]
     float *cp_l = cp_m + kRows;                                     // [kRows]
+    // up to 8 query rows: rows g + 8 hold the P_lo V half of row g
+    const bool packed = !MQ || p.rows <= kMaxGroup;
     if (ok) {
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) {
-            // one token: rows g + 8 hold the P_lo V half of row g
-            float2 v = MQ ? make_float2(o[nt][0], o[nt][1]) : make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]);
+            float2 v = packed ? make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3]) : make_float2(o[nt][0], o[nt][1]);
             *reinterpret_cast<float2 *>(&sm_o[(warp * kRows + g) * MS + nt * 8 + 2 * t]) = v;
-            if (MQ) {
+            if (!packed) {
                 float2 w = make_float2(o[nt][2], o[nt][3]);
                 *reinterpret_cast<float2 *>(&sm_o[(warp * kRows + g + 8) * MS + nt * 8 + 2 * t]) = w;
             }
@@ -1009,7 +1067,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         if (t == 0) {
             sm_m[warp * kRows + g] = m_run[0];
             sm_l[warp * kRows + g] = l_run[0];
-            if (MQ) {
+            if (!packed) {
                 sm_m[warp * kRows + g + 8] = m_run[1];
                 sm_l[warp * kRows + g + 8] = l_run[1];
             }
