@@ -44,6 +44,9 @@ SWEEP_N = [1, 4, 8, 16, 24, 32, 48, 63, 64]
 TABLE1 = {1: 10.67, 4: 9.56, 8: 7.15, 16: 3.96, 24: 2.75, 32: 2.10, 48: 1.43, 63: 1.10, 64: 1.00}
 
 
+SECTIONS = ("retention", "speculative", "other", "ragged")
+
+
 def parse_args():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -55,7 +58,15 @@ def parse_args():
     ap.add_argument("--layers", type=int, default=WL["layers"])
     ap.add_argument("--batch", type=int, default=WL["batch"])
     ap.add_argument("--kv-len", type=int, default=WL["kv_len"])
-    return ap.parse_args()
+    ap.add_argument("--sections", default=",".join(SECTIONS),
+                    help="comma list of the sections after the headline: " + ", ".join(SECTIONS))
+    ap.add_argument("--ragged-requests", type=int, default=64, help="requests of the ragged mixed-step section")
+    args = ap.parse_args()
+    args.sections = [x for x in args.sections.split(",") if x]
+    unknown = set(args.sections) - set(SECTIONS)
+    if unknown:
+        ap.error(f"unknown sections {sorted(unknown)}")
+    return args
 
 
 # ---------------------------------------------------------------------------
@@ -399,13 +410,17 @@ def run_gpu(args, ranks: Ranks):
     result["e2e"] = e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks)
 
     # ---- retention sweep vs dense (Table 1) ----
-    if not args.no_sweep:
+    sections = [] if args.no_sweep else args.sections
+    if "retention" in sections:
         result["retention_sweep"] = retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps,
                                                     NL, B, Hq, Hkv, D, P, L0, S, dev, peak)
+    if "speculative" in sections:
         result["speculative_sweep"] = speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv,
                                                         D, P, L0, S, W, k_main, dev, peak, seed0)
+    if "other" in sections:
         result["other_workloads"] = other_workloads(dev, peak, seed0)
-        result["ragged_mixed_step"] = ragged_mixed_step(dev, peak, seed0)
+    if "ragged" in sections:
+        result["ragged_mixed_step"] = ragged_mixed_step(dev, peak, seed0, B=args.ragged_requests)
     return result
 
 
@@ -739,9 +754,9 @@ def other_workloads(dev, peak, seed0, layers=4, reps=10):
                                         "the slow step; bytes as in the main workload's roofline"}
 
 
-def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
+def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5, B=64):
     """One decode step of a ragged batch where a few requests take the slow step and the
-    rest the fast step (ASPIRE's mixed forward; SFI's per-request boundaries): 64
+    rest the fast step (ASPIRE's mixed forward; SFI's per-request boundaries): B (64)
     requests with lengths log-uniform in [4096, 131072], 32 Q / 8 KV heads, retention
     per request from {3, 12.5, 25}%, `n_slow` slow requests. Times the attention of the
     step (appends fused) as one mixed launch and as two launches."""
@@ -750,7 +765,8 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
     import sfi_synth as syn
     import sparse_kv_long_sfi_gb300 as sfi
 
-    B, Hq, Hkv, D, P, S, W = 64, 32, 8, 128, 16, 64, 256
+    Hq, Hkv, D, P, S, W = 32, 8, 128, 16, 64, 256
+    n_slow = min(n_slow, B)
     shape = sfi.AttnShape(Hq, Hkv, D, P)
     g = syn.rng(seed0, 50)
     lens = syn.log_uniform_lengths(g, B, 4096, 131072)
@@ -857,7 +873,7 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5):
         by += append_bytes(1, Hkv, D)
     del lay
     torch.cuda.empty_cache()
-    return {"workload": "ragged 64 requests, kv 4K-128K log-uniform, 32q/8kv heads, retention {3,12.5,25}%",
+    return {"workload": f"ragged {B} requests, kv 4K-128K log-uniform, 32q/8kv heads, retention {{3,12.5,25}}%",
             "slow_requests": int(n_slow), "total_kv_tokens": int(lens.sum()), "bytes": by,
             "one_launch_us": round(t1, 2), "one_launch_GBps": round(by / (t1 * 1e-6) / 1e9, 1),
             "one_launch_frac_of_peak": round(by / (t1 * 1e-6) / 1e9 / peak, 3),

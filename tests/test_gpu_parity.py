@@ -656,10 +656,12 @@ def test_mixed_launch_matches_oracle(bounds):
     (64, 8, 2, [1024, 777, 36, 3, 40], [64, 100, 64, 8, 64], 128),          # L < S, L < S + W, keff < k
     (128, 16, 8, [300, 21000, 530], [400, 1500, 10], 1600),                  # keff == |C|; |C| > 16384 (rounds)
     (128, 32, 8, [4096, 2048], [256, 128], 256),
+    (128, 16, 8, [700 + 37 * i for i in range(16)], [8 * i for i in range(16)], 128),  # 128 units: one launch
 ])
 def test_select_compact_bit_exact(D, Hq, Hkv, lens, k_per_req, k_cap):
-    """The fused Selector + compaction equals the oracle Selector (on the GPU-written scores)
-    followed by the oracle compaction, byte for byte, and leaves the same counts."""
+    """Selector + compaction in one call (one fused launch when the units fill the GPU and k is
+    small, else the two kernels) equals the oracle Selector (on the GPU-written scores) followed
+    by the oracle compaction, byte for byte, and leaves the same counts."""
     sfi = _sfi()
     S, W = 4, 32
     prob = Problem(seed=700 + D + len(lens), lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, heavy_frac=0.03).to_device()
@@ -691,33 +693,40 @@ def test_select_compact_bit_exact(D, Hq, Hkv, lens, k_per_req, k_cap):
                 np.testing.assert_array_equal(cv[base + lo:base + hi], rv[kvh, lo:hi], err_msg=f"V r={r} kv={kvh}")
 
 
-def test_select_compact_subset_and_bad_capacity():
+@pytest.mark.parametrize("B,Hkv", [(3, 2), (16, 8)], ids=["two-kernels", "one-launch"])
+def test_select_compact_subset_and_bad_capacity(B, Hkv):
     """A request subset is handled alone; a request whose capacity is below S + k_eff keeps its
-    selection, is not packed, and is reported."""
+    selection, is not packed, and is reported (both forms of the call)."""
     sfi = _sfi()
     S, W = 4, 32
-    prob = Problem(seed=720, lens=[800, 900, 1000], Hq=8, Hkv=2, D=128, S=S, W=W).to_device()
+    lens = [800 + 100 * (i % 3) for i in range(B)]
+    prob = Problem(seed=720 + B, lens=lens, Hq=2 * Hkv, Hkv=Hkv, D=128, S=S, W=W).to_device()
     stride = 1008
-    scores = torch.full((prob.B, 2, stride), float("nan"), device="cuda")
+    scores = torch.full((prob.B, Hkv, stride), float("nan"), device="cuda")
     _dense(prob, scores=scores)
-    comp = _compact_buffers(prob, [64, 8, 64])  # request 1: capacity S + 8 < S + 64
-    idx = torch.full((prob.B, 2, 64), -7, dtype=torch.int32, device="cuda")
+    comp = _compact_buffers(prob, [8 if r == 1 else 64 for r in range(B)])  # request 1: capacity S + 8 < S + 64
+    idx = torch.full((prob.B, Hkv, 64), -7, dtype=torch.int32, device="cuda")
     st = _status()
-    sfi.sfi_select_compact(prob.shape, prob.d_kv, scores, S, W, dev_i32([64, 64, 64]), idx, comp,
-                           req_ids=dev_i32([2, 1]), dev_status=st)
+    subset = [2, 1] if B == 3 else list(range(B - 1, 0, -1))  # every request but 0
+    sfi.sfi_select_compact(prob.shape, prob.d_kv, scores, S, W, dev_i32([64] * B), idx, comp,
+                           req_ids=dev_i32(subset), dev_status=st)
     torch.cuda.synchronize()
     assert st.item() == 4  # SFI_DEV_K_OVERFLOW for request 1
     sc = scores.cpu().numpy()
-    ref_idx, ref_count = run_oracle_selection(prob, sc, [64, 64, 64], 64)
+    ref_idx, ref_count = run_oracle_selection(prob, sc, [64] * B, 64)
     got_idx = idx.cpu().numpy()
-    for r in (1, 2):
+    for r in subset:
         np.testing.assert_array_equal(got_idx[r], ref_idx[r])
     assert (got_idx[0] == -7).all()
     ck = host_bf16(comp.k)
     off, cap = comp.row_offset.cpu().numpy(), comp.capacity.cpu().numpy()
-    rk, _ = oracle_compact_request(prob, 2, ref_idx[2], 64, cap[2])
-    for kvh in range(2):
-        base = off[2] + kvh * cap[2]
-        np.testing.assert_array_equal(ck[base:base + S + 64], rk[kvh, :S + 64])
+    for r in subset:
+        if r == 1:
+            continue
+        rk, _ = oracle_compact_request(prob, r, ref_idx[r], 64, cap[r])
+        for kvh in range(Hkv):
+            base = off[r] + kvh * cap[r]
+            np.testing.assert_array_equal(ck[base:base + S + 64], rk[kvh, :S + 64])
+    for kvh in range(Hkv):
         base1 = off[1] + kvh * cap[1]
         assert not ck[base1:base1 + cap[1]].any(), "the request with too small a capacity is not packed"
