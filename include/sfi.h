@@ -356,11 +356,8 @@ SFI_API sfi_status sfi_compact_gather(const sfi_attn_shape *shape, const sfi_pag
 /*
  * sfi_select_compact - sfi_select_topk followed by sfi_compact_gather in one call
  * (Figure 2 caption: the Selector refreshes the selected memory; Figure 3: cache
- * reorganisation into the contiguous compact buffer). When the call's (request, KV
- * head) units number at least 3/4 of the SMs and k_cap <= 1024, one launch does both
- * (the CTA that selects a unit also packs its sink and selected rows); otherwise the
- * two kernels run in sequence, the compaction spread over every SM. The results are
- * those of the two calls in sequence with count = count_out.
+ * reorganisation into the contiguous compact buffer): the two kernels are launched in
+ * sequence on the stream, with count = count_out.
  *   scores, score_stride, k_per_req, k_cap, idx_out : as for sfi_select_topk
  *   count_out : int32 [B], normally the same array as compact->count
  *   kv->seq_lens gives L (as for both calls)

@@ -92,7 +92,7 @@ __device__ __forceinline__ int compact_rows(const CopyParams &p, int r, uint32_t
 // counts (an exclusive prefix over the launch's requests, in shared memory) and walks
 // it with a grid stride, so the work follows the rows actually selected, not k_cap.
 template <int D>
-__global__ void __launch_bounds__(kCopyThreads, 4) compact_gather_kernel(const CopyParams p, int b_begin, int nb) {
+__global__ void __launch_bounds__(kCopyThreads, 3) compact_gather_kernel(const CopyParams p, int b_begin, int nb) {
     constexpr int kChunks = D / 8;
     constexpr int kThreadsPerRow = 2 * kChunks;  // K chunks then V chunks
     constexpr int kRowsPerIter = kCopyThreads / kThreadsPerRow;
@@ -160,6 +160,7 @@ __global__ void __launch_bounds__(kCopyThreads, 4) compact_gather_kernel(const C
     const bool is_v = cc >= kChunks;
     const int chunk = is_v ? cc - kChunks : cc;
     const __nv_bfloat16 *pool = is_v ? p.v_pool_src : p.k_pool_src;
+    uint32_t werr = 0;
     for (int work = blockIdx.x; work < total; work += gridDim.x) {
         // request entry owning this chunk: the last b with s_prefix[b] <= work (an entry
         // without chunks shares its prefix with the next entry, so it is never the last)
@@ -184,37 +185,43 @@ __global__ void __launch_bounds__(kCopyThreads, 4) compact_gather_kernel(const C
         const int32_t *sel = p.idx + ((int64_t)r * p.hkv + kvh) * p.k_cap;
         const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
 
-        int4 vals[kIters];
-        int dst_row[kIters];
+        // Three batched phases (all indices, then all page ids, then all rows), so the
+        // kIters rows' dependent loads overlap instead of running one row after another;
+        // errors are collected in a register and reported once.
+        int pos[kIters];
+        uint32_t take = 0;  // bit it: row it of this thread is copied
 #pragma unroll
         for (int it = 0; it < kIters; ++it) {
             const int i = row0 + it * kRowsPerIter + sub;
-            int pos = -1;
-            if (i < ns) {
-                pos = i;
-            } else if (i >= p.sink && i < p.sink + cnt) {
-                pos = sel[i - p.sink];
-                if (pos < 0 || pos >= L) {
-                    report(p.dev_status, SFI_DEV_BAD_INDEX);
-                    pos = -1;
-                }
+            const bool t = i < ns || (i >= p.sink && i < p.sink + cnt);
+            take |= (t ? 1u : 0u) << it;
+            pos[it] = i < ns ? i : (t ? __ldg(&sel[i - p.sink]) : 0);
+        }
+        int page[kIters];
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+            if (((take >> it) & 1u) && (pos[it] < 0 || pos[it] >= L)) {
+                werr |= SFI_DEV_BAD_INDEX;
+                take &= ~(1u << it);
             }
-            dst_row[it] = -1;
-            if (pos >= 0) {
-                const int page = ptab[pos / kSubTokens];
-                if (page < 0 || page >= p.num_pages) {
-                    report(p.dev_status, SFI_DEV_BAD_PAGE);
-                } else {
-                    vals[it] = ld_nc_v4(pool + (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D +
-                                        chunk * 8);
-                    dst_row[it] = i;
-                }
+            page[it] = ((take >> it) & 1u) ? __ldg(&ptab[pos[it] / kSubTokens]) : 0;
+        }
+        int4 vals[kIters];
+#pragma unroll
+        for (int it = 0; it < kIters; ++it) {
+            if (((take >> it) & 1u) && (page[it] < 0 || page[it] >= p.num_pages)) {
+                werr |= SFI_DEV_BAD_PAGE;
+                take &= ~(1u << it);
             }
+            if ((take >> it) & 1u)
+                vals[it] = ld_nc_v4(pool + (((int64_t)page[it] * p.hkv + kvh) * kSubTokens + pos[it] % kSubTokens) * D +
+                                    chunk * 8);
         }
 #pragma unroll
         for (int it = 0; it < kIters; ++it)
-            if (dst_row[it] >= 0) st_v4(dst_base + (int64_t)dst_row[it] * D, vals[it]);
+            if ((take >> it) & 1u) st_v4(dst_base + (int64_t)(row0 + it * kRowsPerIter + sub) * D, vals[it]);
     }
+    if (werr) report(p.dev_status, werr);
 }
 
 cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t stream) {

@@ -79,65 +79,7 @@ __device__ __forceinline__ int4 ld_nc_v4_sel(const void *ptr) {
     return v;
 }
 
-// Compaction of one (request, KV head) by the CTA that selected it: compact rows
-// [0, ns) <- positions [0, ns) (the sink, ns = min(S, L)) and rows [S, S + keff) <-
-// the selected positions (sel[t], or S + t when sel is null: everything selected), K
-// and V, copied bit for bit. 2 * D / 8 threads per row, 16 bytes each; kGatherUnroll
-// rows per thread in flight.
-constexpr int kGatherUnroll = 4;
-template <int D>
-__device__ __forceinline__ void gather_compact(const CopyParams &c, int r, int kvh, int L, int keff, const int32_t *sel,
-                                               int tid) {
-    constexpr int kChunks = D / 8;
-    constexpr int kThreadsPerRow = 2 * kChunks;
-    constexpr int kRowsPerPass = kTopkThreads / kThreadsPerRow;
-    const int cap = c.c_capacity[r];
-    const int64_t off = c.c_row_offset[r];
-    if (c.sink + keff > cap) {
-        if (tid == 0) report(c.dev_status, SFI_DEV_K_OVERFLOW);
-        return;
-    }
-    if (off < 0 || off + (int64_t)c.hkv * cap > c.c_total_rows) {
-        if (tid == 0) report(c.dev_status, SFI_DEV_BAD_COMPACT);
-        return;
-    }
-    const int ns = min(c.sink, L);
-    const int rows = ns + keff;
-    const int sub = tid / kThreadsPerRow, cc = tid - sub * kThreadsPerRow;
-    const bool is_v = cc >= kChunks;
-    const int chunk = is_v ? cc - kChunks : cc;
-    const __nv_bfloat16 *pool = is_v ? c.v_pool_src : c.k_pool_src;
-    __nv_bfloat16 *dst_base = (is_v ? c.cv : c.ck) + (off + (int64_t)kvh * cap) * D + chunk * 8;
-    const int32_t *ptab = c.page_table + (int64_t)r * c.max_pages;
-    for (int base = 0; base < rows; base += kRowsPerPass * kGatherUnroll) {
-        int4 vals[kGatherUnroll];
-        int crow[kGatherUnroll];
-#pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u) {
-            const int i = base + u * kRowsPerPass + sub;
-            crow[u] = -1;
-            if (i < rows) {
-                const int pos = i < ns ? i : (sel ? sel[i - ns] : c.sink + (i - ns));
-                const int page = ptab[pos / kSubTokens];
-                if (page < 0 || page >= c.num_pages) {
-                    report(c.dev_status, SFI_DEV_BAD_PAGE);
-                } else {
-                    vals[u] = ld_nc_v4_sel(pool + (((int64_t)page * c.hkv + kvh) * kSubTokens + pos % kSubTokens) * D +
-                                           chunk * 8);
-                    crow[u] = i < ns ? i : c.sink + (i - ns);
-                }
-            }
-        }
-#pragma unroll
-        for (int u = 0; u < kGatherUnroll; ++u)
-            if (crow[u] >= 0) *reinterpret_cast<int4 *>(dst_base + (int64_t)crow[u] * D) = vals[u];
-    }
-}
-
-// D = 0: the Selector alone; D = 64 or 128: the Selector followed by the compaction of
-// its (request, KV head) (parameters in c).
-template <int D>
-__global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p, const CopyParams c) {
+__global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p) {
     extern __shared__ __align__(16) float s_keys[];
     __shared__ __align__(8) uint64_t s_bar[2];
     __shared__ uint32_t hist[256];
@@ -161,15 +103,11 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     }
     const int keff = min(k, n);
     if (kvh == 0 && tid == 0) p.count_out[r] = keff;
-    if (keff == 0) {
-        if constexpr (D > 0) gather_compact<D>(c, r, kvh, L, 0, nullptr, tid);
-        return;
-    }
+    if (keff == 0) return;
     int32_t *out = p.idx_out + ((int64_t)r * p.hkv + kvh) * p.k_cap;
     const float *row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride + p.sink;
     if (keff == n) {  // everything is selected
         for (int i = tid; i < n; i += kTopkThreads) out[i] = p.sink + i;
-        if constexpr (D > 0) gather_compact<D>(c, r, kvh, L, keff, nullptr, tid);
         return;
     }
 
@@ -382,11 +320,9 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     __syncthreads();  // the selection is complete (in shared memory, or in `out` for long rows)
     if (rounds == 1)
         for (int i = tid; i < keff; i += kTopkThreads) out[i] = dst[i];
-    if constexpr (D > 0) gather_compact<D>(c, r, kvh, L, keff, dst, tid);
 }
 
-template <int D>
-static cudaError_t launch_topk(const TopkParams &p, const CopyParams &c, int batch, cudaStream_t stream) {
+cudaError_t launch_select_topk(const TopkParams &p, int batch, cudaStream_t stream) {
     // The shared-memory opt-in is a per-device function attribute: set it once per device.
     static std::atomic<uint64_t> configured{0};
     int dev = 0;
@@ -394,21 +330,13 @@ static cudaError_t launch_topk(const TopkParams &p, const CopyParams &c, int bat
     if (e != cudaSuccess) return e;
     const uint64_t bit = (dev >= 0 && dev < 64) ? (uint64_t(1) << dev) : 0;
     if (!bit || !(configured.load(std::memory_order_acquire) & bit)) {
-        e = cudaFuncSetAttribute(select_topk_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemBytes);
+        e = cudaFuncSetAttribute(select_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTopkSmemBytes);
         if (e != cudaSuccess) return e;
         configured.fetch_or(bit, std::memory_order_acq_rel);
     }
     dim3 grid(p.hkv, batch);
-    select_topk_kernel<D><<<grid, kTopkThreads, kTopkSmemBytes, stream>>>(p, c);
+    select_topk_kernel<<<grid, kTopkThreads, kTopkSmemBytes, stream>>>(p);
     return cudaGetLastError();
-}
-
-cudaError_t launch_select_topk(const TopkParams &p, int batch, cudaStream_t stream) {
-    return launch_topk<0>(p, CopyParams{}, batch, stream);
-}
-
-cudaError_t launch_select_compact(const TopkParams &p, const CopyParams &c, int batch, cudaStream_t stream) {
-    return c.head_dim == 128 ? launch_topk<128>(p, c, batch, stream) : launch_topk<64>(p, c, batch, stream);
 }
 
 }  // namespace sfi

@@ -106,8 +106,6 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
 
 bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
 
-// Largest k_cap for which sfi_select_compact packs the rows in the Selector's own CTAs.
-constexpr int32_t kFusedCompactMaxK = 1024;
 
 // Plan of a mixed launch. The host knows only upper bounds of the units' lengths, so
 // each mode is cut into fixed-size chunks of sub-blocks: one wave of two CTAs per SM
@@ -671,15 +669,6 @@ sfi_status sfi_select_compact(const sfi_attn_shape *shape, const sfi_paged_kv *k
     c.c_row_offset = compact->row_offset;
     c.c_capacity = compact->capacity;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // The fused launch has one CTA per (request, KV head), which also gathers that unit's
-    // rows: it wins only while the units fill the GPU and the selections are small
-    // (measured: 16K x batch 16 at k = 704, 37 against 39 us). Otherwise the Selector runs
-    // alone and the compaction kernel spreads the rows of all units over every SM
-    // (ragged batch of 8 requests up to 128K: 881 -> 277 us; 64K x batch 8 at k = 4096:
-    // 197 -> 141 us). Both forms give the same results.
-    const int64_t units = (int64_t)batch * shape->num_kv_heads;
-    if (k_cap <= kFusedCompactMaxK && 4 * units >= 3 * (int64_t)sm_count_current_device())
-        return sfi::launch_select_compact(p, c, batch, s) == cudaSuccess ? SFI_OK : SFI_ERR_CUDA;
     if (sfi::launch_select_topk(p, batch, s) != cudaSuccess) return SFI_ERR_CUDA;
     if ((int64_t)sink + k_cap == 0) return SFI_OK;
     c.idx = idx_out;

@@ -131,8 +131,6 @@ struct CopyParams {
     const int32_t *c_capacity;
 };
 cudaError_t launch_paged_append(const CopyParams &p, int batch, cudaStream_t stream);
-// The Selector with the compaction of each (request, KV head) in the same CTA.
-cudaError_t launch_select_compact(const TopkParams &p, const CopyParams &c, int batch, cudaStream_t stream);
 cudaError_t launch_compact_gather(const CopyParams &p, int batch, int max_rows, cudaStream_t stream);
 
 }  // namespace sfi

@@ -21,9 +21,9 @@ import numpy as np
 import torch
 
 from .api import (SFI_ATTN_EARLY_KV_PREFETCH, SFI_ATTN_RAGGED, SFI_MAX_QUERY_TOKENS, AttnShape, CompactKV,
-                  PagedKV, alloc_mixed_workspace, alloc_multi_workspace, alloc_ragged_workspace, alloc_workspace, sfi_compact_gather,
+                  PagedKV, alloc_mixed_workspace, alloc_multi_workspace, alloc_ragged_workspace, alloc_workspace,
                   sfi_dense_verify_attn, sfi_fast_decode_attn, sfi_mixed_decode_attn, sfi_paged_kv_append,
-                  sfi_paged_kv_append_tokens, sfi_select_compact, sfi_select_topk, sfi_slow_dense_attn_with_scores,
+                  sfi_paged_kv_append_tokens, sfi_select_compact, sfi_slow_dense_attn_with_scores,
                   sfi_sparse_draft_attn)
 
 
@@ -125,8 +125,7 @@ class SFIDecoder:
     def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
                  max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
                  main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None,
-                 fuse_append: bool = True, single_launch_mixed: bool = True, fused_select_compact: bool = False,
-                 ragged: bool = False):
+                 fuse_append: bool = True, single_launch_mixed: bool = True, ragged: bool = False):
         self.shape, self.layers, self.batch = shape, layers, batch
         # fuse_append: the attention kernels write the current token into the pages
         # themselves (no separate append launch per layer)
@@ -134,13 +133,6 @@ class SFIDecoder:
         # single_launch_mixed: a mixed step runs one attention launch per layer for its
         # fast and slow requests together (sfi_mixed_decode_attn) instead of two
         self.single_launch_mixed = bool(single_launch_mixed)
-        # fused_select_compact: inside slow steps, the Selector's CTAs also pack the
-        # compact buffer (sfi_select_compact) instead of a separate compaction launch.
-        # Off by default: there the side stream runs beside the slow step's attention,
-        # and the fused CTAs hold whole SMs long enough to delay its waves (measured:
-        # decode step 687 -> 698 us at 16K, batch 16). refresh_selection, which runs on
-        # an otherwise idle GPU, always uses the fused call.
-        self.fused_select_compact = bool(fused_select_compact)
         # ragged: the requests' lengths differ widely; the single-token fast and slow
         # launches are planned in fixed-size chunks sized by each request's own length
         # (SFI_ATTN_RAGGED) rather than with one split count for the whole batch
@@ -224,19 +216,12 @@ class SFIDecoder:
             cur.wait_stream(self.main)
 
     def _refresh(self, i: int, L: LayerBuffers, kv: PagedKV, seq_lens: torch.Tensor,
-                 req_ids: Optional[torch.Tensor], n: Optional[int], fused: Optional[bool] = None):
+                 req_ids: Optional[torch.Tensor], n: Optional[int]):
         """Selector + compaction of layer i on the aux stream (already ordered after the
         scores), then record a_i."""
-        if self.fused_select_compact if fused is None else fused:
-            sfi_select_compact(self.shape, PagedKV(kv.k_pool, kv.v_pool, kv.page_table, seq_lens), L.scores, self.sink,
-                               self.recent, self.batch.k_per_req, L.idx, L.compact, req_ids=req_ids, batch=n,
-                               dev_status=self.dev_status, stream=self.aux)
-        else:
-            sfi_select_topk(L.scores, self.shape.num_kv_heads, seq_lens, self.sink, self.recent,
-                            self.batch.k_per_req, L.idx, L.compact.count, req_ids=req_ids, batch=n,
-                            dev_status=self.dev_status, stream=self.aux)
-            sfi_compact_gather(self.shape, kv, L.idx, L.compact.count, self.sink, L.compact, req_ids=req_ids,
-                               batch=n, dev_status=self.dev_status, stream=self.aux)
+        sfi_select_compact(self.shape, PagedKV(kv.k_pool, kv.v_pool, kv.page_table, seq_lens), L.scores, self.sink,
+                           self.recent, self.batch.k_per_req, L.idx, L.compact, req_ids=req_ids, batch=n,
+                           dev_status=self.dev_status, stream=self.aux)
         self.e_aux[i].record(self.aux)
         self.pending[i] = True
 
@@ -368,7 +353,7 @@ class SFIDecoder:
         self._enter()
         self.aux.wait_stream(self.main)
         for i, L in enumerate(self.layers):
-            self._refresh(i, L, self.kv(i, seq_lens), seq_lens, req_ids, n, fused=True)
+            self._refresh(i, L, self.kv(i, seq_lens), seq_lens, req_ids, n)
         self._leave()
 
     def draft_step(self, io: StepIO, seq_lens: torch.Tensor, num_tokens: int,

@@ -650,18 +650,17 @@ def test_mixed_launch_matches_oracle(bounds):
 
 
 # ---------------------------------------------------------------------------
-# Selector + compaction in one launch (sfi_select_compact)
+# Selector + compaction in one call (sfi_select_compact)
 # ---------------------------------------------------------------------------
 @pytest.mark.parametrize("D,Hq,Hkv,lens,k_per_req,k_cap", [
     (64, 8, 2, [1024, 777, 36, 3, 40], [64, 100, 64, 8, 64], 128),          # L < S, L < S + W, keff < k
     (128, 16, 8, [300, 21000, 530], [400, 1500, 10], 1600),                  # keff == |C|; |C| > 16384 (rounds)
     (128, 32, 8, [4096, 2048], [256, 128], 256),
-    (128, 16, 8, [700 + 37 * i for i in range(16)], [8 * i for i in range(16)], 128),  # 128 units: one launch
+    (128, 16, 8, [700 + 37 * i for i in range(16)], [8 * i for i in range(16)], 128),  # 128 units, ragged k
 ])
 def test_select_compact_bit_exact(D, Hq, Hkv, lens, k_per_req, k_cap):
-    """Selector + compaction in one call (one fused launch when the units fill the GPU and k is
-    small, else the two kernels) equals the oracle Selector (on the GPU-written scores) followed
-    by the oracle compaction, byte for byte, and leaves the same counts."""
+    """Selector + compaction in one call equals the oracle Selector (on the GPU-written scores)
+    followed by the oracle compaction, byte for byte, and leaves the same counts."""
     sfi = _sfi()
     S, W = 4, 32
     prob = Problem(seed=700 + D + len(lens), lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=S, W=W, heavy_frac=0.03).to_device()
@@ -693,10 +692,10 @@ def test_select_compact_bit_exact(D, Hq, Hkv, lens, k_per_req, k_cap):
                 np.testing.assert_array_equal(cv[base + lo:base + hi], rv[kvh, lo:hi], err_msg=f"V r={r} kv={kvh}")
 
 
-@pytest.mark.parametrize("B,Hkv", [(3, 2), (16, 8)], ids=["two-kernels", "one-launch"])
+@pytest.mark.parametrize("B,Hkv", [(3, 2), (16, 8)])
 def test_select_compact_subset_and_bad_capacity(B, Hkv):
     """A request subset is handled alone; a request whose capacity is below S + k_eff keeps its
-    selection, is not packed, and is reported (both forms of the call)."""
+    selection, is not packed, and is reported."""
     sfi = _sfi()
     S, W = 4, 32
     lens = [800 + 100 * (i % 3) for i in range(B)]
