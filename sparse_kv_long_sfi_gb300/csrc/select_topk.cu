@@ -89,9 +89,37 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     const int kvh = blockIdx.x, b = blockIdx.y;
     const int r = p.req_ids ? p.req_ids[b] : b;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const float *row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride + p.sink;
+    // The row's first round (at most 16384 candidates) is requested before the length is
+    // known, from the row's capacity (score_stride - S) rather than its length: the copy
+    // then overlaps the metadata round trip. Every exit below waits for it first.
+    const int64_t room = p.score_stride - p.sink;
+    const int cap0 = room <= 0 ? 0 : room < kTopkRound ? (int)room : kTopkRound;
+    float *const sbuf = s_keys;  // [2][kTopkRound]
+    auto copy_span = [&](int base, int len, uintptr_t &a0, uintptr_t &a1) {  // 16-byte-aligned interior
+        const uintptr_t a = reinterpret_cast<uintptr_t>(row + base);
+        a0 = (a + 15) & ~uintptr_t(15);
+        a1 = (a + 4 * (uintptr_t)len) & ~uintptr_t(15);
+    };
+    if (tid == 0) {
+        mbar_init(&s_bar[0], 1);
+        mbar_init(&s_bar[1], 1);
+        fence_barrier_init();
+        uintptr_t a0, a1;
+        copy_span(0, cap0, a0, a1);
+        if (a1 > a0) {
+            mbar_arrive_expect_tx(&s_bar[0], (uint32_t)(a1 - a0));
+            bulk_load_1d(sbuf, reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0), &s_bar[0]);
+        } else {
+            mbar_arrive(&s_bar[0]);
+        }
+    }
+    __syncthreads();
+    auto drain = [&]() { mbar_wait_warp(&s_bar[0], 0); };  // the first copy has landed (bounded)
     const int L = p.seq_lens[r];
     if (L < 0 || L > p.score_stride) {
         if (tid == 0 && kvh == 0) report(p.dev_status, SFI_DEV_BAD_LEN);
+        drain();
         return;
     }
     const int n = max(0, L - p.recent - p.sink);  // |C|, C = [S, L - W)
@@ -99,15 +127,17 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     const int rounds = (n + kTopkRound - 1) / kTopkRound;
     if (k < 0 || k > p.k_cap || rounds > kTopkMaxRounds) {
         if (tid == 0 && kvh == 0) report(p.dev_status, SFI_DEV_K_OVERFLOW);
+        drain();
         return;
     }
     const int keff = min(k, n);
     if (kvh == 0 && tid == 0) p.count_out[r] = keff;
-    if (keff == 0) return;
     int32_t *out = p.idx_out + ((int64_t)r * p.hkv + kvh) * p.k_cap;
-    const float *row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride + p.sink;
     if (keff == n) {  // everything is selected
         for (int i = tid; i < n; i += kTopkThreads) out[i] = p.sink + i;
+    }
+    if (keff == 0 || keff == n) {
+        drain();
         return;
     }
 
@@ -117,14 +147,12 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     // the whole selection. Two rounds: both stay in the two buffers. More: every use of
     // a round (4 radix passes, the counts, the output) streams through the two buffers,
     // the next copy in flight while the current round is read.
-    float *const sbuf = s_keys;                                             // [2][kTopkRound]
     uint32_t *hrep = reinterpret_cast<uint32_t *>(s_keys + 2 * kTopkRound);  // [256][32] lane counters
     const int total_uses = 6 * rounds;
     auto issue = [&](int b, int rd) {  // thread 0: copy round rd into buffer b
         const int base = rd * kTopkRound, len = min(kTopkRound, n - base);
-        const uintptr_t a = reinterpret_cast<uintptr_t>(row + base);
-        const uintptr_t a0 = (a + 15) & ~uintptr_t(15);
-        const uintptr_t a1 = (a + 4 * (uintptr_t)len) & ~uintptr_t(15);
+        uintptr_t a0, a1;
+        copy_span(base, len, a0, a1);
         if (a1 > a0) {
             mbar_arrive_expect_tx(&s_bar[b], (uint32_t)(a1 - a0));
             bulk_load_1d(sbuf + b * kTopkRound, reinterpret_cast<const void *>(a0), (uint32_t)(a1 - a0), &s_bar[b]);
@@ -137,8 +165,8 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
         const int rd = u % rounds, b = u & 1, base = rd * kTopkRound, len = min(kTopkRound, n - base);
         if ((rounds != 2 || u < 2) && !mbar_wait_warp(&s_bar[b], (u >> 1) & 1)) return false;
         const uintptr_t a = reinterpret_cast<uintptr_t>(row + base);
-        const uintptr_t a0 = (a + 15) & ~uintptr_t(15);
-        const uintptr_t a1 = (a + 4 * (uintptr_t)len) & ~uintptr_t(15);
+        uintptr_t a0, a1;
+        copy_span(base, len, a0, a1);  // (the early copy of round 0 covers at least this span)
         const int lo_i = (int)((a0 - a) >> 2);  // row[base + i], lo_i <= i < hi_i, is sbuf[b][i - lo_i]
         const int hi_i = a1 > a0 ? (int)((a1 - a) >> 2) : lo_i;
         const float *bb = sbuf + b * kTopkRound;
@@ -155,14 +183,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             if (tid == 0) issue(u & 1, (u + 2) % rounds);
         }
     };
-    if (tid == 0) {
-        mbar_init(&s_bar[0], 1);
-        mbar_init(&s_bar[1], 1);
-        fence_barrier_init();
-        issue(0, 0);
-        if (rounds > 1) issue(1, 1);
-    }
-    __syncthreads();
+    if (tid == 0 && rounds > 1) issue(1, 1);  // round 0 is already on its way
     int use = 0;
     if (rounds == 1) {  // resident in registers for the whole selection
         if (!fetch(use++)) {
@@ -252,12 +273,14 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             if (lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
             return;
         }
-        int gt = 0, eq = 0;
+        unsigned gt_l = 0, eq_l = 0;  // this lane's counts, then summed over the warp
 #pragma unroll
         for (int j = 0; j < kTopkPerThread; ++j) {
-            gt += __popc(__ballot_sync(0xffffffffu, key[j] != kNoKey && key[j] > tau));
-            eq += __popc(__ballot_sync(0xffffffffu, key[j] == tau));
+            gt_l += (key[j] != kNoKey && key[j] > tau) ? 1u : 0u;
+            eq_l += key[j] == tau ? 1u : 0u;
         }
+        const int gt = (int)__reduce_add_sync(0xffffffffu, gt_l);
+        const int eq = (int)__reduce_add_sync(0xffffffffu, eq_l);
         if (lane == 0) {
             s_gt[rd * kTopkWarps + warp] = gt;
             s_eq[rd * kTopkWarps + warp] = eq;
@@ -301,19 +324,34 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
         }
         int eq_before = s_eq[rd * kTopkWarps + warp];
         int out_pos = s_gt[rd * kTopkWarps + warp] + min(eq_before, take_eq);
+        bool ties = false;  // does this warp hold keys equal to tau in this round?
 #pragma unroll
-        for (int j = 0; j < kTopkPerThread; ++j) {
-            const bool valid = key[j] != kNoKey;
-            const bool is_eq = valid && key[j] == tau;
-            const uint32_t eq_bal = __ballot_sync(0xffffffffu, is_eq);
-            const int eq_rank = eq_before + __popc(eq_bal & lt_mask);
-            const bool take = valid && (key[j] > tau || (is_eq && eq_rank < take_eq));
-            const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
-            if (take)
-                dst[out_pos + __popc(take_bal & lt_mask)] =
-                    p.sink + rd * kTopkRound + warp * (32 * kTopkPerThread) + 32 * j + lane;
-            out_pos += __popc(take_bal);
-            eq_before += __popc(eq_bal);
+        for (int j = 0; j < kTopkPerThread; ++j) ties |= key[j] == tau;
+        if (!__any_sync(0xffffffffu, ties)) {  // common case: take exactly the keys above tau
+#pragma unroll
+            for (int j = 0; j < kTopkPerThread; ++j) {
+                const bool take = key[j] != kNoKey && key[j] > tau;
+                const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
+                if (take)
+                    dst[out_pos + __popc(take_bal & lt_mask)] =
+                        p.sink + rd * kTopkRound + warp * (32 * kTopkPerThread) + 32 * j + lane;
+                out_pos += __popc(take_bal);
+            }
+        } else {
+#pragma unroll
+            for (int j = 0; j < kTopkPerThread; ++j) {
+                const bool valid = key[j] != kNoKey;
+                const bool is_eq = valid && key[j] == tau;
+                const uint32_t eq_bal = __ballot_sync(0xffffffffu, is_eq);
+                const int eq_rank = eq_before + __popc(eq_bal & lt_mask);
+                const bool take = valid && (key[j] > tau || (is_eq && eq_rank < take_eq));
+                const uint32_t take_bal = __ballot_sync(0xffffffffu, take);
+                if (take)
+                    dst[out_pos + __popc(take_bal & lt_mask)] =
+                        p.sink + rd * kTopkRound + warp * (32 * kTopkPerThread) + 32 * j + lane;
+                out_pos += __popc(take_bal);
+                eq_before += __popc(eq_bal);
+            }
         }
         if (rounds > 1) release(use++);
     }
