@@ -82,8 +82,8 @@ __device__ __forceinline__ int4 ld_nc_v4_sel(const void *ptr) {
 __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkParams p) {
     extern __shared__ __align__(16) float s_keys[];
     __shared__ __align__(8) uint64_t s_bar[2];
-    __shared__ uint32_t hist[256];
-    __shared__ uint32_t s_bin, s_rem;
+    __shared__ uint32_t hist[2][256];  // pass p uses hist[p & 1]
+    __shared__ uint32_t s_bin[2], s_rem[2];
     __shared__ int32_t s_gt[kTopkMaxRounds * kTopkWarps], s_eq[kTopkMaxRounds * kTopkWarps];
 
     const int kvh = blockIdx.x, b = blockIdx.y;
@@ -193,19 +193,21 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
     }
 
     // ---- radix select of the keff-th largest key ----
+    // Double-buffered bins and results: pass p clears hist[(p + 1) & 1] for the next pass
+    // (its last reader, pass p - 1's scan, is behind every thread) and the lane counters
+    // are cleared as they are summed, so each pass needs no barrier of its own for that.
     uint32_t prefix = 0u, mask = 0u;
     uint32_t rem = (uint32_t)keff;  // how many still to take inside the current prefix
-    for (int shift = 24; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 256 * 32; i += kTopkThreads) hrep[i] = 0u;
+    __syncthreads();
+    int pass = 0;
+    for (int shift = 24; shift >= 0; shift -= 8, ++pass) {
         const bool lanes = shift >= 16;
-        if (lanes) {
-            for (int i = tid; i < 256 * 32; i += kTopkThreads) hrep[i] = 0u;
-        } else {
-            for (int i = tid; i < 256; i += kTopkThreads) hist[i] = 0u;
-        }
-        __syncthreads();
+        uint32_t *const hcur = hist[pass & 1];
+        if (tid < 256) hist[(pass + 1) & 1][tid] = 0u;
         if (rounds == 1) {
             if (lanes) histogram_lanes(key, prefix, mask, shift, lane, hrep);
-            else histogram_round(key, prefix, mask, shift, lane, hist);
+            else histogram_round(key, prefix, mask, shift, lane, hcur);
         } else {
             for (int rd = 0; rd < rounds; ++rd) {
                 if (!fetch(use)) {
@@ -213,17 +215,21 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
                     return;
                 }
                 if (lanes) histogram_lanes(key, prefix, mask, shift, lane, hrep);
-                else histogram_round(key, prefix, mask, shift, lane, hist);
+                else histogram_round(key, prefix, mask, shift, lane, hcur);
                 release(use++);
             }
         }
         __syncthreads();
-        if (lanes) {  // hist[b] = sum of bin b's 32 lane counters (rotated: a warp's reads hit 32 banks)
+        if (lanes) {  // bin b = sum of its 32 lane counters (rotated: a warp's reads hit 32 banks), cleared
             if (tid < 256) {
                 uint32_t sum = 0u;
 #pragma unroll 8
-                for (int l = 0; l < 32; ++l) sum += hrep[tid * 32 + ((l + tid) & 31)];
-                hist[tid] = sum;
+                for (int l = 0; l < 32; ++l) {
+                    const int i = tid * 32 + ((l + tid) & 31);
+                    sum += hrep[i];
+                    hrep[i] = 0u;
+                }
+                hcur[tid] = sum;
             }
             __syncthreads();
         }
@@ -233,7 +239,7 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             uint32_t sum = 0u;
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                c[j] = hist[255 - 8 * lane - j];
+                c[j] = hcur[255 - 8 * lane - j];
                 sum += c[j];
             }
             uint32_t incl = sum;  // inclusive prefix over lanes (from the top bins)
@@ -250,8 +256,8 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
 #pragma unroll
                 for (int j = 0; j < 8; ++j) {
                     if (above + c[j] >= rem) {
-                        s_bin = 255u - 8u * lane - j;
-                        s_rem = rem - above;
+                        s_bin[pass & 1] = 255u - 8u * lane - j;
+                        s_rem[pass & 1] = rem - above;
                         break;
                     }
                     above += c[j];
@@ -259,10 +265,9 @@ __global__ void __launch_bounds__(kTopkThreads) select_topk_kernel(const TopkPar
             }
         }
         __syncthreads();
-        prefix |= s_bin << shift;
+        prefix |= s_bin[pass & 1] << shift;
         mask |= 255u << shift;
-        rem = s_rem;
-        __syncthreads();
+        rem = s_rem[pass & 1];
     }
     const uint32_t tau = prefix;
     const int take_eq = (int)rem;  // keys equal to tau to take, lowest positions first
