@@ -99,6 +99,12 @@ typedef enum {
  * sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0) bytes for the fast call and
  * sfi_mixed_workspace_size(shape, 0, batch, 0, max_tokens) for the dense one. */
 #define SFI_ATTN_RAGGED 2u
+/* Diagnostic flag of the same two calls, for testing the bounded in-kernel waits: the
+ * TMA producer of every CTA withholds the copies of its second stage, so the consumers'
+ * wait for it runs out (after about 2 s) and the launch reports SFI_DEV_TIMEOUT; the
+ * outputs are then unspecified, the workspace must be zeroed again, and the context
+ * stays usable. Units shorter than two stages are unaffected. Not for production use. */
+#define SFI_ATTN_TEST_WITHHOLD 4u
 
 /* Most query tokens per request in the multi-token calls (tokens x G must also be
  * <= 16: G = 2 allows 8 tokens, G = 4 four, G = 8 two). */
@@ -169,7 +175,8 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  *                is small. It affects speed only, never results.
  *   num_splits : 0 = automatic; otherwise the number of KV splits per
  *                (request, KV head) (clamped to the plan's maximum).
- *   flags      : 0, SFI_ATTN_EARLY_KV_PREFETCH and/or SFI_ATTN_RAGGED.
+ *   flags      : 0, SFI_ATTN_EARLY_KV_PREFETCH and/or SFI_ATTN_RAGGED (and the diagnostic
+ *                SFI_ATTN_TEST_WITHHOLD).
  *   workspace  : at least sfi_workspace_size(shape, batch, max_tokens, num_splits)
  *                bytes of device memory, zero-filled before its first use. The
  *                kernels leave it zero-filled again when they finish without a

@@ -35,6 +35,7 @@ SFI_DEV_BAD_PAGE, SFI_DEV_BAD_LEN, SFI_DEV_K_OVERFLOW = 1, 2, 4
 SFI_DEV_BAD_INDEX, SFI_DEV_TIMEOUT, SFI_DEV_BAD_COMPACT = 8, 16, 32
 SFI_ATTN_EARLY_KV_PREFETCH = 1
 SFI_ATTN_RAGGED = 2
+SFI_ATTN_TEST_WITHHOLD = 4
 SFI_MAX_QUERY_TOKENS = 16
 
 P_SHAPE = ctypes.POINTER(sfi_attn_shape)

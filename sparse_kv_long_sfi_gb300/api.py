@@ -19,6 +19,7 @@ from . import _abi
 SFI_ATTN_EARLY_KV_PREFETCH = _abi.SFI_ATTN_EARLY_KV_PREFETCH
 SFI_MAX_QUERY_TOKENS = _abi.SFI_MAX_QUERY_TOKENS
 SFI_ATTN_RAGGED = _abi.SFI_ATTN_RAGGED
+SFI_ATTN_TEST_WITHHOLD = _abi.SFI_ATTN_TEST_WITHHOLD
 
 
 class SFIError(RuntimeError):

@@ -870,6 +870,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     break;
                 }
             }
+            if (p.withhold == st + 1) continue;  // diagnostic: this stage's copies never come
             // A stage of compact sub-blocks needs no page id; skipping the shuffle there keeps
             // the page-table loads off the path of the first TMA copies.
             const bool paged = sb_begin + (st + 1) * kConsumerWarps > u.nb1;  // warp-uniform

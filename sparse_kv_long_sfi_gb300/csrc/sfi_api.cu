@@ -316,6 +316,7 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
     p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
+    p.withhold = (flags & SFI_ATTN_TEST_WITHHOLD) ? 2 : 0;  // the second stage
     p.c_row_offset = compact->row_offset;
     p.c_capacity = compact->capacity;
     p.c_count = compact->count;
@@ -359,6 +360,7 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
     p.k_new = static_cast<const __nv_bfloat16 *>(k_new);
     p.v_new = static_cast<const __nv_bfloat16 *>(v_new);
     p.early_prefetch = (flags & SFI_ATTN_EARLY_KV_PREFETCH) ? 1 : 0;
+    p.withhold = (flags & SFI_ATTN_TEST_WITHHOLD) ? 2 : 0;  // the second stage
     p.scores = scores;
     p.score_stride = score_stride;
     AttnMaps maps;

@@ -425,6 +425,37 @@ def test_bad_page_and_length_are_reported_not_faulted():
     assert st.item() & 2
 
 
+@pytest.mark.parametrize("splits", [2, 12], ids=["cluster-merge", "workspace-merge"])
+def test_bounded_wait_runs_out_and_reports_timeout(splits):
+    """SFI_ATTN_TEST_WITHHOLD: every CTA's producer withholds its second stage, so the
+    consumers' bounded wait runs out (about 2 s): the launch returns with SFI_DEV_TIMEOUT
+    and writes no output, and a normal launch right after it (fresh status, zeroed
+    workspace) is correct, so the context stays usable."""
+    sfi = _sfi()
+    prob = Problem(seed=53, lens=[3000, 2500], Hq=16, Hkv=8, D=128, S=4, W=32).to_device()
+    maxL = int(prob.lens.max()) + 16
+    sentinel = float("nan")
+    out = torch.full((prob.B, prob.Hq, prob.D), sentinel, device="cuda")
+    ws = sfi.alloc_workspace(prob.shape, prob.B, maxL, splits)
+    st = _status()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, None, None,
+                                        max_tokens=maxL, num_splits=splits, workspace=ws, dev_status=st,
+                                        flags=sfi.SFI_ATTN_TEST_WITHHOLD)
+    torch.cuda.synchronize()
+    assert st.item() & 16, f"status {st.item()}"  # SFI_DEV_TIMEOUT
+    assert np.isnan(out.cpu().numpy()).all(), "a timed-out launch writes no output"
+    ws.zero_()
+    st.zero_()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, None, None,
+                                        max_tokens=maxL, num_splits=splits, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 0
+    o = out.cpu().numpy()
+    for r in range(prob.B):
+        o_ref, _ = prob.oracle_dense(r)
+        assert_close(o[r], o_ref, f"after the timeout r={r}")
+
+
 def test_bad_selected_index_is_reported():
     sfi = _sfi()
     prob = Problem(seed=52, lens=[200], Hq=8, Hkv=2, D=64, S=4, W=32).to_device()
