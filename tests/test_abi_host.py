@@ -161,3 +161,15 @@ def test_select_compact_validates_on_the_host(libsfi):
     assert call(cnt=None) == 1 and call(c=None) == 1 and call(sink=-1) == 1
     assert call(c=_abi.sfi_compact_kv(4097, 4096, 100, 4096, 4096, 4096)) == 1  # unaligned compact K
     assert call(batch=0) == 0
+
+
+def test_binding_constants_match_the_header():
+    """Every numeric #define and status enumerator of include/sfi.h has the same value
+    in the Python binding."""
+    from sparse_kv_long_sfi_gb300 import _abi
+    text = open(os.path.join(os.path.dirname(__file__), "..", "include", "sfi.h")).read()
+    defines = {m.group(1): int(m.group(2)) for m in re.finditer(r"^#define (SFI_(?:DEV|ATTN|MAX)_\w+) (\d+)u?\b", text, re.M)}
+    enums = {m.group(1): int(m.group(2)) for m in re.finditer(r"^\s+(SFI_(?:OK|ERR_\w+)) = (\d+)", text, re.M)}
+    assert len(defines) >= 10 and len(enums) == 5
+    for name, value in {**defines, **enums}.items():
+        assert getattr(_abi, name) == value, name
