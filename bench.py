@@ -193,7 +193,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "4eb302d621a124b4", "fast": 68_341_888 + 16_896, "slow": 1_074_210_048 + 5_368_960}
+PROFILED_TRAFFIC = {"sha256_16": "c30f96b44878e281", "fast": 68_341_760 + 15_616, "slow": 1_074_202_368 + 5_353_984}
 
 
 def profiled_traffic(kind):
