@@ -91,19 +91,20 @@ typedef enum {
  * preceding kernel has finished; q, k_new and v_new are still read, and every output
  * written, only after it has finished. Without the flag nothing is read before then. */
 #define SFI_ATTN_EARLY_KV_PREFETCH 1u
-/* Flag of sfi_fast_decode_attn and sfi_slow_dense_attn_with_scores: the requests' lengths
- * differ widely (a ragged batch). The launch is then planned in fixed-size chunks, as
- * sfi_mixed_decode_attn does (each (request, KV head) gets splits in proportion to its
- * real length, found on the device), instead of the same number of splits for every
- * request; num_splits is ignored and the workspace must hold
- * sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0) bytes for the fast call and
- * sfi_mixed_workspace_size(shape, 0, batch, 0, max_tokens) for the dense one. */
+/* SFI_ATTN_RAGGED (sfi_fast_decode_attn and sfi_slow_dense_attn_with_scores): the
+ * requests' lengths differ widely (a ragged batch). The launch is then planned in
+ * fixed-size chunks, as sfi_mixed_decode_attn does (each (request, KV head) gets
+ * splits in proportion to its real length, found on the device), instead of the same
+ * number of splits for every request; num_splits is ignored and the workspace must
+ * hold sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0) bytes for the fast
+ * call and sfi_mixed_workspace_size(shape, 0, batch, 0, max_tokens) for the dense one. */
 #define SFI_ATTN_RAGGED 2u
-/* Diagnostic flag of the same two calls, for testing the bounded in-kernel waits: the
- * TMA producer of every CTA withholds the copies of its second stage, so the consumers'
- * wait for it runs out (after about 2 s) and the launch reports SFI_DEV_TIMEOUT; the
- * outputs are then unspecified, the workspace must be zeroed again, and the context
- * stays usable. Units shorter than two stages are unaffected. Not for production use. */
+/* SFI_ATTN_TEST_WITHHOLD (the same two calls; diagnostic, for testing the bounded
+ * in-kernel waits): the TMA producer of every CTA withholds the copies of its second
+ * stage, so the consumers' wait for it runs out (after about 2 s) and the launch
+ * reports SFI_DEV_TIMEOUT; the outputs are then unspecified, the workspace must be
+ * zeroed again, and the context stays usable. Units shorter than two stages are
+ * unaffected. Not for production use. */
 #define SFI_ATTN_TEST_WITHHOLD 4u
 
 /* Most query tokens per request in the multi-token calls (tokens x G must also be
