@@ -242,6 +242,34 @@ def test_ragged_mixed_batch_64_requests(single_launch, ragged):
     _run_schedule(w, modes, sampled=sorted({short, long_, slow_then_fast}), retention=ret)
 
 
+@pytest.mark.parametrize("single_launch,ragged", [(True, False), (False, True)], ids=["one-launch", "ragged-flag"])
+def test_randomized_schedule_small(single_launch, ragged):
+    """Twelve decode steps whose kinds are drawn at random (all slow, all fast, fast with
+    a refresh layer, mixed) over 6 requests of different lengths, 2 layers, D 64, G 4,
+    per-request retention; every request is checked against the oracle after every
+    step, so stale compact buffers or mis-ordered side-stream work would show."""
+    g = syn.rng(78, 0)  # a draw with every step kind at least twice
+    B, steps, S, W = 6, 12, 16, 64
+    lens = g.integers(1500, 5000, size=B)
+    ret = g.choice([0.05, 0.1, 0.2], size=B)
+    k0 = [syn.retention_budget(ret[r], int(lens[r]) + 1, S, W) for r in range(B)]
+    k_cap = max(syn.retention_budget(ret[r], int(lens[r]) + steps + 1, S, W) for r in range(B))
+    w = Workload(78, lens, 8, 2, 64, S, W, k0, steps=steps, layers=2, heavy_frac=0.02, k_cap=k_cap,
+                 single_launch_mixed=single_launch, ragged=ragged)
+    modes, refresh = [[1] * B], [()]
+    for _ in range(1, steps):
+        kind = int(g.integers(0, 4))
+        if kind == 3:  # mixed: at least one slow and one fast request
+            m = (g.random(B) < 0.4).astype(int)
+            m[0], m[1] = 1, 0
+            modes.append(list(m))
+        else:
+            modes.append([1 if kind == 0 else 0] * B)
+        refresh.append((1,) if kind == 2 else ())
+    assert any(0 < sum(x) < B for x in modes) and any(refresh)
+    _run_schedule(w, modes, sampled=list(range(B)), retention=ret, refresh=refresh)
+
+
 def test_refresh_layer_inside_fast_steps():
     """ASPIRE's intra-draft refresh layer: layer 1 runs the slow path (dense attention,
     scores, Selector, compaction) inside fast steps; the step after uses its fresh
