@@ -261,7 +261,7 @@ def run_gpu(args, ranks: Ranks):
     layers = sfi.allocate_layers(shape, NL, num_pages, batch, S, device=dev, pool_init=pool_init)
     torch.cuda.synchronize()
     t_alloc = time.time() - t_alloc
-    dec = sfi.SFIDecoder(shape, layers, batch, S, W, max_len=L0 + cyc, device=dev)
+    dec = sfi.SFIDecoder(shape, layers, batch, S, W, max_len=L0 + cyc, device=dev, k_max=k_main)
     ios = [sfi.StepIO(q_all[t], kn_all[t], vn_all[t], out) for t in range(cyc)]
 
     def cycle():

@@ -125,7 +125,8 @@ class SFIDecoder:
     def __init__(self, shape: AttnShape, layers: List[LayerBuffers], batch: DecodeBatch, sink: int, recent: int,
                  max_len: int, dev_status: Optional[torch.Tensor] = None, device="cuda",
                  main_stream: Optional[torch.cuda.Stream] = None, aux_stream: Optional[torch.cuda.Stream] = None,
-                 fuse_append: bool = True, single_launch_mixed: bool = True, ragged: bool = False):
+                 fuse_append: bool = True, single_launch_mixed: bool = True, ragged: bool = False,
+                 k_max: Optional[int] = None):
         self.shape, self.layers, self.batch = shape, layers, batch
         # fuse_append: the attention kernels write the current token into the pages
         # themselves (no separate append launch per layer)
@@ -140,7 +141,11 @@ class SFIDecoder:
         self.sink, self.recent = int(sink), int(recent)
         self.max_len = int(max_len)
         B = batch.page_table.shape[0]
-        self.max_fast_tokens = self.sink + int(batch.k_cap) + self.recent + 2 * shape.page_size
+        # k_max: the largest k_per_req the caller will set (default: the compact capacity).
+        # It only sizes the split-KV plan of the fast launches: a bound above the real k
+        # over-splits small batches, one below it costs speed, never correctness.
+        k_plan = int(batch.k_cap) if k_max is None else max(0, min(int(k_max), int(batch.k_cap)))
+        self.max_fast_tokens = self.sink + k_plan + self.recent + 2 * shape.page_size
         self.max_dense_tokens = self.max_len + shape.page_size
         if self.ragged:
             self.ws_fast = alloc_ragged_workspace(shape, B, self.max_fast_tokens, device=device)
