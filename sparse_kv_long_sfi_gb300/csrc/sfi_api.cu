@@ -86,7 +86,12 @@ sfi_status check_paged(const sfi_attn_shape *s, const sfi_paged_kv *kv) {
 // Split-KV plan of one attention launch. Automatic plans fill one wave of resident
 // CTAs (two per SM) and keep at least four full stages of sub-blocks per split; an
 // explicit request is honoured down to two stages per split. Plans of up to
-// kMaxClusterSplits merge inside a thread-block cluster (no workspace).
+// kMaxClusterSplits merge inside a thread-block cluster (no workspace). Beyond that the
+// last CTA of a unit merges every split from the workspace, a tail that grows with the
+// split count: such plans take one CTA per SM, and only when that still gives at least
+// twice kMaxClusterSplits; otherwise they stay at kMaxClusterSplits. (Batch 1 at 16K:
+// dense 31.7 -> 20.4 us per layer at 19-24 splits instead of 38; batch 4: 8 splits in
+// a cluster beat 9 through the workspace.)
 int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_count) {
     constexpr int kMaxSplits = 256;
     if (units <= 0) return 1;
@@ -99,6 +104,10 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
         s = 1;
     } else {
         s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm / units);
+        if (s > sfi::kMaxClusterSplits) {
+            const int one_per_sm = (int)std::max<int64_t>(1, (int64_t)sm_count / units);
+            s = one_per_sm >= 2 * sfi::kMaxClusterSplits ? one_per_sm : sfi::kMaxClusterSplits;
+        }
         s = std::min(s, std::max(1, nb / (4 * sfi::kConsumerWarps)));
     }
     return std::max(1, std::min(s, kMaxSplits));
