@@ -193,7 +193,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "c30f96b44878e281", "fast": 68_341_760 + 15_616, "slow": 1_074_202_368 + 5_353_984}
+PROFILED_TRAFFIC = {"sha256_16": "186a99400c22433f", "fast": 68_341_760 + 19_584, "slow": 1_074_204_416 + 5_356_160}
 
 
 def profiled_traffic(kind):
