@@ -62,6 +62,25 @@ def _dense(prob, num_splits=0, scores=None, req_ids=None, ragged=False, max_toke
 # ---------------------------------------------------------------------------
 # Dense / slow-step attention
 # ---------------------------------------------------------------------------
+def test_automatic_split_plans():
+    """The automatic plans on this GPU: one wave of two CTAs per SM while that stays within
+    a cluster (8 splits); above that, one CTA per SM when it still gives >= 16 splits,
+    else 8; never fewer than four stages (16 sub-blocks) per split; the workspace
+    follows the plan (none inside a cluster)."""
+    sfi = _sfi()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    shape = sfi.AttnShape(16, 8, 128)
+    for batch in (1, 2, 4, 16, 64):
+        for L in (1040, 16400, 65600):
+            units, nb = batch * 8, (L + 15) // 16 + 1
+            s = max(1, 2 * sms // units)
+            if s > 8:
+                s = sms // units if sms // units >= 16 else 8
+            s = max(1, min(s, nb // 16, 256))
+            assert sfi.sfi_plan_splits(shape, batch, L, 0) == s, (batch, L)
+            assert (sfi.sfi_workspace_size(shape, batch, L, 0) == 0) == (s <= 8), (batch, L)
+
+
 @pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 8), (128, 32, 8), (128, 64, 8), (64, 8, 2), (128, 8, 8)])
 @pytest.mark.parametrize("splits", [1, 3, 0])
 def test_dense_attention_matches_oracle(D, Hq, Hkv, splits):
