@@ -413,13 +413,19 @@ SFI_API sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, con
 /*
  * sfi_workspace_size - bytes of workspace the attention entry points need for this
  * batch, token bound and split request on the current device (split-KV partial
- * states plus one counter per (request, KV head)). Returns 0 on invalid input.
+ * states plus one counter per (request, KV head)). Returns 0 when the plan needs none
+ * (at most 8 splits: the splits of a unit merge inside a thread-block cluster) and on
+ * invalid input.
  */
 SFI_API size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
 
 /*
  * sfi_plan_splits - the split count the attention entry points will use for these
  * arguments on the current device (for reports and tests). 0 on invalid input.
+ * Automatic plans (num_splits = 0) fill one wave of two CTAs per SM over the
+ * (request, KV head) units; above 8 splits they take one CTA per SM when that still
+ * gives at least 16 splits, else 8; every split keeps at least four stages of 64
+ * tokens. An explicit num_splits is honoured down to two stages per split.
  */
 SFI_API int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
 
