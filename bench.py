@@ -13,10 +13,22 @@ fast steps (append, sparse attention over sink + selected + recent) at 6.25%
 retention (k = 704). The whole cycle is one CUDA graph replay. `value` is the
 decode-attention time per decode step (cycle time / 16, all 28 layers).
 
-Also reported: the fast-step retention sweep of Table 1 against the dense decode
-kernel, the end-to-end time through the public API with host buffers (per decode
-step: H2D of q/k/v, D2H of the outputs), the roofline of the dominant kernel, and
-the CPU oracle timed on a bounded sample (the reference arm: --impl reference).
+Also reported: the end-to-end time through the public API with host buffers (per
+decode step: H2D of q/k/v, D2H of the outputs), the roofline of the dominant kernel,
+the CPU oracle timed on a bounded sample (the reference arm: --impl reference), and
+these sections (--sections):
+  overlap          the side stream's overlap: the cycle with the Selector and
+                   compaction on the main stream against the two-stream cycle, the
+                   side work alone, and the first fast step's penalty against the
+                   side work's own HBM time;
+  retention        Table 1's retention sweep against the dense decode kernel;
+  speculative      verification and draft passes of T = 1, 2, 4, 8 tokens;
+  batch1           the same cycle and retention sweep at batch 1;
+  qwen3_8b         the Qwen3-8B-shaped workload as a full cycle: 36 layers, batch 32,
+                   KV 32K, 6.25% retention, one slow step every 16;
+  other            per-launch times of the 64-query-head, KV 64K, top-4096 slow step;
+  ragged           one step of the ragged 64-request batch, one vs two launches;
+  ragged_schedule  the ragged batch under its seeded boundary process for 64 steps.
 """
 from __future__ import annotations
 
@@ -44,7 +56,7 @@ SWEEP_N = [1, 4, 8, 16, 24, 32, 48, 63, 64]
 TABLE1 = {1: 10.67, 4: 9.56, 8: 7.15, 16: 3.96, 24: 2.75, 32: 2.10, 48: 1.43, 63: 1.10, 64: 1.00}
 
 
-SECTIONS = ("retention", "speculative", "other", "ragged")
+SECTIONS = ("overlap", "retention", "speculative", "batch1", "qwen3_8b", "other", "ragged", "ragged_schedule")
 
 
 def parse_args():
@@ -214,13 +226,186 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+class Cycle:
+    """One SFI refresh cycle of a uniform batch, resident in HBM: 1 slow + (cyc - 1) fast
+    decode steps over NL layers through SFIDecoder (main + side stream), replayable as
+    one CUDA graph. Every layer has its own paged pools, compact buffers and scores."""
+
+    def __init__(self, dev, seed0, Hq, Hkv, NL, B, L0, retention, cyc, D=128, P=16, S=64, W=256, heavy=True,
+                 k_cap=None):
+        import torch
+        import sfi_synth as syn
+        import sparse_kv_long_sfi_gb300 as sfi
+        self.dev, self.Hq, self.Hkv, self.NL, self.B, self.L0 = dev, Hq, Hkv, NL, B, L0
+        self.D, self.P, self.S, self.W, self.cyc = D, P, S, W, cyc
+        self.shape = sfi.AttnShape(Hq, Hkv, D, P)
+        self.k = syn.retention_budget(retention, L0, S, W)
+        k_cap = self.k if k_cap is None else max(self.k, k_cap)
+        g = syn.rng(seed0, 1)
+        table, num_pages = syn.make_page_table(g, [L0 + cyc] * B, P, shuffle=True)
+        self.page_table = torch.as_tensor(table).to(dev)
+        off, cap = sfi.compact_layout(self.shape, S, [k_cap] * B, device=dev)
+        self.batch = sfi.DecodeBatch(self.page_table, off, cap, torch.full((B,), self.k, dtype=torch.int32, device=dev),
+                                     k_cap, score_stride=L0 + cyc)
+        self.seq_steps = torch.tensor([[L0 + t] * B for t in range(cyc)], dtype=torch.int32, device=dev)
+        self.q_all = torch.empty((cyc, NL, B, Hq, D), dtype=torch.bfloat16, device=dev)
+        self.kn_all = torch.empty((cyc, NL, B, Hkv, D), dtype=torch.bfloat16, device=dev)
+        self.vn_all = torch.empty_like(self.kn_all)
+        syn.device_normal_bf16_(self.q_all, syn.stream_seed(seed0, 2))
+        syn.device_normal_bf16_(self.kn_all, syn.stream_seed(seed0, 3))
+        syn.device_normal_bf16_(self.vn_all, syn.stream_seed(seed0, 4))
+        self.out = torch.zeros((NL, B, Hq, D), dtype=torch.float32, device=dev)
+
+        def pool_init(i, kp, vp):
+            syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 10, i))
+            syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 11, i))
+            if heavy:
+                syn.device_plant_heavy_hitters_(kp, self.page_table, self.q_all[0, i], self.seq_steps[0], S, W,
+                                                WL["heavy_hitter_frac"], WL["heavy_hitter_beta"],
+                                                syn.stream_seed(seed0, 12, i))
+
+        t0 = time.time()
+        self.layers = sfi.allocate_layers(self.shape, NL, num_pages, self.batch, S, device=dev, pool_init=pool_init)
+        torch.cuda.synchronize()
+        self.alloc_s = time.time() - t0
+        self.dec = sfi.SFIDecoder(self.shape, self.layers, self.batch, S, W, max_len=L0 + cyc, device=dev, k_max=self.k)
+        self.ios = [sfi.StepIO(self.q_all[t], self.kn_all[t], self.vn_all[t], self.out) for t in range(cyc)]
+        # algorithmic bytes: per launch (the fused append included) and per cycle
+        self.by_fast = fast_bytes(B, Hq, Hkv, D, P, S + self.k + W, W) + append_bytes(B, Hkv, D)
+        self.by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True) + append_bytes(B, Hkv, D)
+        self.by_aux = select_bytes(B, Hkv, L0 - S - W, self.k) + compact_bytes(B, Hkv, D, S, self.k)
+        self.by_cycle = NL * (self.by_slow + self.by_aux) + (cyc - 1) * NL * self.by_fast
+        self.launches_per_cycle = NL * 3 + (cyc - 1) * NL  # slow + Selector + compaction, then fast
+
+    def run(self, dec=None, marks=None):
+        """Issue one cycle on dec's streams; with marks, record timing events at the decode-
+        step boundaries of the main stream as ("slow"|"fast", start, end)."""
+        import torch
+        dec = dec or self.dec
+
+        def mark():
+            ev = torch.cuda.Event(enable_timing=True, external=True)
+            ev.record(dec.main)
+            return ev
+        for t in range(self.cyc):
+            a = mark() if marks is not None else None
+            if t == 0:
+                dec.slow_step(self.ios[0], self.seq_steps[0])
+            else:
+                dec.fast_step(self.ios[t], self.seq_steps[t])
+            if marks is not None:
+                marks.append(("slow" if t == 0 else "fast", a, mark()))
+        dec.join()
+
+    def graph(self, fn):
+        import torch
+        with torch.cuda.stream(self.dec.main):
+            fn()
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=self.dec.main):
+            fn()
+        return g
+
+    def replay_ms(self, g, reps, warmup):
+        import torch
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(self.dec.main):
+            for _ in range(warmup):
+                g.replay()
+            e0.record(self.dec.main)
+            for _ in range(reps):
+                g.replay()
+            e1.record(self.dec.main)
+        torch.cuda.synchronize()
+        return e0.elapsed_time(e1) / reps
+
+    def step_durations(self, reps, warmup):
+        """Per-layer durations of the slow step and of each fast step (µs), from events at
+        the decode-step boundaries captured as graph nodes, read after the last replay."""
+        marks = []
+        g = self.graph(lambda: (marks.clear(), self.run(marks=marks)))
+        ms = self.replay_ms(g, reps, warmup)
+        dur = {"slow": [], "fast": []}
+        for kind, a, b in marks:
+            dur[kind].append(a.elapsed_time(b) * 1e3 / self.NL)
+        return dur, ms
+
+    def aux_alone_us(self, reps=5):
+        """The side stream's work of one slow step (Selector + compaction of every layer)
+        timed alone, as one graph on one stream, per layer."""
+        import sparse_kv_long_sfi_gb300 as sfi
+        d = self.dec
+
+        def aux():
+            for i, Lb in enumerate(self.layers):
+                kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, self.page_table, self.seq_steps[0])
+                sfi.sfi_select_compact(self.shape, kv, Lb.scores, self.S, self.W, self.batch.k_per_req, Lb.idx,
+                                       Lb.compact, stream=d.main)
+        g = self.graph(aux)
+        return self.replay_ms(g, reps, 2) * 1e3 / self.NL
+
+    def free(self):
+        import torch
+        del self.layers, self.dec, self.ios, self.q_all, self.kn_all, self.vn_all, self.out
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+
+
+def cycle_report(cy, dur, ms_cycle, peak):
+    """Amortised decode step and per-launch figures of a measured cycle."""
+    fast_wait = dur["fast"][:1]
+    fast_clean = dur["fast"][1:] or dur["fast"]
+    t_fast = statistics.mean(fast_clean)
+    t_first = statistics.mean(fast_wait)
+    t_slow = statistics.mean(dur["slow"])
+    gbps = lambda by, us: round(by / (us * 1e-6) / 1e9, 1)
+    return {"us_per_step": round(ms_cycle * 1e3 / cy.cyc, 3),
+            "tokens_per_s": round(cy.B * cy.cyc / (ms_cycle * 1e-3), 1),
+            "hbm_GBps_cycle": gbps(cy.by_cycle, ms_cycle * 1e3),
+            "frac_of_peak_cycle": round(cy.by_cycle / (ms_cycle * 1e-3) / 1e9 / peak, 3),
+            "bytes_per_cycle": cy.by_cycle,
+            "fast_us_per_launch": round(t_fast, 3), "fast_bytes_per_launch": cy.by_fast,
+            "fast_GBps": gbps(cy.by_fast, t_fast), "fast_frac_of_peak": round(cy.by_fast / (t_fast * 1e-6) / 1e9 / peak, 3),
+            "slow_us_per_launch": round(t_slow, 3), "slow_bytes_per_launch": cy.by_slow,
+            "slow_GBps": gbps(cy.by_slow, t_slow), "slow_frac_of_peak": round(cy.by_slow / (t_slow * 1e-6) / 1e9 / peak, 3),
+            "first_fast_step_us_per_layer": round(t_first, 3)}
+
+
+def overlap_report(cy, dur, ms_cycle, peak, reps):
+    """The side stream's overlap (SFI Figure 3 (A)): the same cycle with the Selector and
+    compaction issued on the main stream (serial) against the two-stream cycle, the side
+    work timed alone, and the first fast step's penalty against its HBM floor."""
+    import sparse_kv_long_sfi_gb300 as sfi
+    d = cy.dec
+    serial = sfi.SFIDecoder(cy.shape, cy.layers, cy.batch, cy.S, cy.W, max_len=cy.L0 + cy.cyc, device=cy.dev,
+                            main_stream=d.main, aux_stream=d.main, k_max=cy.k)
+    g = cy.graph(lambda: cy.run(dec=serial))
+    ms_serial = cy.replay_ms(g, reps, 2)
+    del g
+    aux_us = cy.aux_alone_us()
+    t_fast = statistics.mean(dur["fast"][1:] or dur["fast"])
+    t_first = statistics.mean(dur["fast"][:1])
+    floor_us = cy.by_aux / (peak * 1e3)  # the side work's own bytes at the measured copy bandwidth
+    saved = (ms_serial - ms_cycle) * 1e3 / cy.NL  # per layer of the slow step
+    return {"serial_cycle_ms": round(ms_serial, 4), "overlapped_cycle_ms": round(ms_cycle, 4),
+            "aux_alone_us_per_layer": round(aux_us, 3), "saved_us_per_layer": round(saved, 3),
+            "overlap_efficiency": round(saved / aux_us, 3) if aux_us > 0 else None,
+            "first_fast_step_us_per_layer": round(t_first, 3), "fast_step_us_per_layer": round(t_fast, 3),
+            "first_fast_step_ratio": round(t_first / t_fast, 3),
+            "aux_bytes_per_layer": cy.by_aux, "aux_hbm_floor_us_per_layer": round(floor_us, 3),
+            "first_fast_penalty_us_per_layer": round(t_first - t_fast, 3),
+            "penalty_over_floor": round((t_first - t_fast) / floor_us, 3),
+            "note": "efficiency = (serial - overlapped) / side work alone; the first fast step after a slow step "
+                    "waits for the side work layer by layer, and its extra time is compared with the side work's "
+                    "own HBM bytes (Selector reads, compaction reads and writes) at the measured copy bandwidth"}
+
+
 def run_gpu(args, ranks: Ranks):
-    import numpy as np
     import torch
 
     import __graft_entry__
     __graft_entry__.build()
-    import sfi_synth as syn
     import sparse_kv_long_sfi_gb300 as sfi
 
     dev = torch.device("cuda", ranks.local)
@@ -228,59 +413,23 @@ def run_gpu(args, ranks: Ranks):
     Hq, Hkv, D, P = WL["num_q_heads"], WL["num_kv_heads"], WL["head_dim"], WL["page_size"]
     NL, B, L0 = args.layers, args.batch, args.kv_len
     S, W, cyc = WL["sink"], WL["recent"], WL["refresh_interval"]
-    shape = sfi.AttnShape(Hq, Hkv, D, P)
-    k_main = syn.retention_budget(WL["retention"], L0, S, W)
-    k_cap = max(k_main, L0 - S - W)  # room for the 100% sweep point
     seed0 = 1000 + 97 * ranks.rank
+    sections = [] if args.no_sweep else args.sections
+    peak, peak_kind = measured_peaks()
 
-    # ---- requests: shuffled page table with room for the cycle's appends ----
-    g = syn.rng(seed0, 1)
-    table, num_pages = syn.make_page_table(g, [L0 + cyc] * B, P, shuffle=True)
-    page_table = torch.as_tensor(table).to(dev)
-    off, cap = sfi.compact_layout(shape, S, [k_cap] * B, device=dev)
-    batch = sfi.DecodeBatch(page_table, off, cap, torch.full((B,), k_main, dtype=torch.int32, device=dev), k_cap,
-                            score_stride=L0 + cyc)
-    seq_steps = torch.tensor([[L0 + t] * B for t in range(cyc)], dtype=torch.int32, device=dev)  # [cyc][B]
-
-    # ---- per-step inputs (all layers) ----
-    q_all = torch.empty((cyc, NL, B, Hq, D), dtype=torch.bfloat16, device=dev)
-    kn_all = torch.empty((cyc, NL, B, Hkv, D), dtype=torch.bfloat16, device=dev)
-    vn_all = torch.empty_like(kn_all)
-    syn.device_normal_bf16_(q_all, syn.stream_seed(seed0, 2))
-    syn.device_normal_bf16_(kn_all, syn.stream_seed(seed0, 3))
-    syn.device_normal_bf16_(vn_all, syn.stream_seed(seed0, 4))
-    out = torch.zeros((NL, B, Hq, D), dtype=torch.float32, device=dev)
-
-    def pool_init(i, kp, vp):
-        syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 10, i))
-        syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 11, i))
-        syn.device_plant_heavy_hitters_(kp, page_table, q_all[0, i], seq_steps[0], S, W, WL["heavy_hitter_frac"],
-                                        WL["heavy_hitter_beta"], syn.stream_seed(seed0, 12, i))
-
-    t_alloc = time.time()
-    layers = sfi.allocate_layers(shape, NL, num_pages, batch, S, device=dev, pool_init=pool_init)
-    torch.cuda.synchronize()
-    t_alloc = time.time() - t_alloc
-    dec = sfi.SFIDecoder(shape, layers, batch, S, W, max_len=L0 + cyc, device=dev, k_max=k_main)
-    ios = [sfi.StepIO(q_all[t], kn_all[t], vn_all[t], out) for t in range(cyc)]
-
-    def cycle():
-        dec.slow_step(ios[0], seq_steps[0])
-        for t in range(1, cyc):
-            dec.fast_step(ios[t], seq_steps[t])
-        dec.join()
+    # room in the compact buffers for the 100% point of the retention sweep
+    cy = Cycle(dev, seed0, Hq, Hkv, NL, B, L0, WL["retention"], cyc, D, P, S, W, heavy=True,
+               k_cap=(L0 - S - W) if "retention" in sections else None)
+    dec, k_main = cy.dec, cy.k
 
     # eager warm-up (sets kernel attributes; checks status)
     with torch.cuda.stream(dec.main):
-        cycle()
+        cy.run()
     torch.cuda.synchronize()
     assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
-    launches_per_cycle = NL * 3 + (cyc - 1) * NL  # slow + Selector + compaction, then fast (append fused)
 
     # headline graph: the cycle with no timing nodes
-    g_cycle = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_cycle, stream=dec.main):
-        cycle()
+    g_cycle = cy.graph(cy.run)
     with torch.cuda.stream(dec.main):
         for _ in range(args.warmup):
             g_cycle.replay()
@@ -305,88 +454,39 @@ def run_gpu(args, ranks: Ranks):
 
     # per-kernel averages: the same cycle with timing events (graph nodes) at the step
     # boundaries only; each step's main stream is NL back-to-back attention launches
-    step_marks = []
-
-    def cycle_marked():
-        def mark():
-            ev = torch.cuda.Event(enable_timing=True, external=True)
-            ev.record(dec.main)
-            return ev
-        a = mark()
-        dec.slow_step(ios[0], seq_steps[0])
-        b = mark()
-        step_marks.append(("slow", a, b))
-        for t in range(1, cyc):
-            a = mark()
-            dec.fast_step(ios[t], seq_steps[t])
-            b = mark()
-            step_marks.append(("fast", a, b))
-        dec.join()
-
-    g_marked = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_marked, stream=dec.main):
-        cycle_marked()
     reps = max(3, min(args.steps, 10))
-    m0, m1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    with torch.cuda.stream(dec.main):
-        for _ in range(args.warmup):
-            g_marked.replay()
-        m0.record(dec.main)
-        for _ in range(reps):
-            g_marked.replay()
-        m1.record(dec.main)
-    torch.cuda.synchronize()
-    ms_marked = m0.elapsed_time(m1) / reps
-    try:  # durations of the last replay
-        dur = {"slow": [], "fast": []}
-        for kind, a, b in step_marks:
-            dur[kind].append(a.elapsed_time(b) * 1e3 / NL)
+    try:
+        dur, ms_marked = cy.step_durations(reps, args.warmup)
         timing_method = (f"events at decode-step boundaries (graph nodes), {NL} back-to-back launches per step, "
                          f"last of {reps} replays after the headline region; the fast kernel's average over the "
                          f"{cyc - 2} fast steps that do not follow the slow step")
     except RuntimeError as exc:
-        dur = None
+        dur, ms_marked = None, None
         timing_method = f"unavailable: {exc}"
 
-    # ---- algorithmic bytes of one cycle ----
-    n_ret_fast = S + k_main + W  # per (request, KV head) at L > S + W
-    # per attention launch, the fused append included (read k_new/v_new, write the page slot)
-    by_fast = fast_bytes(B, Hq, Hkv, D, P, n_ret_fast, W) + append_bytes(B, Hkv, D)
-    by_slow = dense_bytes(B, Hq, Hkv, D, P, L0, scores=True) + append_bytes(B, Hkv, D)
-    nC = L0 - S - W
-    by_cycle = (NL * (by_slow + select_bytes(B, Hkv, nC, k_main) + compact_bytes(B, Hkv, D, S, k_main)) +
-                (cyc - 1) * NL * by_fast)
     us_step = ms_cycle * 1e3 / cyc
-    peak, peak_kind = measured_peaks()
-
     roofline = None
     if dur:
         # The first fast step after the slow step also waits, layer by layer, for the
-        # side stream's Selector and compaction (the slow step's attention leaves them no
-        # room to run beside it), so the fast kernel's own duration is taken from the
-        # other fast steps; the first one is reported on its own.
-        fast_wait = dur["fast"][:1]
-        fast_clean = dur["fast"][1:] or dur["fast"]
-        t_fast = statistics.mean(fast_clean) if fast_clean else 0.0
-        t_fast_first = statistics.mean(fast_wait) if fast_wait else 0.0
-        t_slow = statistics.mean(dur["slow"]) if dur["slow"] else 0.0
-        share_fast = (t_fast * (cyc - 2) + t_fast_first) * NL / (ms_marked * 1e3)
+        # side stream's Selector and compaction, so the fast kernel's own duration is
+        # taken from the other fast steps; the first one is reported on its own.
+        rep = cycle_report(cy, dur, ms_marked, peak)
+        t_fast, t_slow, t_first = rep["fast_us_per_launch"], rep["slow_us_per_launch"], rep["first_fast_step_us_per_layer"]
+        share_fast = (t_fast * (cyc - 2) + t_first) * NL / (ms_marked * 1e3)
         share_slow = t_slow * NL / (ms_marked * 1e3)
         if share_slow >= share_fast:
-            name, per, tl, sh = "attn_decode_kernel<128,dense,scores> (slow step)", by_slow, t_slow, share_slow
+            name, per, tl, sh = "attn_decode_kernel<128,dense,scores> (slow step)", cy.by_slow, t_slow, share_slow
         else:
-            name, per, tl, sh = "attn_decode_kernel<128,fast> (fast step)", by_fast, t_fast, share_fast
+            name, per, tl, sh = "attn_decode_kernel<128,fast> (fast step)", cy.by_fast, t_fast, share_fast
         ach = per / (tl * 1e-6) / 1e9
         roofline = {"bound": "hbm", "kernel": name, "achieved": round(ach, 1), "peak": peak, "unit": "GB/s",
-                    "frac": round(ach / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs",
-                    "traffic": profiled_traffic("fast" if "fast" in name else "slow"), "bytes_per_launch": per, "avg_launch_us": round(tl, 3),
-                    "time_share": round(sh, 4), "timing": timing_method,
-                    "other": {"fast_avg_us": round(t_fast, 3), "fast_GBps": round(by_fast / (t_fast * 1e-6) / 1e9, 1)
-                              if t_fast else None, "fast_share": round(share_fast, 4),
-                              "first_fast_step_us_per_layer": round(t_fast_first, 3),
+                    "frac": round(ach / peak, 4), "peak_kind": f"{peak_kind} hbm_gbs (burst copy)",
+                    "traffic": profiled_traffic("fast" if "fast" in name else "slow"), "bytes_per_launch": per,
+                    "avg_launch_us": round(tl, 3), "time_share": round(sh, 4), "timing": timing_method,
+                    "other": {"fast_avg_us": t_fast, "fast_GBps": rep["fast_GBps"], "fast_share": round(share_fast, 4),
+                              "first_fast_step_us_per_layer": t_first,
                               "first_fast_step_note": "waits for the side stream's Selector and compaction",
-                              "slow_avg_us": round(t_slow, 3), "slow_GBps": round(by_slow / (t_slow * 1e-6) / 1e9, 1)
-                              if t_slow else None, "slow_share": round(share_slow, 4)}}
+                              "slow_avg_us": t_slow, "slow_GBps": rep["slow_GBps"], "slow_share": round(share_slow, 4)}}
 
     result = {
         "metric": METRIC, "value": round(us_step, 3), "unit": UNIT, "n_gpus": ranks.world, "steps": args.steps,
@@ -394,34 +494,208 @@ def run_gpu(args, ranks: Ranks):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {**WL, "layers": NL, "batch": B, "kv_len": L0, "k": k_main,
                    "step": f"1 slow + {cyc - 1} fast decode steps x {NL} layers (one CUDA graph)",
-                   "l2": f"inputs larger than L2: {NL} distinct layers, {by_cycle / cyc / 1e9:.2f} GB per decode step",
+                   "l2": f"inputs larger than L2: {NL} distinct layers, {cy.by_cycle / cyc / 1e9:.2f} GB per decode step",
                    "parallelism": f"replicas x{ranks.world}"},
-        "us_per_step_with_step_timing_nodes": round(ms_marked * 1e3 / cyc, 3),
+        "us_per_step_with_step_timing_nodes": round(ms_marked * 1e3 / cyc, 3) if ms_marked else None,
         "tokens_per_s": round(ranks.world * B * cyc / (ms_cycle * 1e-3), 1),
-        "hbm_GBps_cycle": round(by_cycle / (ms_cycle * 1e-3) / 1e9, 1),
-        "bytes_per_cycle": by_cycle,
-        "gpu_launches": launches_per_cycle * args.steps,
+        "hbm_GBps_cycle": round(cy.by_cycle / (ms_cycle * 1e-3) / 1e9, 1),
+        "bytes_per_cycle": cy.by_cycle,
+        "gpu_launches": cy.launches_per_cycle * args.steps,
         "clocks": clk,
         "roofline": roofline,
-        "alloc_s": round(t_alloc, 1),
+        "alloc_s": round(cy.alloc_s, 1),
     }
 
     # ---- end to end through the public API with host buffers ----
-    result["e2e"] = e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks)
+    result["e2e"] = e2e_cycle(args, dec, cy.ios, cy.seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks)
 
-    # ---- retention sweep vs dense (Table 1) ----
-    sections = [] if args.no_sweep else args.sections
+    if "overlap" in sections and dur:
+        result["overlap"] = overlap_report(cy, dur, ms_cycle, peak, reps=max(3, min(args.steps, 5)))
     if "retention" in sections:
-        result["retention_sweep"] = retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps,
-                                                    NL, B, Hq, Hkv, D, P, L0, S, dev, peak)
+        result["retention_sweep"] = retention_sweep(cy, dev, peak)
     if "speculative" in sections:
-        result["speculative_sweep"] = speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv,
-                                                        D, P, L0, S, W, k_main, dev, peak, seed0)
+        result["speculative_sweep"] = speculative_sweep(dec, cy.layers, cy.batch, cy.shape, cy.q_all, cy.seq_steps,
+                                                        NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak, seed0)
+    cy.free()
+    del cy, dec, g_cycle
+    torch.cuda.empty_cache()
+    if "batch1" in sections:
+        result["batch1"] = batch_one(args, dev, peak, seed0)
+    if "qwen3_8b" in sections:
+        result["qwen3_8b_cycle"] = qwen3_8b_cycle(args, dev, peak, seed0)
     if "other" in sections:
         result["other_workloads"] = other_workloads(dev, peak, seed0)
     if "ragged" in sections:
         result["ragged_mixed_step"] = ragged_mixed_step(dev, peak, seed0, B=args.ragged_requests)
+    if "ragged_schedule" in sections:
+        result["ragged_schedule"] = ragged_schedule(dev, peak, seed0, B=args.ragged_requests)
     return result
+
+
+def batch_one(args, dev, peak, seed0):
+    """Config 2's other batch: the same Qwen3-0.6B cycle and Table 1 retention sweep at batch 1."""
+    import torch
+    reps = max(3, min(args.steps, 10))
+    cy = Cycle(dev, seed0 + 5, WL["num_q_heads"], WL["num_kv_heads"], args.layers, 1, args.kv_len, WL["retention"],
+               WL["refresh_interval"], heavy=True, k_cap=args.kv_len - WL["sink"] - WL["recent"])
+    with torch.cuda.stream(cy.dec.main):
+        cy.run()
+    torch.cuda.synchronize()
+    g = cy.graph(cy.run)
+    ms = cy.replay_ms(g, max(3, args.steps), args.warmup)
+    dur, _ = cy.step_durations(reps, 2)
+    rep = cycle_report(cy, dur, ms, peak)
+    rep["retention_sweep"] = retention_sweep(cy, dev, peak)
+    assert cy.dec.dev_status.item() == 0
+    cy.free()
+    return {"workload": f"qwen3-0.6b-attn kv{args.kv_len} b1 sfi-cycle, {args.layers} layers", **rep}
+
+
+def qwen3_8b_cycle(args, dev, peak, seed0, NL=36, B=32, L0=32768):
+    """The Qwen3-8B-shaped workload as stated: 32 Q / 8 KV heads, 36 layers, batch 32, KV
+    32K, fast steps at 6.25% retention with one slow step every 16 (its Selector and
+    compaction on the side stream, overlapped with the next layers), as one graph."""
+    import torch
+    free, total = torch.cuda.mem_get_info(dev)
+    need = 2 * NL * B * (L0 + 32) * 8 * 128 * 2 * 1.08
+    if need > free:
+        return {"skipped": f"needs about {need / 1e9:.0f} GB of device memory, {free / 1e9:.0f} GB free"}
+    reps = 3
+    cy = Cycle(dev, seed0 + 7, 32, 8, NL, B, L0, 0.0625, WL["refresh_interval"], heavy=False)
+    with torch.cuda.stream(cy.dec.main):
+        cy.run()
+    torch.cuda.synchronize()
+    g = cy.graph(cy.run)
+    ms = cy.replay_ms(g, reps, 1)
+    dur, _ = cy.step_durations(reps, 1)
+    rep = cycle_report(cy, dur, ms, peak)
+    del g
+    ov = overlap_report(cy, dur, ms, peak, reps=2)
+    assert cy.dec.dev_status.item() == 0
+    alloc = cy.alloc_s
+    kv_gb = 2 * NL * cy.layers[0].k_pool.numel() * 2 / 1e9
+    cy.free()
+    return {"workload": f"qwen3-8b-attn kv{L0} b{B} sfi-cycle, {NL} layers, k {cy.k}", "kv_GB": round(kv_gb, 1),
+            **rep, "overlap": ov, "alloc_s": round(alloc, 1),
+            "note": "one graph per refresh cycle (1 slow + 15 fast decode steps x 36 layers); amortised per decode "
+                    "step; Q/K/V N(0,1)"}
+
+
+def ragged_schedule(dev, peak, seed0, B=64, steps=64, p_boundary=0.06, interval=32):
+    """Config 5 as a schedule: B (64) requests with lengths log-uniform in [4096, 131072],
+    32 Q / 8 KV heads, shuffled pages, per-request retention from {3, 12.5, 25}%, and a
+    seeded boundary process (slow with p = 0.06 per token, forced every 32 steps, the first
+    step slow) run for `steps` decode steps of one layer. Each step is one attention
+    launch (fast and slow requests together) plus, for the slow requests, the Selector and
+    compaction on the side stream; k is fixed at each slow step from the request's
+    retention. The whole run is one graph."""
+    import numpy as np
+    import torch
+    import sfi_synth as syn
+    import sparse_kv_long_sfi_gb300 as sfi
+
+    Hq, Hkv, D, P, S, W = 32, 8, 128, 16, 64, 256
+    shape = sfi.AttnShape(Hq, Hkv, D, P)
+    g = syn.rng(seed0, 60)
+    lens = syn.log_uniform_lengths(g, B, 4096, 131072) - 1
+    ret = g.choice([0.03, 0.125, 0.25], size=B)
+    k_cap = max(syn.retention_budget(ret[r], int(lens[r]) + steps, S, W) for r in range(B))
+    caps = [syn.retention_budget(ret[r], int(lens[r]) + steps, S, W) for r in range(B)]
+    table, num_pages = syn.make_page_table(g, lens + steps + 1, P, shuffle=True)
+    pt = torch.as_tensor(table).to(dev)
+    off, cap = sfi.compact_layout(shape, S, caps, device=dev)
+    k_now = np.array([syn.retention_budget(ret[r], int(lens[r]) + 1, S, W) for r in range(B)], np.int32)
+    batch = sfi.DecodeBatch(pt, off, cap, torch.as_tensor(k_now).to(dev), k_cap,
+                            score_stride=int(lens.max()) + steps + 1)
+    lens_t = torch.as_tensor((lens + 1).astype(np.int32)).to(dev)
+
+    q = torch.empty((steps, 1, B, Hq, D), dtype=torch.bfloat16, device=dev)
+    kn = torch.empty((steps, 1, B, Hkv, D), dtype=torch.bfloat16, device=dev)
+    vn = torch.empty_like(kn)
+    for t_, tag in ((q, 61), (kn, 62), (vn, 63)):
+        syn.device_normal_bf16_(t_, syn.stream_seed(seed0, tag))
+
+    def init(i, kp, vp):
+        syn.device_normal_bf16_(kp, syn.stream_seed(seed0, 64))
+        syn.device_normal_bf16_(vp, syn.stream_seed(seed0, 65))
+        syn.device_plant_heavy_hitters_(kp, pt, q[0, 0], lens_t, S, W, WL["heavy_hitter_frac"],
+                                        WL["heavy_hitter_beta"], syn.stream_seed(seed0, 66))
+
+    layers = sfi.allocate_layers(shape, 1, num_pages, batch, S, device=dev, pool_init=init)
+    out = torch.zeros((1, B, Hq, D), dtype=torch.float32, device=dev)
+    dec = sfi.SFIDecoder(shape, layers, batch, S, W, max_len=int(lens.max()) + steps + 1, device=dev)
+    # the seeded schedule and every step's lengths, ids and k (precomputed on the host)
+    sched = sfi.SlowFastSchedule(B, interval)
+    draws = syn.boundary_draws(syn.rng(seed0, 67), steps, B, p_boundary)
+    plan = []
+    cur = lens.astype(np.int64).copy()
+    k_host = k_now.copy()
+    by_total = 0
+    for t in range(steps):
+        cur = cur + 1
+        m = sched.next(draws[t]).astype(bool)
+        for r in np.flatnonzero(m):
+            k_host[r] = syn.retention_budget(ret[r], int(cur[r]), S, W)
+        sid = torch.as_tensor(np.flatnonzero(m).astype(np.int32)).to(dev)
+        fid = torch.as_tensor(np.flatnonzero(~m).astype(np.int32)).to(dev)
+        plan.append((m, torch.as_tensor(cur.astype(np.int32)).to(dev), sid, fid,
+                     torch.as_tensor(k_host.copy()).to(dev)))
+        for r in np.flatnonzero(m):  # slow requests: dense + scores, then the side work
+            L = int(cur[r])
+            by_total += (dense_bytes(1, Hq, Hkv, D, P, L, scores=True) +
+                         select_bytes(1, Hkv, max(0, L - S - W), int(k_host[r])) +
+                         compact_bytes(1, Hkv, D, S, int(k_host[r])))
+    # fast-step bytes use the selection a request holds at that step (its last slow step's k)
+    held = np.zeros(B, np.int64)
+    by_fast_total = 0
+    for m, _, _, _, kt in plan:
+        k_t = kt.cpu().numpy()
+        held[m] = k_t[m]
+        for r in np.flatnonzero(~m):
+            by_fast_total += fast_bytes(1, Hq, Hkv, D, P, S + int(held[r]) + W, W)
+    by_total += by_fast_total + steps * append_bytes(B, Hkv, D)
+
+    def run():
+        for t, (m, seq, sid, fid, kt) in enumerate(plan):
+            dec.batch.k_per_req = kt
+            io = sfi.StepIO(q[t], kn[t], vn[t], out)
+            if m.all():
+                dec.slow_step(io, seq)
+            elif not m.any():
+                dec.fast_step(io, seq)
+            else:
+                dec.mixed_step(io, seq, sid, fid)
+        dec.join()
+
+    with torch.cuda.stream(dec.main):
+        run()
+    torch.cuda.synchronize()
+    assert dec.dev_status.item() == 0, f"device status {dec.dev_status.item()}"
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=dec.main):
+        run()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = 5
+    with torch.cuda.stream(dec.main):
+        gr.replay()
+        e0.record(dec.main)
+        for _ in range(reps):
+            gr.replay()
+        e1.record(dec.main)
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / reps
+    n_slow = [int(x[0].sum()) for x in plan]
+    del gr, layers, dec, q, kn, vn, out
+    torch.cuda.empty_cache()
+    return {"workload": f"ragged {B} requests, kv 4K-128K log-uniform, 32q/8kv heads, retention {{3,12.5,25}}%, "
+                        f"boundary p={p_boundary}, refresh forced every {interval} steps, {steps} steps, 1 layer",
+            "steps": steps, "total_kv_tokens": int(lens.sum()), "us_per_step": round(ms * 1e3 / steps, 2),
+            "bytes_per_run": by_total, "GBps": round(by_total / (ms * 1e-3) / 1e9, 1),
+            "frac_of_peak": round(by_total / (ms * 1e-3) / 1e9 / peak, 3),
+            "slow_requests_per_step_mean": round(float(np.mean(n_slow)), 2),
+            "slow_requests_first_step": n_slow[0], "slow_requests_max_after_first": max(n_slow[1:]) if steps > 1 else 0,
+            "note": "one graph of all steps; each step: one mixed attention launch (append fused) + Selector and "
+                    "compaction of its slow requests on the side stream; bytes include the side work"}
 
 
 def e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks):
@@ -492,34 +766,21 @@ def e2e_cycle(args, dec, ios, seq_steps, cyc, NL, B, Hq, Hkv, D, dev, ranks):
             "steps": n, "path": "SFIDecoder (libsfi C ABI), pinned host inputs/outputs copied on a side stream, one graph per cycle"}
 
 
-def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_steps, NL, B, Hq, Hkv, D, P, L0, S,
-                    dev, peak):
+def retention_sweep(cy, dev, peak):
     """Fast decode steps (all layers) at Table 1's retention points vs the dense decode kernel."""
     import torch
-    import sfi_synth as syn
     import sparse_kv_long_sfi_gb300 as sfi
 
     reps = 20
+    dec, layers, batch, shape = cy.dec, cy.layers, cy.batch, cy.shape
+    NL, B, Hq, Hkv, D, P, L0, S = cy.NL, cy.B, cy.Hq, cy.Hkv, cy.D, cy.P, cy.L0, cy.S
+    q_all, kn_all, vn_all, out, seq_steps = cy.q_all, cy.kn_all, cy.vn_all, cy.out, cy.seq_steps
     L1 = L0 + 1
     seq = seq_steps[1]
 
     def time_graph(fn):
-        with torch.cuda.stream(dec.main):
-            fn()
-        torch.cuda.synchronize()
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g, stream=dec.main):
-            fn()
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        with torch.cuda.stream(dec.main):
-            for _ in range(3):
-                g.replay()
-            e0.record(dec.main)
-            for _ in range(reps):
-                g.replay()
-            e1.record(dec.main)
-        torch.cuda.synchronize()
-        return e0.elapsed_time(e1) * 1e3 / reps
+        g = cy.graph(fn)
+        return cy.replay_ms(g, reps, 3) * 1e3
 
     ws_dense = dec.ws_dense
 
@@ -563,10 +824,10 @@ def retention_sweep(dec, layers, batch, shape, q_all, kn_all, vn_all, out, seq_s
                      "speedup_vs_dense": round(us_dense / us, 3), "table1_speedup_context": TABLE1[n]})
     # restore the main cycle's selection state
     dec.pending = [False] * len(layers)
-    return {"dense_us_per_step": round(us_dense, 2),
+    return {"batch": B, "dense_us_per_step": round(us_dense, 2),
             "dense_GBps": round(NL * by_dense / (us_dense * 1e-6) / 1e9, 1),
             "dense_frac_of_peak": round(NL * by_dense / (us_dense * 1e-6) / 1e9 / peak, 3),
-            "points": rows, "note": "fast and dense steps include the (fused) paged append; 28 layers per step; "
+            "points": rows, "note": f"fast and dense steps include the (fused) paged append; {NL} layers per step; "
                                     "Table 1 speedups are the paper's (hardware unstated), context only"}
 
 
@@ -660,8 +921,6 @@ def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hk
 
 
 OTHER_WORKLOADS = [
-    dict(workload="qwen3-8b-attn kv32k b32", num_q_heads=32, num_kv_heads=8, kv_len=32768, batch=32,
-         retention=0.0625, fast=True),
     dict(workload="64q/8kv-heads kv64k b8 top-4096", num_q_heads=64, num_kv_heads=8, kv_len=65536, batch=8, k=4096,
          fast=False),
 ]
@@ -907,6 +1166,26 @@ def ragged_mixed_step(dev, peak, seed0, reps=20, n_slow=5, B=64):
 _SAMPLE = {}
 
 
+def host_cpu():
+    """(logical CPUs of this host, CPU model name) from os and /proc/cpuinfo."""
+    model = "unknown"
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":", 1)[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware") and ":" in line:
+                    model = line.split(":", 1)[1].strip()
+                    break
+        if model == "unknown":  # Arm hosts: no model name line; report the part number
+            with open("/proc/cpuinfo") as f:
+                parts = {line.split(":", 1)[1].strip() for line in f if line.lower().startswith("cpu part")}
+            if parts:
+                model = "Arm CPU part " + "/".join(sorted(parts))
+    except OSError:
+        pass
+    return os.cpu_count() or 1, model
+
+
 def oracle_sample_us_per_step(min_seconds: float, layers: int, batch: int, kv_len: int):
     """Time the CPU oracle on a bounded sample of the workload and scale it.
 
@@ -914,7 +1193,8 @@ def oracle_sample_us_per_step(min_seconds: float, layers: int, batch: int, kv_le
     heads are independent and cost the same), one refresh cycle's work: a slow step
     (dense attention + masked scores + Selector + compaction) and a fast step. Scaled
     by 4 for the heads, by batch x layers, and to a decode step as
-    (slow + (cycle - 1) * fast) / cycle."""
+    (slow + (cycle - 1) * fast) / cycle. Returns a dict with the scaled value, the
+    measured sample times and the scale factor, so the figure can be reproduced."""
     import numpy as np
     import oracle
     import sfi_synth as syn
@@ -948,35 +1228,57 @@ def oracle_sample_us_per_step(min_seconds: float, layers: int, batch: int, kv_le
         if time.perf_counter() - t_begin >= min_seconds:
             break
     head_scale = Hkv_all / Hkv
-    per_req_layer_cycle = (t_slow + (cyc - 1) * t_fast) / n * head_scale
-    us_step = per_req_layer_cycle / cyc * batch * layers * 1e6
+    slow_s, fast_s = t_slow / n, t_fast / n
+    sample_s = (slow_s + (cyc - 1) * fast_s) / cyc  # one decode step of the sample (1 request, 1 layer, 2 heads)
+    factor = head_scale * batch * layers
+    us_step = sample_s * factor * 1e6
+    nproc, model = host_cpu()
     sample = (f"{n} x (one slow step: dense + scores + Selector + compaction, and one fast step) of one request, "
               f"one layer, {Hkv} of {Hkv_all} KV heads ({Hq} of {Hq_all} query heads), L={L0}; scaled x{head_scale:g} "
               f"heads x{batch} requests x{layers} layers, (slow + {cyc - 1} fast)/{cyc} per decode step")
-    return us_step, sample, time.perf_counter() - t_begin
+    return {"value": us_step, "sample": sample, "wall_s": time.perf_counter() - t_begin,
+            "sample_slow_step_s": round(slow_s, 6), "sample_fast_step_s": round(fast_s, 6),
+            "sample_decode_step_us": round(sample_s * 1e6, 3), "extrapolation_factor": factor,
+            "extrapolation": f"value = sample_decode_step_us x {factor:g} ({head_scale:g} heads x {batch} requests "
+                             f"x {layers} layers)",
+            "cores": 1, "host_cpus": nproc, "cpu_model": model,
+            "cores_note": f"1 core used of {nproc} ({model}); the oracle is single-threaded"}
+
+
+def cpu_baseline_entry(r, extra=""):
+    return {"value": round(r["value"], 1), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": r["sample"] + extra, "host_cpus": r["host_cpus"], "cpu_model": r["cpu_model"],
+            "cores_note": r["cores_note"], "sample_decode_step_us": r["sample_decode_step_us"],
+            "sample_slow_step_s": r["sample_slow_step_s"], "sample_fast_step_s": r["sample_fast_step_s"],
+            "extrapolation_factor": r["extrapolation_factor"], "extrapolation": r["extrapolation"]}
 
 
 def run_reference(args, ranks: Ranks):
     if ranks.rank != 0:
         return None
     times = []
-    sample = ""
+    last = None
     for _ in range(args.warmup):
         oracle_sample_us_per_step(0.0, args.layers, args.batch, args.kv_len)
     t_all = time.perf_counter()
     for _ in range(args.steps):
-        us, sample, _ = oracle_sample_us_per_step(0.0, args.layers, args.batch, args.kv_len)
-        times.append(us)
+        last = oracle_sample_us_per_step(0.0, args.layers, args.batch, args.kv_len)
+        times.append(last["value"])
     wall = time.perf_counter() - t_all
     us = statistics.mean(times)
+    cpu = cpu_baseline_entry({**last, "value": us},
+                             f"; one sample per step, {wall:.1f} s wall for {args.steps} steps")
     return {
         "impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT, "n_gpus": ranks.world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(us * WL["refresh_interval"] / 1e3, 3),
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(wall / max(1, args.steps) * 1e3, 3),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": {**WL, "layers": args.layers, "batch": args.batch, "kv_len": args.kv_len,
                    "parallelism": "rank 0 only"},
-        "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                         "sample": sample + f"; one sample per step, {wall:.1f} s wall for {args.steps} steps"},
+        "timed_region_note": (f"one step of this arm is one bounded sample of the workload, timed on the host "
+                              f"({wall:.1f} s of wall time for {args.steps} steps; ms_per_step is that wall time per "
+                              f"step); value extrapolates the sample by {last['extrapolation_factor']:g} to the "
+                              f"time of one full decode step"),
+        "cpu_baseline": cpu,
         "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
 
@@ -990,9 +1292,8 @@ def main():
         else:
             res = run_gpu(args, ranks)
             if res is not None and ranks.rank == 0 and ranks.world == 1 and not args.no_cpu:
-                us, sample, secs = oracle_sample_us_per_step(12.0, args.layers, args.batch, args.kv_len)
-                res["cpu_baseline"] = {"value": round(us, 1), "unit": UNIT, "cores": 1, "kind": "oracle",
-                                       "sample": sample + f"; {secs:.1f} s of CPU time"}
+                r = oracle_sample_us_per_step(12.0, args.layers, args.batch, args.kv_len)
+                res["cpu_baseline"] = cpu_baseline_entry(r, f"; {r['wall_s']:.1f} s of CPU time")
         if res is not None and ranks.rank == 0:
             print(json.dumps(res), flush=True)
     finally:

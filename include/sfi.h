@@ -39,6 +39,10 @@
  *     SFI_ERR_CUDA.
  *   - Device-side errors never trap: the kernel ORs an SFI_DEV_* bit into
  *     *dev_status (optional; may be NULL) and skips the offending unit's writes.
+ *     In the attention calls the unit is a (request, KV head): when any of its
+ *     page ids is out of range, or one of its waits runs out, none of its outputs,
+ *     log-sum-exps or score entries is written (the caller's values stay), in every
+ *     split plan; other units are unaffected.
  *   - Per-request arrays (q, out, lse, scores, seq_lens, page_table rows,
  *     k_per_req, counts, compact rows) are indexed by the request id r. An entry
  *     point processes `batch` requests: r = req_ids[b] when req_ids is non-NULL
@@ -102,9 +106,9 @@ typedef enum {
 /* SFI_ATTN_TEST_WITHHOLD (the same two calls; diagnostic, for testing the bounded
  * in-kernel waits): the TMA producer of every CTA withholds the copies of its second
  * stage, so the consumers' wait for it runs out (after about 2 s) and the launch
- * reports SFI_DEV_TIMEOUT; the outputs are then unspecified, the workspace must be
- * zeroed again, and the context stays usable. Units shorter than two stages are
- * unaffected. Not for production use. */
+ * reports SFI_DEV_TIMEOUT; the affected units write no output, the workspace is
+ * left zeroed as after any launch, and the context stays usable. Units shorter than
+ * two stages are unaffected. Not for production use. */
 #define SFI_ATTN_TEST_WITHHOLD 4u
 
 /* Most query tokens per request in the multi-token calls (tokens x G must also be
@@ -180,9 +184,10 @@ SFI_API sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_pa
  *                SFI_ATTN_TEST_WITHHOLD).
  *   workspace  : at least sfi_workspace_size(shape, batch, max_tokens, num_splits)
  *                bytes of device memory, zero-filled before its first use. The
- *                kernels leave it zero-filled again when they finish without a
- *                device error; after SFI_DEV_TIMEOUT zero it again. Launches
- *                that share one workspace must not overlap in time.
+ *                kernels leave its split counters zero-filled again when they
+ *                finish, device errors and timed-out waits included (every split
+ *                of a unit reaches the counter). Launches that share one
+ *                workspace must not overlap in time.
  * Device errors: SFI_DEV_BAD_LEN, SFI_DEV_BAD_PAGE, SFI_DEV_K_OVERFLOW,
  * SFI_DEV_BAD_COMPACT, SFI_DEV_TIMEOUT.
  */
@@ -393,13 +398,19 @@ SFI_API sfi_status sfi_select_compact(const sfi_attn_shape *shape, const sfi_pag
  *   - Its first call on a device looks up the array's device address on that device
  *     (cudaGetSymbolAddress, with that device current); make that first call before
  *     any stream capture.
+ *   - The looked-up address is kept for the life of the process: a device reset
+ *     (cudaDeviceReset) after the first call on a device is not supported.
  *   - Returns SFI_ERR_WORKSPACE when the split plan for these arguments needs more
- *     than SFI_NOALLOC_SCRATCH_BYTES (sfi_workspace_size tells the need); reduce
- *     num_splits or the batch per call.
+ *     than SFI_NOALLOC_SCRATCH_BYTES (sfi_workspace_size tells the need, or
+ *     sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0) with SFI_ATTN_RAGGED);
+ *     reduce num_splits or the batch per call.
  *   - All calls on a device share the one array, which keeps what the last call left
- *     in it; each call zeroes the split counters it needs (an async memset on
- *     `stream`) before its kernel. Calls whose work can overlap on the GPU (for
- *     example on two streams) race on the array: order them on one stream.
+ *     in it. A call whose plan uses the array (more than 8 splits, or any chunked
+ *     plan of more than one chunk under SFI_ATTN_RAGGED) first zeroes its split
+ *     counters with an async memset on `stream`; a plan that merges inside a
+ *     thread-block cluster uses no scratch and issues no memset. Calls whose work can
+ *     overlap on the GPU (for example on two streams) race on the array: order them
+ *     on one stream.
  * Arguments, results and device errors are those of sfi_fast_decode_attn.
  */
 #define SFI_NOALLOC_SCRATCH_BYTES (4u << 20)

@@ -64,10 +64,46 @@ struct AttnTile {
 };
 
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
+// Stages between a unit's TMA copies and its rolling L2 prefetch (deep_prefetch).
+constexpr int kDeepPrefetch = 8;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void consumer_bar_sync() {
     asm volatile("bar.sync 1, %0;" ::"n"(kConsumerWarps * 32) : "memory");
+}
+
+// Barrier over the consumer threads that also returns whether any of them passed true.
+__device__ __forceinline__ bool consumer_bar_or(bool v) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 q, %1, 0;\n\t"
+        "bar.red.or.pred p, 1, %2, q;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(r)
+        : "r"((uint32_t)v), "n"(kConsumerWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Whether any page id of positions [0, L) of request r lies outside the pool. Called by
+// every consumer thread before the first score write of a unit, so a unit with a bad
+// page writes none of its scores (the pages are checked again as they are streamed).
+__device__ __forceinline__ bool request_pages_bad(const AttnParams &p, int r, int L) {
+    const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+    const int npg = (L + kSubTokens - 1) / kSubTokens;
+    bool bad = false;
+    for (int i0 = threadIdx.x; i0 < npg; i0 += 8 * kConsumerWarps * 32) {
+        int pg[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {  // eight independent loads in flight
+            const int i = i0 + j * kConsumerWarps * 32;
+            pg[j] = i < npg ? __ldg(ptab + i) : 0;
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) bad |= pg[j] < 0 || pg[j] >= p.num_pages;
+    }
+    return consumer_bar_or(bad);
 }
 
 // Geometry of one (request, KV head) unit's token stream.
@@ -152,11 +188,11 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
     const int g = lane >> 2, t = lane & 3;
     const int mi = lane >> 3, r8 = lane & 7;
 
-    // S = Q K^T for 16 tokens: two n-tiles (tokens 0-7 and 8-15), each accumulated in
-    // two independent chains (even and odd k-steps) to halve the mma dependency depth.
+    // S = Q K^T for 16 tokens: two n-tiles (tokens 0-7 and 8-15), one accumulation chain
+    // each. (Splitting each into even and odd k-steps was measured: no change, and it
+    // made the kernel spill.)
     float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
-        float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
         const int tok = ((mi >> 1) << 3) + r8;
         const uint32_t row_addr = kaddr + tok * 128;
 #pragma unroll
@@ -167,11 +203,6 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
             ldsm_x4(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
             mma_bf16_16816(s[0], qa[ks][0], 0u, qa[ks][1], 0u, b0, b1);
             mma_bf16_16816(s[1], qa[ks][0], 0u, qa[ks][1], 0u, b2, b3);
-        }
-#pragma unroll
-        for (int n = 0; n < 2; ++n) {
-            s[n][0] += s2[n][0];
-            s[n][1] += s2[n][1];
         }
     }
     const int tk0 = 2 * t, tk1 = 2 * t + 1, tk2 = 8 + 2 * t, tk3 = 9 + 2 * t;
@@ -271,7 +302,7 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
 // tile and are written to the page (k_new/v_new: [request][T][Hkv][D]).
 template <int D>
 __device__ __forceinline__ void fuse_tokens(uint8_t *tile, const AttnParams &p, int r, int kvh, int L, int pos0,
-                                            int lane) {
+                                            int lane, int *s_bad) {
     using T = AttnTile<D>;
     constexpr int kChunks = D / 8;
     const int ntok = p.tokens;
@@ -294,7 +325,10 @@ __device__ __forceinline__ void fuse_tokens(uint8_t *tile, const AttnParams &p, 
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
-    if (!page_ok && lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
+    if (!page_ok && lane == 0) {
+        report(p.dev_status, SFI_DEV_BAD_PAGE);
+        *s_bad = 1;  // the unit writes no output
+    }
     __syncwarp();
 }
 
@@ -524,7 +558,7 @@ __device__ __forceinline__ void stage_current_token(const AttnParams &p, int r, 
 template <int D>
 __device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
                                                    const UnitStream &u, int lane, const int4 *s_val,
-                                                   const int *s_page) {
+                                                   const int *s_page, int *s_bad) {
     using T = AttnTile<D>;
     constexpr int kChunks = D / 8;
     // the copies issued by stage_current_token have landed (each lane waits for its own)
@@ -540,7 +574,10 @@ __device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnPara
         const int pos = u.L - 1;
         const int page = *s_page;
         if (page < 0 || page >= p.num_pages) {
-            if (lane == 0) report(p.dev_status, SFI_DEV_BAD_PAGE);
+            if (lane == 0) {
+                report(p.dev_status, SFI_DEV_BAD_PAGE);
+                *s_bad = 1;  // the unit writes no output
+            }
         } else {
             __nv_bfloat16 *dst = (is_v ? p.v_pool_w : p.k_pool_w) +
                                  (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D + c * 8;
@@ -569,10 +606,13 @@ __host__ __device__ constexpr bool cluster_push_fits(int splits, int rows, int r
 // partial is complete: in cp_o [rows][D], cp_m, cp_l (shared memory) when the unit's
 // splits form a cluster, in workspace slot (slot0 + split) otherwise. recv is the
 // receive region (recv_bytes) where the other CTAs of a cluster push their partials.
+// A partial with l < 0 comes from a split that must not write (a bad page id or a
+// timed-out wait): the merge then writes nothing for the unit.
 template <int D, int kRows, bool CLUSTER, typename OutRow>
 __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, int recv_bytes, uint64_t *merge_bar,
                                              int *s_last, float *cp_o, float *cp_m, float *cp_l, int rows, int splits,
-                                             int split, int64_t unit, int64_t slot0, bool ok, OutRow out_row) {
+                                             int split, int64_t unit, int64_t slot0, float *stage, int stage_bytes,
+                                             OutRow out_row) {
     const int ctid = threadIdx.x;  // 0 .. 127
     if (CLUSTER && cluster_push_fits<D>(splits, rows, recv_bytes)) {
         // ---- split merge inside the cluster: the other CTAs push their partials into
@@ -599,7 +639,6 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
             if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
             return;
         }
-        if (!ok) return;
         for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
             const int row = (2 * e2) / D, d = 2 * e2 - row * D;
             float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
@@ -617,9 +656,14 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
                 }
             }
             float M = -INFINITY;
+            bool fail = false;
 #pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s)
-                if (s < splits) M = fmaxf(M, ms[s]);
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s < splits) {
+                    M = fmaxf(M, ms[s]);
+                    fail |= ls[s] < 0.f;
+                }
+            }
             float ax = 0.f, ay = 0.f, lsum = 0.f;
 #pragma unroll
             for (int s = 0; s < kMaxClusterSplits; ++s) {
@@ -630,6 +674,7 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
                     lsum += ls[s] * f;
                 }
             }
+            if (fail) continue;
             *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
             if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
         }
@@ -650,7 +695,7 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
         }
         if (ctid == 0) *s_last = mbar_wait_cluster_bounded(merge_bar, 0) ? 1 : 0;
         consumer_bar_sync();
-        if (*s_last && ok) {
+        if (*s_last) {
             // Each thread merges pairs of outputs. All loads from the peers' shared
             // memory are issued before any is used, so their latencies overlap.
             for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
@@ -666,9 +711,14 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
                     }
                 }
                 float M = -INFINITY;
+                bool fail = false;
 #pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s)
-                    if (s < splits) M = fmaxf(M, ms[s]);
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < splits) {
+                        M = fmaxf(M, ms[s]);
+                        fail |= ls[s] < 0.f;
+                    }
+                }
                 float ax = 0.f, ay = 0.f, lsum = 0.f;
 #pragma unroll
                 for (int s = 0; s < kMaxClusterSplits; ++s) {
@@ -679,6 +729,7 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
                         lsum += ls[s] * f;
                     }
                 }
+                if (fail) continue;
                 *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
                 if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
             }
@@ -690,7 +741,9 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
     }
 
     // ---- split merge by the last CTA of this unit, through the global workspace ----
-    if (!ok) return;
+    // Every split arrives (a failed one with l = -1), so the counter always completes and
+    // the last CTA leaves it zeroed for the next launch.
+    asm volatile("fence.proxy.async.global;" ::: "memory");  // this thread's partial, for the bulk copies below
     __threadfence();
     consumer_bar_sync();
     if (ctid == 0) {
@@ -700,26 +753,86 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
     consumer_bar_sync();
     if (!*s_last) return;
     __threadfence();
-    for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
-        const int row = e / D, d = e - (e / D) * D;
-        float M = -INFINITY;
-#pragma unroll 8
-        for (int s = 0; s < splits; ++s) M = fmaxf(M, __ldcg(&p.ws_ml[((slot0 + s) * kRows + row) * 2]));
-        float acc = 0.f, lsum = 0.f;
-#pragma unroll 8
-        for (int s = 0; s < splits; ++s) {
-            const int64_t slot = (slot0 + s) * kRows + row;
-            const float ls = __ldcg(&p.ws_ml[slot * 2 + 1]);
-            if (ls > 0.f) {
-                const float f = fast_exp2(__ldcg(&p.ws_ml[slot * 2]) - M);
-                acc += __ldcg(&p.ws_part[slot * D + d]) * f;
-                lsum += ls * f;
+    // The unit's partials come into shared memory (`stage`, the ring: free once this CTA's
+    // own partial is in the workspace) by bulk copies, in batches of whole splits: the
+    // (m, l) block of the batch, then each split's rows x D partial output. Each thread
+    // merges its 4-float output chunks online over the staged splits (running max and
+    // normaliser per chunk), so the whole merge costs a few round trips.
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of the ring
+    consumer_bar_sync();
+    if (ctid == 0) {
+        p.ws_count[unit] = 0;
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+    }
+    constexpr int kC = D / 4;  // 4-float chunks per row
+    constexpr int kCpt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    const int o_floats = rows * D;
+    const int nbmax = stage_bytes / (kRows * 2 * 4 + o_floats * 4);
+    float *ml_st = stage;                        // [nbmax][kRows][2]
+    float *o_st = stage + nbmax * kRows * 2;     // [nbmax][rows][D]
+    float4 acc[kCpt];
+    float Mr[kCpt], Lr[kCpt];
+    int crow[kCpt], cd[kCpt];
+#pragma unroll
+    for (int j = 0; j < kCpt; ++j) {
+        const int c = ctid + j * kConsumerWarps * 32;
+        crow[j] = c < rows * kC ? c / kC : -1;
+        cd[j] = (c - (c / kC) * kC) * 4;
+        acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        Mr[j] = -INFINITY;
+        Lr[j] = 0.f;
+    }
+    bool fail = false;
+    for (int b0 = 0, batch = 0; b0 < splits; b0 += nbmax, ++batch) {
+        const int nbt = min(nbmax, splits - b0);
+        if (ctid == 0) {
+            const uint32_t ml_bytes = (uint32_t)(nbt * kRows * 2 * 4), o_bytes = (uint32_t)(o_floats * 4);
+            mbar_arrive_expect_tx(merge_bar, ml_bytes + (uint32_t)nbt * o_bytes);
+            bulk_load_1d(ml_st, &p.ws_ml[(slot0 + b0) * kRows * 2], ml_bytes, merge_bar);
+            for (int i = 0; i < nbt; ++i)
+                bulk_load_1d(o_st + i * o_floats, &p.ws_part[(slot0 + b0 + i) * kRows * D], o_bytes, merge_bar);
+        }
+        const bool got = mbar_wait_warp(merge_bar, batch & 1);
+        if (!got && (ctid & 31) == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+        for (int i = 0; i < nbt && got; ++i) {
+#pragma unroll
+            for (int j = 0; j < kCpt; ++j) {
+                if (crow[j] < 0) continue;
+                const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + crow[j]) * 2]);
+                fail |= ml.y < 0.f;
+                if (ml.y > 0.f) {
+                    const float4 o = *reinterpret_cast<const float4 *>(&o_st[i * o_floats + crow[j] * D + cd[j]]);
+                    const float Mn = fmaxf(Mr[j], ml.x);
+                    const float a = Lr[j] > 0.f ? fast_exp2(Mr[j] - Mn) : 0.f;
+                    const float f = fast_exp2(ml.x - Mn);
+                    acc[j].x = acc[j].x * a + o.x * f;
+                    acc[j].y = acc[j].y * a + o.y * f;
+                    acc[j].z = acc[j].z * a + o.z * f;
+                    acc[j].w = acc[j].w * a + o.w * f;
+                    Lr[j] = Lr[j] * a + ml.y * f;
+                    Mr[j] = Mn;
+                }
             }
         }
-        p.out[out_row(row) * D + d] = acc / lsum;
-        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+        // every thread is done with this batch before the next overwrites it; a wait that
+        // ran out in any warp ends the merge for all of them
+        if (consumer_bar_or(!got)) {
+            fail = true;
+            break;
+        }
     }
-    if (ctid == 0) p.ws_count[unit] = 0;  // leave the workspace zeroed for the next launch
+    // A failed split fails every row of the unit; make the decision CTA-wide.
+    fail = consumer_bar_or(fail);
+    if (fail) return;
+#pragma unroll
+    for (int j = 0; j < kCpt; ++j) {
+        if (crow[j] < 0) continue;
+        const float lsum = Lr[j];
+        float *dst = &p.out[out_row(crow[j]) * D + cd[j]];
+        *reinterpret_cast<float2 *>(dst) = make_float2(acc[j].x / lsum, acc[j].y / lsum);
+        *reinterpret_cast<float2 *>(dst + 2) = make_float2(acc[j].z / lsum, acc[j].w / lsum);
+        if (cd[j] == 0 && p.lse) p.lse[out_row(crow[j])] = (Mr[j] + log2f(lsum)) * kLn2;
+    }
 }
 
 // MQ: p.tokens query tokens per request (rows = tokens x G <= 16), no fused append.
@@ -734,10 +847,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[T::kStages];
     __shared__ __align__(8) uint64_t empty_bar[T::kStages];
-    __shared__ __align__(8) uint64_t merge_bar;  // cluster merge handshake
+    __shared__ __align__(8) uint64_t merge_bar;  // cluster merge handshake, or the workspace merge's copies
     __shared__ int2 s_info[T::kStages][kConsumerWarps];
     __shared__ int s_last;
     __shared__ int s_timeout;
+    __shared__ int s_bad;  // a page id of this unit is out of range: the unit writes no output
     __shared__ __align__(16) int4 s_app_val[32];  // the current token's K/V chunks (fused append)
     __shared__ int s_app_page;
 
@@ -814,13 +928,17 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             mbar_init(&full_bar[i], kConsumerWarps);
             mbar_init(&empty_bar[i], kConsumerWarps);
         }
-        // push merge: every consumer thread of every other CTA arrives once at rank 0
+        // push merge: every consumer thread of every other CTA arrives once at rank 0;
+        // workspace merge: the last CTA's bulk copies of the unit's partials
         if (CLUSTER)
             mbar_init(&merge_bar, split != 0 ? 1u
                                   : cluster_push_fits<D>(splits, MQ ? p.rows : p.group)
                                       ? (uint32_t)(splits - 1) * kConsumerWarps * 32
                                       : (uint32_t)(splits - 1));
+        else
+            mbar_init(&merge_bar, 1u);
         s_timeout = 0;
+        s_bad = 0;
         fence_barrier_init();
     }
     // Every CTA of a cluster reaches this point unconditionally (the only branch
@@ -838,17 +956,30 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             if (sb >= sb_end || sb < u.nb1) return -1;
             return ptab[u.page0 + (sb - u.nb1)];
         };
+        // page ids of the current chunk of 32 sub-blocks and of the next two (the rolling
+        // prefetch reads one chunk ahead; loading two ahead keeps it off the load latency)
         int cur = page_of(sb_begin + lane);
         int nxt = page_of(sb_begin + 32 + lane);
-        if (!fast) {
-            // Dense units: L2 prefetch of the stages after the ring's first fill (the rest
-            // of the first chunk of 32 sub-blocks), so the first refills read L2. (Measured:
-            // it shortens the slow step; on short fast-step units it costs more than it saves.)
-            const int page_all = cur;
-            for (int pst = T::kStages; pst < 8 && pst < n_stages; ++pst) {
-                const int page = __shfl_sync(0xffffffffu, page_all, (pst * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
-                const int sb = sb_begin + pst * kConsumerWarps + lane;
-                if (lane < kConsumerWarps && sb < sb_end && page >= 0 && page < p.num_pages) {
+        int nxt2 = page_of(sb_begin + 64 + lane);
+        // L2 prefetch of stage pst's sub-blocks (page ids of its chunk of 32 in page_src;
+        // warp-collective). Dense units prefetch the rest of their first chunk right after
+        // the ring's first fill, so the first refills read L2 without delaying the ring's
+        // own copies (measured: it shortens the slow step; on short fast-step units it
+        // costs more than it saves). With deep_prefetch (launches of at most one CTA per
+        // SM, whose own ring keeps too few bytes in flight) every unit also prefetches a
+        // rolling window kDeepPrefetch stages ahead of its copies.
+        auto prefetch_stage = [&](int pst, int page_src) {
+            const int page = __shfl_sync(0xffffffffu, page_src, ((pst & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
+            const int sb = sb_begin + pst * kConsumerWarps + lane;
+            if (lane < kConsumerWarps && sb < sb_end) {
+                if (sb < u.nb1) {  // compact rows
+                    const int32_t y = static_cast<int32_t>(u.crow0 + (int64_t)sb * kSubTokens);
+#pragma unroll
+                    for (int bx = 0; bx < T::kBoxes; ++bx) {
+                        tma_prefetch_l2_2d(&tm_comp_k, bx * 64, y);
+                        tma_prefetch_l2_2d(&tm_comp_v, bx * 64, y);
+                    }
+                } else if (page >= 0 && page < p.num_pages) {
                     const int32_t y = (page * p.hkv + kvh) * kSubTokens;
 #pragma unroll
                     for (int bx = 0; bx < T::kBoxes; ++bx) {
@@ -857,11 +988,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     }
                 }
             }
-        }
+        };
+        const bool first_chunk_pf = !fast || p.deep_prefetch;
         for (int st = 0; st < n_stages; ++st) {
             if (st > 0 && (st & 7) == 0) {  // 8 stages x 4 sub-blocks = 32 page ids per chunk
                 cur = nxt;
-                nxt = page_of(sb_begin + (st / 8 + 1) * 32 + lane);
+                nxt = nxt2;
+                nxt2 = page_of(sb_begin + (st / 8 + 2) * 32 + lane);
             }
             const int slot = st % T::kStages;
             if (st >= T::kStages) {
@@ -893,6 +1026,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                         const int pg = u.page0 + (sb - u.nb1);
                         if (page < 0 || page >= p.num_pages) {
                             report(p.dev_status, SFI_DEV_BAD_PAGE);
+                            s_bad = 1;  // seen by the consumers through this stage's barrier
                         } else {
                             y = (page * p.hkv + kvh) * kSubTokens;
                             pos0 = pg * kSubTokens;
@@ -915,6 +1049,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     mbar_arrive(&full_bar[slot]);
                 }
             }
+            if (first_chunk_pf && st == T::kStages - 1)
+                for (int pst = T::kStages; pst < 8 && pst < n_stages; ++pst) prefetch_stage(pst, cur);
+            // stage st + 8 lies in the next chunk of page ids (nxt)
+            if (p.deep_prefetch && st + kDeepPrefetch < n_stages && st + kDeepPrefetch >= 8)
+                prefetch_stage(st + kDeepPrefetch, nxt);
         }
         return;  // the producer takes no part in the merges
     }
@@ -978,7 +1117,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     float *score_row = nullptr;
     if (SCORES && p.scores && !fast) {
         if (u.L <= p.score_stride) {
-            score_row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride;
+            // Scores are written as the stream goes; a unit with a bad page id anywhere in
+            // [0, L) writes none of them (nor its output: the flag reaches the merge).
+            if (!request_pages_bad(p, r, u.L)) {
+                score_row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride;
+            } else if (threadIdx.x == 0) {
+                s_bad = 1;
+            }
         } else if (threadIdx.x == 0 && split == 0) {
             report(p.dev_status, SFI_DEV_BAD_LEN);  // score row too short: scores not written
         }
@@ -1002,12 +1147,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             // Only the split that owns that sub-block does it (a stage's padding slots
             // past sb_end may carry the same index).
             fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane,
-                                  s_app_val, &s_app_page);
+                                  s_app_val, &s_app_page, &s_bad);
         }
         if (MQ && p.k_new != nullptr && in.y >= 0 && sb_begin + st * kConsumerWarps + warp < sb_end &&
             in.y + kSubTokens > u.L0 - 1 && in.y < u.L) {
             // Fused append of the query tokens (positions [L - T, L)) in this paged sub-block.
-            fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane);
+            fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane,
+                           &s_bad);
         }
         if (hi > lo) {
             const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);
@@ -1085,6 +1231,9 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         const int tok = row / G;
         return ((int64_t)r * p.tokens + tok) * p.hq + (int64_t)kvh * G + (row - tok * G);
     };
+    // A partial that must not reach the output (a bad page id in the unit, or a timed-out
+    // wait) carries l = -1: every merge that sees it skips the unit's writes.
+    const bool skip = !ok || s_bad != 0;
     if (ok) {
         for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
             const int row = e / D, d = e - (e / D) * D;
@@ -1101,9 +1250,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     lsum += sm_l[w * kRows + row] * f;
                 }
             }
+            if (skip) lsum = -1.f;
             if (splits == 1) {
-                p.out[out_row(row) * D + d] = acc / lsum;
-                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+                if (!skip) {
+                    p.out[out_row(row) * D + d] = acc / lsum;
+                    if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+                }
             } else if (CLUSTER) {
                 cp_o[row * D + d] = acc;
                 if (d == 0) {
@@ -1119,10 +1271,22 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 }
             }
         }
+    } else if (splits > 1) {
+        for (int row = ctid; row < rows; row += kConsumerWarps * 32) {
+            if (CLUSTER) {
+                cp_m[row] = -INFINITY;
+                cp_l[row] = -1.f;
+            } else {
+                const int64_t slot = (slot0 + split) * kRows + row;
+                p.ws_ml[slot * 2 + 0] = -INFINITY;
+                p.ws_ml[slot * 2 + 1] = -1.f;
+            }
+        }
     }
     if (splits == 1) return;
     merge_splits<D, kRows, CLUSTER>(p, reinterpret_cast<float *>(smem + T::kRecvOffset), T::kRecvBytes, &merge_bar,
-                                     &s_last, cp_o, cp_m, cp_l, rows, splits, split, unit, slot0, ok, out_row);
+                                     &s_last, cp_o, cp_m, cp_l, rows, splits, split, unit, slot0,
+                                     reinterpret_cast<float *>(smem), T::kRingBytes, out_row);
 }
 
 template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>

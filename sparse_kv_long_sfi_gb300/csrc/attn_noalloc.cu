@@ -52,18 +52,21 @@ extern "C" sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, 
                                                    int32_t batch, int32_t max_tokens, int32_t num_splits,
                                                    uint32_t flags, int32_t *dev_status, void *stream) {
     if (!shape || batch < 0 || num_splits < 0) return SFI_ERR_INVALID_ARG;
-    const size_t need = sfi_workspace_size(shape, batch, max_tokens, num_splits);
+    // The scratch the inner call will use: the chunked plan's under SFI_ATTN_RAGGED,
+    // the regular split plan's otherwise (0 when the splits merge inside a cluster).
+    const bool ragged = (flags & SFI_ATTN_RAGGED) != 0;
+    const size_t need = ragged ? sfi_mixed_workspace_size(shape, batch, 0, max_tokens, 0)
+                               : sfi_workspace_size(shape, batch, max_tokens, num_splits);
     if (need > kScratchBytes) return SFI_ERR_WORKSPACE;  // the plan needs more than the fixed scratch
     void *scratch = nullptr;
     sfi_status st = scratch_address(&scratch);
     if (st != SFI_OK) return st;
     if (need > 0) {
-        // The split counters must start at zero; the array keeps whatever the last
-        // call (on any stream) left in it.
-        const sfi::WorkspaceLayout l =
-            sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, sfi_plan_splits(shape, batch, max_tokens,
-                                                                                        num_splits),
-                                  shape->head_dim);
+        // Both plans start the scratch with one split counter per (request, KV head),
+        // which must be zero; the array keeps whatever the last call (on any stream)
+        // left in it.
+        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots((int64_t)batch * shape->num_kv_heads, 0,
+                                                                   shape->head_dim);
         if (cudaMemsetAsync(static_cast<char *>(scratch) + l.count_off, 0, l.ml_off - l.count_off,
                             static_cast<cudaStream_t>(stream)) != cudaSuccess)
             return SFI_ERR_CUDA;

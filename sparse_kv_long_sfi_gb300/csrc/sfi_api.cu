@@ -115,6 +115,10 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
 
 bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
 
+// Launches of at most one CTA per SM keep too few bytes in flight through their rings
+// alone: their producers also run a rolling L2 prefetch ahead of the copies.
+int32_t deep_prefetch_for(int64_t ctas) { return ctas <= sm_count_current_device() ? 1 : 0; }
+
 
 // Plan of a mixed launch. The host knows only upper bounds of the units' lengths, so
 // each mode is cut into fixed-size chunks of sub-blocks: one wave of two CTAs per SM
@@ -218,6 +222,7 @@ sfi_status launch_chunked(AttnParams &p, bool fast, const int32_t *req_ids, int3
     p.fast_chunk_sb = m.fast_chunk_sb;
     p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);
+    p.deep_prefetch = deep_prefetch_for(units * (fast ? m.fast_splits : m.slow_splits));
     p.ws_count = nullptr;
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
@@ -342,6 +347,7 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
                               stream);
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeFast, false, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -384,6 +390,7 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
                               workspace_bytes, stream);
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeDense, scores != nullptr, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -446,6 +453,8 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.fast_chunk_sb = m.fast_chunk_sb;
     p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);  // > 1: partial states go through the workspace
+    p.deep_prefetch = deep_prefetch_for((int64_t)n_fast * shape->num_kv_heads * m.fast_splits +
+                                        (int64_t)n_slow * shape->num_kv_heads * m.slow_splits);
     if (p.splits > 1) {
         const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim);
         if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -510,6 +519,7 @@ sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.score_stride = score_stride;
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
         return st;
     AttnMaps maps;
@@ -557,6 +567,7 @@ sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.c_total_rows = compact->total_rows;
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
+    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
         return st;
     AttnMaps maps;

@@ -215,6 +215,23 @@ def test_slow_step_stress_64k_zipf_ties():
     # the duplicated rows produced exact ties in the GPU scores
     sc = w.layers[0].scores.cpu().numpy()
     assert any(len(np.unique(sc[r, h, S:S + n])) < n for r in range(8) for h in range(8))
+    # score values of the sampled request (G = 8 at 64K) against the oracle's fp64 group
+    # sums, within the fp32 dot-product bound 2 G D 2^-24 sum |scale q k|
+    r, L = 6, int(w.cur[6])
+    kp, vp, pr = w.host_pages(0, r)
+    q = w.host_q(0, 0, r)
+    ref = oracle.group_scores(q, kp, pr, L, S, W, 64, 8, 128, 16, stride=sc.shape[-1])
+    masked = np.isneginf(ref[:, :L])
+    assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+    qa = np.abs(syn.bf16_values(q))
+    pos = np.arange(L)
+    for h in range(8):
+        rows = np.abs(syn.bf16_values(kp[pr[pos // 16], h, pos % 16]))
+        mag = (rows @ qa[8 * h:8 * h + 8].T).sum(1) / math.sqrt(128)
+        bound = 2 * 8 * 128 * 2.0 ** -24 * mag + 1e-30
+        ok = ~masked[h]
+        err = np.abs(sc[r, h, :L][ok].astype(np.float64) - ref[h, :L][ok])
+        assert (err <= bound[ok]).all(), (h, err.max())
 
 
 @pytest.mark.parametrize("single_launch,ragged", [(True, False), (False, False), (False, True)],
@@ -375,3 +392,83 @@ def test_speculative_draft_verify_refresh_16k_batch16():
     w.dec.join()
     for layer in range(NL):
         _check_fast(w, 1, layer, sampled)
+
+
+def test_schedule_without_join_between_steps():
+    """Nine decode steps (slow, fast, fast with a refresh layer, mixed, ...) issued back to
+    back with no join between them, so a step's fast attention of layer i may be queued
+    while layer i's Selector and compaction from the previous step are still running on
+    the side stream: only the per-layer events order them (Figure 3 (A) of the SFI
+    paper). Each step's outputs, scores and selections are snapshotted on the stream
+    that wrote them; after one final join every step of every request is checked
+    against the oracle (attention within tolerance, selection bit-exact)."""
+    B, NL, S, W = 6, 2, 16, 64
+    g = syn.rng(91, 0)
+    lens = g.integers(2000, 5000, size=B)
+    k = [int(x) for x in g.integers(100, 400, size=B)]
+    steps = 9
+    w = Workload(91, lens, 16, 8, 128, S, W, k, steps=steps, layers=NL, heavy_frac=0.02, k_cap=max(k))
+    # per step: request modes (1 slow / 0 fast) and refresh layers inside an all-fast step
+    modes = [[1] * B, [0] * B, [0] * B, [1, 0, 0, 1, 0, 0], [0] * B, [1] * B, [0] * B, [0, 1, 0, 0, 0, 1], [0] * B]
+    refresh = [(), (), (1,), (), (0,), (), (), (), ()]
+    dec = w.dec
+    keep = []  # device tensors the side stream may still read
+    snaps = []
+    cur = w.cur.copy()
+    for t in range(steps):
+        cur = cur + 1
+        seq = torch.as_tensor(cur.astype(np.int32)).cuda()
+        keep.append(seq)
+        m = np.asarray(modes[t], bool)
+        if m.all():
+            dec.slow_step(w.io(t), seq)
+        elif not m.any():
+            dec.fast_step(w.io(t), seq, refresh_layers=refresh[t])
+        else:
+            sid = torch.as_tensor(np.flatnonzero(m).astype(np.int32)).cuda()
+            fid = torch.as_tensor(np.flatnonzero(~m).astype(np.int32)).cuda()
+            keep += [sid, fid]
+            dec.mixed_step(w.io(t), seq, sid, fid)
+        snap = {"cur": cur.copy()}
+        with torch.cuda.stream(dec.main):  # written by the main stream
+            snap["out"] = w.out.clone()
+            snap["lse"] = w.lse.clone()
+            snap["scores"] = [L.scores.clone() for L in w.layers]
+        with torch.cuda.stream(dec.aux):  # written by the side stream (no join)
+            snap["idx"] = [L.idx.clone() for L in w.layers]
+            snap["count"] = [L.compact.count.clone() for L in w.layers]
+        snaps.append(snap)
+    dec.join()
+    torch.cuda.synchronize()
+    assert dec.dev_status.item() == 0
+    oracle_state = {}  # (layer, request) -> oracle compact rows of the latest slow step
+    n_checked = 0
+    for t in range(steps):
+        sn = snaps[t]
+        w.cur = sn["cur"]
+        out, lse = sn["out"].cpu().numpy(), sn["lse"].cpu().numpy()
+        for layer in range(NL):
+            slow = np.asarray(modes[t], bool) | (layer in refresh[t])
+            sc = sn["scores"][layer].cpu().numpy()
+            idx, count = sn["idx"][layer].cpu().numpy(), sn["count"][layer].cpu().numpy()
+            cap = w.layers[layer].compact.capacity.cpu().numpy()
+            for r in range(B):
+                kp, vp, pr = w.host_pages(layer, r)
+                q = w.host_q(t, layer, r)
+                L = int(w.cur[r])
+                if slow[r]:
+                    o_ref, l_ref = oracle.dense_attn(q, kp, vp, pr, L, w.Hq, w.Hkv, w.D, 16)
+                    for h in range(w.Hkv):
+                        want = oracle.select_topk(sc[r, h], L, S, W, k[r])
+                        assert count[r] == len(want), (t, layer, r)
+                        np.testing.assert_array_equal(idx[r, h, :len(want)], want,
+                                                      err_msg=f"selection t={t} layer={layer} r={r} kv={h}")
+                    rk, rv = oracle.compact(kp, vp, pr, L, S, idx[r], count[r], w.Hkv, w.D, 16, cap[r])
+                    oracle_state[(layer, r)] = (rk, rv, count[r])
+                else:
+                    rk, rv, keff = oracle_state[(layer, r)]
+                    o_ref, l_ref = oracle.fast_attn(q, rk, rv, keff, kp, vp, pr, L, S, W, w.Hq, w.Hkv, w.D, 16)
+                assert_close(out[layer, r], o_ref, f"out t={t} layer={layer} r={r} slow={bool(slow[r])}")
+                assert_close(lse[layer, r], l_ref, f"lse t={t} layer={layer} r={r}")
+                n_checked += 1
+    assert n_checked == steps * NL * B

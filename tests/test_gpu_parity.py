@@ -93,11 +93,19 @@ def test_dense_attention_matches_oracle(D, Hq, Hkv, splits):
         assert_close(lse[r], l_ref, f"lse r={r}")
 
 
-def test_slow_step_scores_match_oracle_within_fp32_bound():
-    prob = Problem(seed=7, lens=[37, 300, 1024, 1031], Hq=8, Hkv=2, D=64, S=4, W=32, heavy_frac=0.04).to_device()
-    stride = 1040
+@pytest.mark.parametrize("D,Hq,Hkv", [(64, 8, 2), (128, 8, 8), (128, 16, 8), (128, 32, 8), (128, 64, 8)],
+                         ids=["d64-g4", "d128-g1", "d128-g2", "d128-g4", "d128-g8"])
+@pytest.mark.parametrize("splits", [0, 12], ids=["auto", "workspace-merge"])
+def test_slow_step_scores_match_oracle_within_fp32_bound(D, Hq, Hkv, splits):
+    """Score values element-wise against the oracle's fp64 group sums (rounded once to
+    fp32), within the fp32 dot-product bound, at every group size G = 1, 2, 4, 8."""
+    prob = Problem(seed=7 + Hq + D, lens=[37, 300, 1024, 2000], Hq=Hq, Hkv=Hkv, D=D, S=4, W=32,
+                   heavy_frac=0.04).to_device()
+    stride = 2016
+    if splits:
+        assert _sfi().sfi_plan_splits(prob.shape, prob.B, 2016, splits) == splits
     scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
-    out, lse = _dense(prob, scores=scores)
+    out, lse = _dense(prob, scores=scores, num_splits=splits)
     sc = scores.cpu().numpy()
     for r in range(prob.B):
         L = prob.lens[r]
@@ -422,19 +430,58 @@ def test_config1_slow_then_eight_fast_steps():
 # ---------------------------------------------------------------------------
 # Device-side error reporting (host-made bad inputs the kernels check; nothing faults)
 # ---------------------------------------------------------------------------
-def test_bad_page_and_length_are_reported_not_faulted():
+@pytest.mark.parametrize("splits", [1, 2, 12], ids=["one-split", "cluster-merge", "workspace-merge"])
+def test_bad_page_and_length_are_reported_not_faulted(splits):
+    """A page id outside the pool is reported (SFI_DEV_BAD_PAGE) and the offending
+    request writes nothing: its outputs, log-sum-exps and score rows keep the caller's
+    NaN sentinel, in every split plan (one CTA, cluster merge, workspace merge), while
+    the healthy request matches the oracle. A bad length is reported the same way."""
     sfi = _sfi()
-    prob = Problem(seed=51, lens=[100, 100], Hq=8, Hkv=2, D=64, S=4, W=32, extra_tokens=16).to_device()
+    prob = Problem(seed=51, lens=[1500, 1500], Hq=8, Hkv=2, D=64, S=4, W=32, extra_tokens=16).to_device()
     pt = prob.d_kv.page_table.clone()
-    pt[1, 2] = 10_000_000  # page id outside the pool
+    # a page id outside the pool, in the middle of request 1 (outside the first split of a
+    # two-split plan, so the bad partial reaches the merge from a peer CTA)
+    pt[1, 60] = 10_000_000
     bad = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, pt, prob.d_kv.seq_lens)
-    out = torch.zeros((2, 8, 64), device="cuda")
+    stride = 1520
+    maxL = 1520
+    ws = sfi.alloc_workspace(prob.shape, 2, maxL, splits)
+    for with_scores in (False, True):
+        out = torch.full((2, 8, 64), float("nan"), device="cuda")
+        lse = torch.full((2, 8), float("nan"), device="cuda")
+        scores = torch.full((2, 2, stride), float("nan"), device="cuda") if with_scores else None
+        st = _status()
+        sfi.sfi_slow_dense_attn_with_scores(prob.shape, bad, 4, 32, prob.d_q, out, lse, scores, max_tokens=maxL,
+                                            num_splits=splits, workspace=ws, dev_status=st)
+        torch.cuda.synchronize()
+        assert st.item() == 1, f"status {st.item()}"  # SFI_DEV_BAD_PAGE only
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        assert np.isnan(o[1]).all() and np.isnan(l[1]).all(), "the bad request's outputs must not be written"
+        o_ref, l_ref = prob.oracle_dense(0)
+        assert_close(o[0], o_ref, "the healthy request is unaffected")
+        assert_close(l[0], l_ref, "the healthy request's lse")
+        if with_scores:
+            sc = scores.cpu().numpy()
+            assert np.isnan(sc[1]).all(), "the bad request's score rows must not be written"
+            ref = prob.oracle_scores(0, stride)
+            masked = np.isneginf(ref[:, :1500])
+            assert np.array_equal(np.isneginf(sc[0, :, :1500]), masked)
+        if splits > 8:
+            assert counters_zero(ws, 2 * prob.Hkv), "split counters must be left zeroed"
+    # the fast step over the same pages (the recent window holds the bad page)
+    pt_fast = prob.d_kv.page_table.clone()
+    pt_fast[1, 1490 // 16] = -3
+    comp = _compact_buffers(prob, [64, 64])
+    badf = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, pt_fast, prob.d_kv.seq_lens)
+    out = torch.full((2, 8, 64), float("nan"), device="cuda")
     st = _status()
-    sfi.sfi_slow_dense_attn_with_scores(prob.shape, bad, 4, 32, prob.d_q, out, None, None, dev_status=st)
+    sfi.sfi_fast_decode_attn(prob.shape, badf, comp, 4, 32, prob.d_q, out, None, max_tokens=4 + 64 + 32 + 32,
+                             num_splits=min(splits, 2), workspace=sfi.alloc_workspace(prob.shape, 2, 132, 2),
+                             dev_status=st)
     torch.cuda.synchronize()
-    assert st.item() & 1
-    o_ref, _ = prob.oracle_dense(0)
-    assert_close(out.cpu().numpy()[0], o_ref, "the healthy request is unaffected")
+    assert st.item() == 1, f"status {st.item()}"
+    assert np.isnan(out.cpu().numpy()[1]).all(), "the bad request's fast-step outputs must not be written"
+    assert np.isfinite(out.cpu().numpy()[0]).all()
     st.zero_()
     lens_bad = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, prob.d_kv.page_table, dev_i32([100, 0]))
     sfi.sfi_slow_dense_attn_with_scores(prob.shape, lens_bad, 4, 32, prob.d_q, out, None, None, dev_status=st)
@@ -447,9 +494,9 @@ def test_bad_page_and_length_are_reported_not_faulted():
 @pytest.mark.parametrize("splits", [2, 12], ids=["cluster-merge", "workspace-merge"])
 def test_bounded_wait_runs_out_and_reports_timeout(splits):
     """SFI_ATTN_TEST_WITHHOLD: every CTA's producer withholds its second stage, so the
-    consumers' bounded wait runs out (about 2 s): the launch returns with SFI_DEV_TIMEOUT
-    and writes no output, and a normal launch right after it (fresh status, zeroed
-    workspace) is correct, so the context stays usable."""
+    consumers' bounded wait runs out (about 2 s): the launch returns with SFI_DEV_TIMEOUT,
+    writes no output and leaves the workspace counters zeroed, and a normal launch right
+    after it (fresh status, same workspace) is correct, so the context stays usable."""
     sfi = _sfi()
     prob = Problem(seed=53, lens=[3000, 2500], Hq=16, Hkv=8, D=128, S=4, W=32).to_device()
     maxL = int(prob.lens.max()) + 16
@@ -463,7 +510,9 @@ def test_bounded_wait_runs_out_and_reports_timeout(splits):
     torch.cuda.synchronize()
     assert st.item() & 16, f"status {st.item()}"  # SFI_DEV_TIMEOUT
     assert np.isnan(out.cpu().numpy()).all(), "a timed-out launch writes no output"
-    ws.zero_()
+    if splits > 8:
+        # every split still reaches the merge counter, so it is left zeroed
+        assert counters_zero(ws, prob.B * prob.Hkv), "split counters must be left zeroed after a timeout"
     st.zero_()
     sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, None, None,
                                         max_tokens=maxL, num_splits=splits, workspace=ws, dev_status=st)
