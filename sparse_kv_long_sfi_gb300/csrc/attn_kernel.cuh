@@ -64,8 +64,6 @@ struct AttnTile {
 };
 
 constexpr int kAttnThreads = (kConsumerWarps + 1) * 32;
-// Stages between a unit's TMA copies and its rolling L2 prefetch (deep_prefetch).
-constexpr int kDeepPrefetch = 8;
 constexpr float kLn2 = 0.6931471805599453f;
 
 __device__ __forceinline__ void consumer_bar_sync() {
@@ -601,175 +599,53 @@ __host__ __device__ constexpr bool cluster_push_fits(int splits, int rows, int r
     return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= recv_bytes;
 }
 
-// Split merge of one unit's partial states (m, l, unnormalised o per query row), run by
-// the consumer threads (threadIdx.x < 128) of each of the unit's CTAs once this CTA's
-// partial is complete: in cp_o [rows][D], cp_m, cp_l (shared memory) when the unit's
-// splits form a cluster, in workspace slot (slot0 + split) otherwise. recv is the
-// receive region (recv_bytes) where the other CTAs of a cluster push their partials.
-// A partial with l < 0 comes from a split that must not write (a bad page id or a
-// timed-out wait): the merge then writes nothing for the unit.
-template <int D, int kRows, bool CLUSTER, typename OutRow>
-__device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, int recv_bytes, uint64_t *merge_bar,
-                                             int *s_last, float *cp_o, float *cp_m, float *cp_l, int rows, int splits,
-                                             int split, int64_t unit, int64_t slot0, float *stage, int stage_bytes,
-                                             OutRow out_row) {
+// Workspace merge of one unit's `nparts` partial states, in workspace slots
+// slot0 + [0, nparts) (rows per slot kRows, this CTA's own already written): the CTA
+// that arrives last merges them. Run by the consumer threads (threadIdx.x < 128).
+// `bar` is an mbarrier (count 1) for the bulk copies, `stage` (stage_bytes) and
+// `scratch` shared memory this CTA no longer needs. A partial with l < 0 comes from a
+// split that must not write: the merge then writes nothing for the unit.
+template <int D, int kRows, typename OutRow>
+__device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *bar, int *s_last, int rows, int nparts,
+                                                int64_t unit, int64_t slot0, float *stage, int stage_bytes,
+                                                float *scratch, OutRow out_row) {
     const int ctid = threadIdx.x;  // 0 .. 127
-    if (CLUSTER && cluster_push_fits<D>(splits, rows, recv_bytes)) {
-        // ---- split merge inside the cluster: the other CTAs push their partials into
-        // rank 0's receive region (distributed shared-memory stores), rank 0 merges them
-        // from its own shared memory ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        const int slot_f = cluster_slot_floats<D>(rows);
-        if (split != 0) {
-            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * slot_f) * 4u;
-            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
-                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
-            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
-                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
-                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
-            }
-            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // release: my stores above
-            // Rank 0 signals once every push has landed; only then may this CTA exit.
-            if (ctid == 0 && !mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
-        const bool got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
-        if (got && ctid >= 1 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
-        if (!got) {
-            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
-        for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-            const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-            float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-            float2 os[kMaxClusterSplits];
-            ms[0] = cp_m[row];
-            ls[0] = cp_l[row];
-            os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
-#pragma unroll
-            for (int s = 1; s < kMaxClusterSplits; ++s) {
-                if (s < splits) {
-                    const float *src = recv + (s - 1) * slot_f;
-                    ms[s] = src[rows * D + row];
-                    ls[s] = src[rows * D + rows + row];
-                    os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
-                }
-            }
-            float M = -INFINITY;
-            bool fail = false;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-                if (s < splits) {
-                    M = fmaxf(M, ms[s]);
-                    fail |= ls[s] < 0.f;
-                }
-            }
-            float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-                if (s < splits && ls[s] > 0.f) {
-                    const float f = fast_exp2(ms[s] - M);
-                    ax += os[s].x * f;
-                    ay += os[s].y * f;
-                    lsum += ls[s] * f;
-                }
-            }
-            if (fail) continue;
-            *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
-            if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-        }
-        return;
-    }
-
-    if (CLUSTER) {
-        // ---- split merge inside the cluster, pulled by rank 0 from the other CTAs'
-        // shared memory (when their partials do not fit rank 0's receive region) ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        if (split != 0) {
-            if (ctid == 0) {
-                mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // "my partial is ready"
-                // Stay alive (shared memory readable) until rank 0 has read it.
-                if (!mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
-            }
-            return;
-        }
-        if (ctid == 0) *s_last = mbar_wait_cluster_bounded(merge_bar, 0) ? 1 : 0;
-        consumer_bar_sync();
-        if (*s_last) {
-            // Each thread merges pairs of outputs. All loads from the peers' shared
-            // memory are issued before any is used, so their latencies overlap.
-            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-                float2 os[kMaxClusterSplits];
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < splits) {
-                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
-                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
-                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
-                    }
-                }
-                float M = -INFINITY;
-                bool fail = false;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < splits) {
-                        M = fmaxf(M, ms[s]);
-                        fail |= ls[s] < 0.f;
-                    }
-                }
-                float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < splits && ls[s] > 0.f) {
-                        const float f = fast_exp2(ms[s] - M);
-                        ax += os[s].x * f;
-                        ay += os[s].y * f;
-                        lsum += ls[s] * f;
-                    }
-                }
-                if (fail) continue;
-                *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
-                if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-            }
-        }
-        if (!*s_last) report(p.dev_status, SFI_DEV_TIMEOUT);
-        consumer_bar_sync();  // every read of the peers' shared memory is done
-        if (ctid > 0 && ctid < splits) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
-        return;
-    }
-
-    // ---- split merge by the last CTA of this unit, through the global workspace ----
+    const int splits = nparts;
+    uint64_t *merge_bar = bar;
+    float *recv = scratch;
     // Every split arrives (a failed one with l = -1), so the counter always completes and
-    // the last CTA leaves it zeroed for the next launch.
-    asm volatile("fence.proxy.async.global;" ::: "memory");  // this thread's partial, for the bulk copies below
-    __threadfence();
+    // the last CTA leaves it zeroed for the next launch. One thread per CTA publishes
+    // the CTA's partial (release fence after the barrier, then the counter) and, in the
+    // last CTA, acquires the others' before the barrier that lets the merge start.
     consumer_bar_sync();
     if (ctid == 0) {
+        asm volatile("fence.acq_rel.gpu;" ::: "memory");
         const int prev = atomicAdd(&p.ws_count[unit], 1);
         *s_last = (prev == splits - 1);
+        if (*s_last) {
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            p.ws_count[unit] = 0;
+        }
     }
     consumer_bar_sync();
     if (!*s_last) return;
-    __threadfence();
     // The unit's partials come into shared memory (`stage`, the ring: free once this CTA's
     // own partial is in the workspace) by bulk copies, in batches of whole splits: the
-    // (m, l) block of the batch, then each split's rows x D partial output. Each thread
-    // merges its 4-float output chunks online over the staged splits (running max and
-    // normaliser per chunk), so the whole merge costs a few round trips.
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of the ring
-    consumer_bar_sync();
-    if (ctid == 0) {
-        p.ws_count[unit] = 0;
-        asm volatile("fence.proxy.async.global;" ::: "memory");
-    }
+    // (m, l) block of the batch, then each split's rows x D partial output, issued by the
+    // lanes of warp 0 in parallel. Per batch, warps first derive each row's maximum,
+    // normaliser and per-split weights (in `recv`, unused without a cluster); each thread
+    // then sums its 4-float output chunks with those weights and folds the batch into its
+    // running state.
+    const int warp = ctid >> 5, lane = ctid & 31;
     constexpr int kC = D / 4;  // 4-float chunks per row
     constexpr int kCpt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
     const int o_floats = rows * D;
     const int nbmax = stage_bytes / (kRows * 2 * 4 + o_floats * 4);
     float *ml_st = stage;                        // [nbmax][kRows][2]
     float *o_st = stage + nbmax * kRows * 2;     // [nbmax][rows][D]
+    float *w_st = recv;                          // [nbmax][kRows] weights e^(m - M_batch), 0 for l <= 0
+    float *mb_st = recv + nbmax * kRows;         // [kRows] batch maximum
+    float *lb_st = mb_st + kRows;                // [kRows] batch normaliser, -1 if a split failed
     float4 acc[kCpt];
     float Mr[kCpt], Lr[kCpt];
     int crow[kCpt], cd[kCpt];
@@ -783,43 +659,87 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
         Lr[j] = 0.f;
     }
     bool fail = false;
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of the ring
+    consumer_bar_sync();
     for (int b0 = 0, batch = 0; b0 < splits; b0 += nbmax, ++batch) {
         const int nbt = min(nbmax, splits - b0);
-        if (ctid == 0) {
+        if (warp == 0) {
             const uint32_t ml_bytes = (uint32_t)(nbt * kRows * 2 * 4), o_bytes = (uint32_t)(o_floats * 4);
-            mbar_arrive_expect_tx(merge_bar, ml_bytes + (uint32_t)nbt * o_bytes);
-            bulk_load_1d(ml_st, &p.ws_ml[(slot0 + b0) * kRows * 2], ml_bytes, merge_bar);
-            for (int i = 0; i < nbt; ++i)
-                bulk_load_1d(o_st + i * o_floats, &p.ws_part[(slot0 + b0 + i) * kRows * D], o_bytes, merge_bar);
+            if (lane == 0) mbar_arrive_expect_tx(merge_bar, ml_bytes + (uint32_t)nbt * o_bytes);
+            __syncwarp();
+            asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquired partials, to the copies
+            for (int i = lane; i <= nbt; i += 32) {
+                if (i == nbt)
+                    bulk_load_1d(ml_st, &p.ws_ml[(slot0 + b0) * kRows * 2], ml_bytes, merge_bar);
+                else
+                    bulk_load_1d(o_st + i * o_floats, &p.ws_part[(slot0 + b0 + i) * kRows * D], o_bytes, merge_bar);
+            }
         }
         const bool got = mbar_wait_warp(merge_bar, batch & 1);
-        if (!got && (ctid & 31) == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
-        for (int i = 0; i < nbt && got; ++i) {
+        if (!got && lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+        if (got) {
+            // per row of the batch: maximum, normaliser and weights (warp w: rows w, w + 4, ...)
+            for (int row = warp; row < rows; row += kConsumerWarps) {
+                float M = -INFINITY;
+                bool f = false;
+                for (int i = lane; i < nbt; i += 32) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + row) * 2]);
+                    f |= ml.y < 0.f;
+                    if (ml.y > 0.f) M = fmaxf(M, ml.x);
+                }
 #pragma unroll
-            for (int j = 0; j < kCpt; ++j) {
-                if (crow[j] < 0) continue;
-                const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + crow[j]) * 2]);
-                fail |= ml.y < 0.f;
-                if (ml.y > 0.f) {
-                    const float4 o = *reinterpret_cast<const float4 *>(&o_st[i * o_floats + crow[j] * D + cd[j]]);
-                    const float Mn = fmaxf(Mr[j], ml.x);
-                    const float a = Lr[j] > 0.f ? fast_exp2(Mr[j] - Mn) : 0.f;
-                    const float f = fast_exp2(ml.x - Mn);
-                    acc[j].x = acc[j].x * a + o.x * f;
-                    acc[j].y = acc[j].y * a + o.y * f;
-                    acc[j].z = acc[j].z * a + o.z * f;
-                    acc[j].w = acc[j].w * a + o.w * f;
-                    Lr[j] = Lr[j] * a + ml.y * f;
-                    Mr[j] = Mn;
+                for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+                float Ls = 0.f;
+                for (int i = lane; i < nbt; i += 32) {
+                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + row) * 2]);
+                    const float wgt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
+                    w_st[i * kRows + row] = wgt;
+                    Ls += ml.y > 0.f ? ml.y * wgt : 0.f;
+                }
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, off);
+                f = __any_sync(0xffffffffu, f);
+                if (lane == 0) {
+                    mb_st[row] = M;
+                    lb_st[row] = f ? -1.f : Ls;
                 }
             }
         }
-        // every thread is done with this batch before the next overwrites it; a wait that
-        // ran out in any warp ends the merge for all of them
+        // a wait that ran out in any warp ends the merge for all of them
         if (consumer_bar_or(!got)) {
             fail = true;
             break;
         }
+#pragma unroll
+        for (int j = 0; j < kCpt; ++j) {
+            if (crow[j] < 0) continue;
+            const float Lb = lb_st[crow[j]];
+            fail |= Lb < 0.f;
+            if (Lb <= 0.f) continue;
+            float4 ab = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int i = 0; i < nbt; ++i) {
+                const float wgt = w_st[i * kRows + crow[j]];
+                const float4 o = *reinterpret_cast<const float4 *>(&o_st[i * o_floats + crow[j] * D + cd[j]]);
+                ab.x += o.x * wgt;
+                ab.y += o.y * wgt;
+                ab.z += o.z * wgt;
+                ab.w += o.w * wgt;
+            }
+            const float Mb = mb_st[crow[j]];
+            const float Mn = fmaxf(Mr[j], Mb);
+            const float a = Lr[j] > 0.f ? fast_exp2(Mr[j] - Mn) : 0.f;
+            const float bb = fast_exp2(Mb - Mn);
+            acc[j].x = acc[j].x * a + ab.x * bb;
+            acc[j].y = acc[j].y * a + ab.y * bb;
+            acc[j].z = acc[j].z * a + ab.z * bb;
+            acc[j].w = acc[j].w * a + ab.w * bb;
+            Lr[j] = Lr[j] * a + Lb * bb;
+            Mr[j] = Mn;
+        }
+        // every thread is done with this batch (generic reads ordered before the next
+        // batch's copies into the same shared memory)
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+        consumer_bar_sync();
     }
     // A failed split fails every row of the unit; make the decision CTA-wide.
     fail = consumer_bar_or(fail);
@@ -832,6 +752,153 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, i
         *reinterpret_cast<float2 *>(dst) = make_float2(acc[j].x / lsum, acc[j].y / lsum);
         *reinterpret_cast<float2 *>(dst + 2) = make_float2(acc[j].z / lsum, acc[j].w / lsum);
         if (cd[j] == 0 && p.lse) p.lse[out_row(crow[j])] = (Mr[j] + log2f(lsum)) * kLn2;
+    }
+}
+
+// Split merge of one unit's partial states (m, l, unnormalised o per query row), run by
+// the consumer threads (threadIdx.x < 128) of each of the unit's CTAs once this CTA's
+// partial is complete: in cp_o [rows][D], cp_m, cp_l (shared memory) when the unit's
+// splits form a thread-block cluster, in workspace slot (slot0 + split) otherwise.
+// Inside the cluster the other CTAs push their partials into rank 0's receive region
+// `recv` (recv_bytes) with distributed shared-memory stores, or rank 0 pulls them when
+// they do not fit. A partial with l < 0 comes from a split that must not write (a bad
+// page id or a timed-out wait): the merge then writes nothing for the unit. (Clusters
+// of 8 whose partials then merge through the workspace were measured and dropped:
+// batch-1 dense at 16K, 32 splits, 15.9 -> 22.9 us per layer against merging the 32
+// splits one by one.)
+template <int D, int kRows, bool CLUSTER, typename OutRow>
+__device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, int recv_bytes, uint64_t *merge_bar,
+                                             int *s_last, float *cp_o, float *cp_m, float *cp_l, int rows, int splits,
+                                             int split, int64_t unit, int64_t slot0, float *stage, int stage_bytes,
+                                             OutRow out_row) {
+    const int ctid = threadIdx.x;  // 0 .. 127
+    if (!CLUSTER) {
+        workspace_merge<D, kRows>(p, merge_bar, s_last, rows, splits, unit, slot0, stage, stage_bytes, recv, out_row);
+        return;
+    }
+    const int crank = split, csize = splits;
+    // the merged values of one output pair
+    auto emit = [&](int row, int d, float M, float ax, float ay, float lsum, bool fail) {
+        if (fail) return;
+        *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
+        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+    };
+    if (cluster_push_fits<D>(csize, rows, recv_bytes)) {
+        // ---- push: the other CTAs store their partials into rank 0's receive region ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        const int slot_f = cluster_slot_floats<D>(rows);
+        if (crank != 0) {
+            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((crank - 1) * slot_f) * 4u;
+            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
+                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
+            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
+                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
+                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
+            }
+            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // release: my stores above
+            // Rank 0 signals once every push has landed; only then may this CTA exit.
+            if (ctid == 0 && !mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            return;
+        }
+        const bool got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
+        if (got && ctid >= 1 && ctid < csize) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
+        if (!got) {
+            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+        } else {
+            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+                float2 os[kMaxClusterSplits];
+                ms[0] = cp_m[row];
+                ls[0] = cp_l[row];
+                os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
+#pragma unroll
+                for (int s = 1; s < kMaxClusterSplits; ++s) {
+                    if (s < csize) {
+                        const float *src = recv + (s - 1) * slot_f;
+                        ms[s] = src[rows * D + row];
+                        ls[s] = src[rows * D + rows + row];
+                        os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
+                    }
+                }
+                float M = -INFINITY;
+                bool fail = false;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize) {
+                        if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
+                        fail |= ls[s] < 0.f;
+                    }
+                }
+                float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize && ls[s] > 0.f) {
+                        const float f = fast_exp2(ms[s] - M);
+                        ax += os[s].x * f;
+                        ay += os[s].y * f;
+                        lsum += ls[s] * f;
+                    }
+                }
+                emit(row, d, M, ax, ay, lsum, fail);
+            }
+        }
+    } else {
+        // ---- pull: rank 0 reads the other CTAs' partials from their shared memory
+        // (when they do not fit its receive region) ----
+        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
+        if (crank != 0) {
+            if (ctid == 0) {
+                mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // "my partial is ready"
+                // Stay alive (shared memory readable) until rank 0 has read it.
+                if (!mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+            }
+            return;
+        }
+        if (ctid == 0) *s_last = mbar_wait_cluster_bounded(merge_bar, 0) ? 1 : 0;
+        consumer_bar_sync();
+        const bool got = *s_last != 0;
+        if (got) {
+            // Each thread merges pairs of outputs. All loads from the peers' shared
+            // memory are issued before any is used, so their latencies overlap.
+            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
+                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
+                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
+                float2 os[kMaxClusterSplits];
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize) {
+                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
+                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
+                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
+                    }
+                }
+                float M = -INFINITY;
+                bool fail = false;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize) {
+                        if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
+                        fail |= ls[s] < 0.f;
+                    }
+                }
+                float ax = 0.f, ay = 0.f, lsum = 0.f;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize && ls[s] > 0.f) {
+                        const float f = fast_exp2(ms[s] - M);
+                        ax += os[s].x * f;
+                        ay += os[s].y * f;
+                        lsum += ls[s] * f;
+                    }
+                }
+                emit(row, d, M, ax, ay, lsum, fail);
+            }
+        } else if (ctid == 0) {
+            report(p.dev_status, SFI_DEV_TIMEOUT);
+        }
+        consumer_bar_sync();  // every read of the peers' shared memory is done
+        if (got && ctid > 0 && ctid < csize) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
     }
 }
 
@@ -956,18 +1023,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             if (sb >= sb_end || sb < u.nb1) return -1;
             return ptab[u.page0 + (sb - u.nb1)];
         };
-        // page ids of the current chunk of 32 sub-blocks and of the next two (the rolling
-        // prefetch reads one chunk ahead; loading two ahead keeps it off the load latency)
         int cur = page_of(sb_begin + lane);
         int nxt = page_of(sb_begin + 32 + lane);
-        int nxt2 = page_of(sb_begin + 64 + lane);
         // L2 prefetch of stage pst's sub-blocks (page ids of its chunk of 32 in page_src;
         // warp-collective). Dense units prefetch the rest of their first chunk right after
         // the ring's first fill, so the first refills read L2 without delaying the ring's
-        // own copies (measured: it shortens the slow step; on short fast-step units it
-        // costs more than it saves). With deep_prefetch (launches of at most one CTA per
-        // SM, whose own ring keeps too few bytes in flight) every unit also prefetches a
-        // rolling window kDeepPrefetch stages ahead of its copies.
+        // own copies. (Measured: it shortens the slow step; on short fast-step units it
+        // costs more than it saves. A rolling prefetch 8 stages ahead for launches of at
+        // most one CTA per SM made them slower: batch-1 dense at 16K, 21.2 -> 23.7 us.)
         auto prefetch_stage = [&](int pst, int page_src) {
             const int page = __shfl_sync(0xffffffffu, page_src, ((pst & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
             const int sb = sb_begin + pst * kConsumerWarps + lane;
@@ -989,12 +1052,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 }
             }
         };
-        const bool first_chunk_pf = !fast || p.deep_prefetch;
         for (int st = 0; st < n_stages; ++st) {
             if (st > 0 && (st & 7) == 0) {  // 8 stages x 4 sub-blocks = 32 page ids per chunk
                 cur = nxt;
-                nxt = nxt2;
-                nxt2 = page_of(sb_begin + (st / 8 + 2) * 32 + lane);
+                nxt = page_of(sb_begin + (st / 8 + 1) * 32 + lane);
             }
             const int slot = st % T::kStages;
             if (st >= T::kStages) {
@@ -1049,11 +1110,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     mbar_arrive(&full_bar[slot]);
                 }
             }
-            if (first_chunk_pf && st == T::kStages - 1)
+            if (!fast && st == T::kStages - 1)
                 for (int pst = T::kStages; pst < 8 && pst < n_stages; ++pst) prefetch_stage(pst, cur);
-            // stage st + 8 lies in the next chunk of page ids (nxt)
-            if (p.deep_prefetch && st + kDeepPrefetch < n_stages && st + kDeepPrefetch >= 8)
-                prefetch_stage(st + kDeepPrefetch, nxt);
         }
         return;  // the producer takes no part in the merges
     }

@@ -83,15 +83,14 @@ sfi_status check_paged(const sfi_attn_shape *s, const sfi_paged_kv *kv) {
     return SFI_OK;
 }
 
-// Split-KV plan of one attention launch. Automatic plans fill one wave of resident
-// CTAs (two per SM) and keep at least four full stages of sub-blocks per split; an
-// explicit request is honoured down to two stages per split. Plans of up to
-// kMaxClusterSplits merge inside a thread-block cluster (no workspace). Beyond that the
-// last CTA of a unit merges every split from the workspace, a tail that grows with the
-// split count: such plans take one CTA per SM, and only when that still gives at least
-// twice kMaxClusterSplits; otherwise they stay at kMaxClusterSplits. (Batch 1 at 16K:
-// dense 31.7 -> 20.4 us per layer at 19-24 splits instead of 38; batch 4: 8 splits in
-// a cluster beat 9 through the workspace.)
+// Split-KV plan of one attention launch. Automatic plans fill about 85% of one wave of
+// resident CTAs (two per SM) and keep at least four full stages of sub-blocks per split;
+// an explicit request is honoured down to two stages per split. Leaving a sixth of the
+// slots free lets the next launch's CTAs become resident and start streaming while this
+// one drains (batch 1 at 16K, dense: 32 splits, 256 CTAs, 15.9 us per layer against 20.6
+// us for 38 splits, 304 CTAs). Plans of up to kMaxClusterSplits merge inside a
+// thread-block cluster (no workspace); between 8 and 16 splits the plan stays at 8;
+// from 16 on the last CTA of a unit merges the splits from the workspace.
 int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_count) {
     constexpr int kMaxSplits = 256;
     if (units <= 0) return 1;
@@ -103,21 +102,14 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
     } else if (nb == 0) {
         s = 1;
     } else {
-        s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm / units);
-        if (s > sfi::kMaxClusterSplits) {
-            const int one_per_sm = (int)std::max<int64_t>(1, (int64_t)sm_count / units);
-            s = one_per_sm >= 2 * sfi::kMaxClusterSplits ? one_per_sm : sfi::kMaxClusterSplits;
-        }
+        s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm * 17 / 20 / units);
+        if (s > sfi::kMaxClusterSplits && s < 2 * sfi::kMaxClusterSplits) s = sfi::kMaxClusterSplits;
         s = std::min(s, std::max(1, nb / (4 * sfi::kConsumerWarps)));
     }
     return std::max(1, std::min(s, kMaxSplits));
 }
 
 bool needs_workspace(int splits) { return splits > sfi::kMaxClusterSplits; }
-
-// Launches of at most one CTA per SM keep too few bytes in flight through their rings
-// alone: their producers also run a rolling L2 prefetch ahead of the copies.
-int32_t deep_prefetch_for(int64_t ctas) { return ctas <= sm_count_current_device() ? 1 : 0; }
 
 
 // Plan of a mixed launch. The host knows only upper bounds of the units' lengths, so
@@ -222,7 +214,6 @@ sfi_status launch_chunked(AttnParams &p, bool fast, const int32_t *req_ids, int3
     p.fast_chunk_sb = m.fast_chunk_sb;
     p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);
-    p.deep_prefetch = deep_prefetch_for(units * (fast ? m.fast_splits : m.slow_splits));
     p.ws_count = nullptr;
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
@@ -347,7 +338,6 @@ sfi_status sfi_fast_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv 
                               stream);
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeFast, false, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -390,7 +380,6 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
                               workspace_bytes, stream);
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes)) != SFI_OK) return st;
     return sfi::launch_attention(shape->head_dim, sfi::kModeDense, scores != nullptr, maps, p, batch,
                                  static_cast<cudaStream_t>(stream)) == cudaSuccess
@@ -453,8 +442,6 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.fast_chunk_sb = m.fast_chunk_sb;
     p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);  // > 1: partial states go through the workspace
-    p.deep_prefetch = deep_prefetch_for((int64_t)n_fast * shape->num_kv_heads * m.fast_splits +
-                                        (int64_t)n_slow * shape->num_kv_heads * m.slow_splits);
     if (p.splits > 1) {
         const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim);
         if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
@@ -519,7 +506,6 @@ sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.score_stride = score_stride;
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
         return st;
     AttnMaps maps;
@@ -567,7 +553,6 @@ sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.c_total_rows = compact->total_rows;
     const int64_t units = (int64_t)batch * shape->num_kv_heads;
     p.splits = plan_splits(units, max_tokens, num_splits, sm_count_current_device());
-    p.deep_prefetch = deep_prefetch_for(units * p.splits);
     if ((st = bind_workspace(p, units, shape->head_dim, workspace, workspace_bytes, sfi::kMaxRows)) != SFI_OK)
         return st;
     AttnMaps maps;

@@ -59,7 +59,6 @@ struct AttnParams {
     // sub-blocks per split in mixed mode (0: the mode's units split evenly into *_splits)
     int32_t fast_chunk_sb, slow_chunk_sb;
     int32_t early_prefetch;  // SFI_ATTN_EARLY_KV_PREFETCH: stream KV before the dependency wait
-    int32_t deep_prefetch;   // rolling L2 prefetch ahead of the copies (launches of at most one CTA per SM)
     int32_t withhold;        // SFI_ATTN_TEST_WITHHOLD: 1 + the stage whose copies are never issued (0 = none)
     // fused append of the current token (position L - 1), or null
     const __nv_bfloat16 *k_new;  // [B][Hkv][D]

@@ -311,3 +311,19 @@ def test_draft_with_fused_append_matches_oracle(T, flags):
         o_ref, _ = oracle.fast_multi_attn(q[r], rk, rv, ref_count[r], prob.kv.k_pool, prob.kv.v_pool,
                                           prob.kv.page_table[r], lens[r], T, S, W, Hq, Hkv, D, 16)
         assert_close(o[r], o_ref, f"draft out r={r}")
+
+
+@pytest.mark.parametrize("splits", [16, 32])
+def test_verify_and_draft_many_splits(splits):
+    """Multi-token passes split 16 and 32 ways (merged from the workspace)."""
+    D, Hq, Hkv, T = 128, 16, 8, 4
+    lens = [8200, 6600, 5000]
+    prob = Problem(seed=90 + splits, lens=lens, Hq=Hq, Hkv=Hkv, D=D, S=4, W=32).to_device()
+    q = _queries(91 + splits, prob.B, T, Hq, D)
+    out, lse = _verify(prob, q, T, num_splits=splits)
+    for r in range(prob.B):
+        o_ref, l_ref = oracle.verify_attn(q[r], prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], prob.lens[r],
+                                          T, Hq, Hkv, D, 16)
+        assert_close(out[r], o_ref, f"verify out r={r}")
+        assert_close(lse[r], l_ref, f"verify lse r={r}")
+    _draft_case(95 + splits, lens, Hq, Hkv, D, 4, 32, T, [4300, 4100, 4200], 4300, splits=splits)

@@ -63,19 +63,18 @@ def _dense(prob, num_splits=0, scores=None, req_ids=None, ragged=False, max_toke
 # Dense / slow-step attention
 # ---------------------------------------------------------------------------
 def test_automatic_split_plans():
-    """The automatic plans on this GPU: one wave of two CTAs per SM while that stays within
-    a cluster (8 splits); above that, one CTA per SM when it still gives >= 16 splits,
-    else 8; never fewer than four stages (16 sub-blocks) per split; the workspace
-    follows the plan (none inside a cluster)."""
+    """The automatic plans on this GPU: about 85% of one wave of two CTAs per SM (8 when
+    that lands between 8 and 16), never fewer than four stages (16 sub-blocks) per split;
+    the workspace follows the plan (none inside a cluster)."""
     sfi = _sfi()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shape = sfi.AttnShape(16, 8, 128)
-    for batch in (1, 2, 4, 16, 64):
+    for batch in (1, 2, 3, 4, 16, 64):
         for L in (1040, 16400, 65600):
             units, nb = batch * 8, (L + 15) // 16 + 1
-            s = max(1, 2 * sms // units)
-            if s > 8:
-                s = sms // units if sms // units >= 16 else 8
+            s = max(1, sms * 2 * 17 // 20 // units)
+            if 8 < s < 16:
+                s = 8
             s = max(1, min(s, nb // 16, 256))
             assert sfi.sfi_plan_splits(shape, batch, L, 0) == s, (batch, L)
             assert (sfi.sfi_workspace_size(shape, batch, L, 0) == 0) == (s <= 8), (batch, L)
@@ -828,3 +827,69 @@ def test_select_compact_subset_and_bad_capacity(B, Hkv):
     for kvh in range(Hkv):
         base1 = off[1] + kvh * cap[1]
         assert not ck[base1:base1 + cap[1]].any(), "the request with too small a capacity is not packed"
+
+
+# ---------------------------------------------------------------------------
+# Long units split many ways (the automatic plan of small batches)
+# ---------------------------------------------------------------------------
+@pytest.mark.parametrize("splits", [16, 32])
+def test_many_split_workspace_merge(splits):
+    """16 and 32 splits per unit (the automatic plan at batch 1-2 for long contexts), merged
+    from the workspace: dense attention, the slow step's scores and the fast step against
+    the oracle; the counters are left zeroed."""
+    sfi = _sfi()
+    lens = [8200, 6000, 17, 5100]
+    prob = Problem(seed=60 + splits, lens=lens, Hq=16, Hkv=8, D=128, S=4, W=32, heavy_frac=0.02).to_device()
+    maxL = 8216
+    assert sfi.sfi_plan_splits(prob.shape, prob.B, maxL, splits) == splits
+    stride = 8216
+    scores = torch.full((prob.B, prob.Hkv, stride), float("nan"), device="cuda")
+    out, lse = _dense(prob, num_splits=splits, scores=scores, max_tokens=maxL)
+    sc = scores.cpu().numpy()
+    for r in range(prob.B):
+        o_ref, l_ref = prob.oracle_dense(r)
+        assert_close(out[r], o_ref, f"dense out r={r}")
+        assert_close(lse[r], l_ref, f"dense lse r={r}")
+        L = prob.lens[r]
+        ref = prob.oracle_scores(r, stride)
+        masked = np.isneginf(ref[:, :L])
+        assert np.array_equal(np.isneginf(sc[r, :, :L]), masked)
+        err = np.abs(sc[r, :, :L][~masked].astype(np.float64) - ref[:, :L][~masked])
+        assert (err <= prob.score_bound(r, stride)[:, :L][~masked]).all(), err.max()
+    # the fast step with a selection long enough for the same split count
+    _fast_case(70 + splits, [8200, 6000, 5100], 16, 8, 128, 4, 32, [4300, 4100, 4200], 4300, splits=splits)
+
+
+def test_many_split_workspace_merge_bad_page_and_timeout():
+    """32 splits through the workspace: a bad page id (in one split) keeps the unit's
+    outputs unwritten, a launch whose waits ran out writes nothing, and the counters are
+    left zeroed either way."""
+    sfi = _sfi()
+    splits = 32
+    prob = Problem(seed=81, lens=[8200, 8200], Hq=16, Hkv=8, D=128, S=4, W=32).to_device()
+    maxL = 8216
+    ws = sfi.alloc_workspace(prob.shape, 2, maxL, splits)
+    pt = prob.d_kv.page_table.clone()
+    pt[1, 300] = 10_000_000
+    bad = sfi.PagedKV(prob.d_kv.k_pool, prob.d_kv.v_pool, pt, prob.d_kv.seq_lens)
+    out = torch.full((2, 16, 128), float("nan"), device="cuda")
+    lse = torch.full((2, 16), float("nan"), device="cuda")
+    st = _status()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, bad, 4, 32, prob.d_q, out, lse, None, max_tokens=maxL,
+                                        num_splits=splits, workspace=ws, dev_status=st)
+    torch.cuda.synchronize()
+    assert st.item() == 1, f"status {st.item()}"
+    o, l = out.cpu().numpy(), lse.cpu().numpy()
+    assert np.isnan(o[1]).all() and np.isnan(l[1]).all()
+    o_ref, l_ref = prob.oracle_dense(0)
+    assert_close(o[0], o_ref, "the healthy request")
+    assert counters_zero(ws, 2 * prob.Hkv)
+    out.fill_(float("nan"))
+    st.zero_()
+    sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, 4, 32, prob.d_q, out, None, None, max_tokens=maxL,
+                                        num_splits=splits, workspace=ws, dev_status=st,
+                                        flags=sfi.SFI_ATTN_TEST_WITHHOLD)
+    torch.cuda.synchronize()
+    assert st.item() & 16, f"status {st.item()}"
+    assert np.isnan(out.cpu().numpy()).all(), "a timed-out launch writes no output"
+    assert counters_zero(ws, 2 * prob.Hkv), "split counters must be left zeroed after a timeout"
