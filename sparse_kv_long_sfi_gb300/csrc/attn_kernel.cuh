@@ -57,6 +57,9 @@ struct AttnTile {
     // After the ring: where the other CTAs of a cluster push their partial results.
     static constexpr int kRecvOffset = kStages * kStageBytes;
     static constexpr int kRecvBytes = 13 * 1024;
+    // Multi-token kernels keep the 16-row query tile in the last kQBytes of the receive
+    // region (128-byte rows swizzled in 16-byte chunks), out of reach of the pushes.
+    static constexpr int kQBytes = kMaxRows * D * 2;
     static constexpr int kSmemBytes = kRecvOffset + kRecvBytes + 1024;  // + alignment slack
     static constexpr int kKSteps = D / 16;                       // mma k-steps of QK^T
     static constexpr int kNTiles = D / 8;                        // mma n-tiles of PV
@@ -340,8 +343,8 @@ struct RowSpan {
 // row sees all 16 tokens; [lo, hi) is the union of the rows' spans.
 template <int D, bool SCORES>
 __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t vaddr, int lo, int hi, bool full,
-                                                     RowSpan ra, RowSpan rb, int pos0,
-                                                     const uint32_t (&qa)[D / 16][4], float (&o)[D / 8][4],
+                                                     RowSpan ra, RowSpan rb, int pos0, uint32_t qtile,
+                                                     float (&o)[D / 8][4],
                                                      float (&m_run)[2], float (&l_run)[2], const AttnParams &p,
                                                      float *score_row, int L, int lane) {
     using T = AttnTile<D>;
@@ -352,14 +355,19 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
     {
         const int tok = ((mi >> 1) << 3) + r8;
         const uint32_t row_addr = kaddr + tok * 128;
+        // A fragments from the query tile: lane l addresses row (l & 7) + 8 * ((l >> 3) & 1)
+        // and the k-half l >> 4 of each 16-column step
+        const int qr = r8 + ((mi & 1) << 3);
+        const uint32_t qrow_addr = qtile + qr * (D * 2);
 #pragma unroll
         for (int ks = 0; ks < T::kKSteps; ++ks) {
             const int box = ks >> 2;
             const int chunk = ((ks & 3) << 1) + (mi & 1);
-            uint32_t b0, b1, b2, b3;
+            uint32_t a0, a1, a2, a3, b0, b1, b2, b3;
+            ldsm_x4(qrow_addr + (((2 * ks + (mi >> 1)) ^ r8) << 4), a0, a1, a2, a3);
             ldsm_x4(row_addr + box * (kSubTokens * 128) + ((chunk ^ r8) << 4), b0, b1, b2, b3);
-            mma_bf16_16816(s[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-            mma_bf16_16816(s[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+            mma_bf16_16816(s[0], a0, a1, a2, a3, b0, b1);
+            mma_bf16_16816(s[1], a0, a1, a2, a3, b2, b3);
         }
     }
     // this lane's tokens, and its elements of rows g (xa) and g + 8 (xb)
@@ -599,60 +607,67 @@ __host__ __device__ constexpr bool cluster_push_fits(int splits, int rows, int r
     return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= recv_bytes;
 }
 
-// Workspace merge of one unit's `nparts` partial states, in workspace slots
-// slot0 + [0, nparts) (rows per slot kRows, this CTA's own already written): the CTA
-// that arrives last merges them. Run by the consumer threads (threadIdx.x < 128).
-// `bar` is an mbarrier (count 1) for the bulk copies, `stage` (stage_bytes) and
-// `scratch` shared memory this CTA no longer needs. A partial with l < 0 comes from a
-// split that must not write: the merge then writes nothing for the unit.
+// Workspace merge of one unit's `nparts` partial states (this CTA's own already
+// written): the CTA that arrives last merges them. A unit's partials are packed
+// densely from the start of its region: (m, l) of split s, row `row` at float pair
+// slot0 * kRows + s * rows + row of ws_ml, its output row at the same index (times D)
+// of ws_part, so a batch of splits is one contiguous block of each. Run by the consumer
+// threads (threadIdx.x < 128). `bar` is an mbarrier (count 1) for the bulk copies,
+// `stage` (stage_bytes) and `scratch` shared memory this CTA no longer needs. A partial
+// with l < 0 comes from a split that must not write: the merge then writes nothing for
+// the unit.
 template <int D, int kRows, typename OutRow>
 __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *bar, int *s_last, int rows, int nparts,
                                                 int64_t unit, int64_t slot0, float *stage, int stage_bytes,
                                                 float *scratch, OutRow out_row) {
     const int ctid = threadIdx.x;  // 0 .. 127
-    const int splits = nparts;
-    uint64_t *merge_bar = bar;
-    float *recv = scratch;
     // Every split arrives (a failed one with l = -1), so the counter always completes and
     // the last CTA leaves it zeroed for the next launch. One thread per CTA publishes
-    // the CTA's partial (release fence after the barrier, then the counter) and, in the
-    // last CTA, acquires the others' before the barrier that lets the merge start.
+    // the CTA's partial and, in the last CTA, acquires the others' with one acquire-
+    // release update of the counter after the CTA barrier.
     consumer_bar_sync();
     if (ctid == 0) {
-        asm volatile("fence.acq_rel.gpu;" ::: "memory");
-        const int prev = atomicAdd(&p.ws_count[unit], 1);
-        *s_last = (prev == splits - 1);
-        if (*s_last) {
-            asm volatile("fence.acq_rel.gpu;" ::: "memory");
-            p.ws_count[unit] = 0;
-        }
+        int prev;
+        asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&p.ws_count[unit]) : "memory");
+        *s_last = (prev == nparts - 1);
+        if (*s_last) p.ws_count[unit] = 0;
     }
     consumer_bar_sync();
     if (!*s_last) return;
-    // The unit's partials come into shared memory (`stage`, the ring: free once this CTA's
-    // own partial is in the workspace) by bulk copies, in batches of whole splits: the
-    // (m, l) block of the batch, then each split's rows x D partial output, issued by the
-    // lanes of warp 0 in parallel. Per batch, warps first derive each row's maximum,
-    // normaliser and per-split weights (in `recv`, unused without a cluster); each thread
-    // then sums its 4-float output chunks with those weights and folds the batch into its
-    // running state.
+    // The partials come into shared memory by two bulk copies per batch of splits (the
+    // batch's (m, l) block and its output rows). Per batch, warps first derive each row's
+    // maximum, normaliser and per-split weights (in `scratch`); each thread then sums its
+    // 4-float output chunks with those weights and folds the batch into its running
+    // state. (Copies issued one per split cost about 40 ns each to issue; loading the
+    // partials with plain loads took longer to arrive.)
     const int warp = ctid >> 5, lane = ctid & 31;
     constexpr int kC = D / 4;  // 4-float chunks per row
-    constexpr int kCpt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
-    const int o_floats = rows * D;
-    const int nbmax = stage_bytes / (kRows * 2 * 4 + o_floats * 4);
-    float *ml_st = stage;                        // [nbmax][kRows][2]
-    float *o_st = stage + nbmax * kRows * 2;     // [nbmax][rows][D]
-    float *w_st = recv;                          // [nbmax][kRows] weights e^(m - M_batch), 0 for l <= 0
-    float *mb_st = recv + nbmax * kRows;         // [kRows] batch maximum
-    float *lb_st = mb_st + kRows;                // [kRows] batch normaliser, -1 if a split failed
+    constexpr int kThreads = kConsumerWarps * 32;
+    constexpr int kCpt = (kRows * kC + kThreads - 1) / kThreads;
+    const int ml_split = rows * 2, o_split = rows * D;             // floats per split
+    const int nfit = (stage_bytes / 4 / (ml_split + o_split)) & ~1;  // even: batches start 16-byte aligned
+    const int ml_cap = nfit * ml_split + 4;                         // + the 16-byte rounding of the copy
+    const int nbmax = min(nfit, (stage_bytes / 4 - ml_cap) / o_split & ~1);
+    float *ml_st = stage;                                           // [nbmax][rows][2] (+ slack)
+    float *o_st = stage + ml_cap;                                   // [nbmax][rows][D]
+    float *w_st = scratch;                                          // [nbmax][rows] weights, 0 for l <= 0
+    float *mb_st = scratch + nbmax * rows;                          // [rows] batch maximum
+    float *lb_st = mb_st + kRows;                                   // [rows] batch normaliser, -1 if failed
+    const float *ml_g = p.ws_ml + slot0 * kRows * 2;
+    const float *o_g = p.ws_part + slot0 * kRows * D;
+    // Each 4-float output chunk is summed by a group of tpc consecutive threads (more than
+    // one when there are fewer chunks than threads), member i taking splits i, i + tpc, ...
+    const int nchunk = rows * kC;
+    int tpc = 1;
+    while (tpc < 32 && 2 * tpc * nchunk <= kThreads) tpc *= 2;
+    const int member = ctid & (tpc - 1), ngrp = kThreads / tpc;
     float4 acc[kCpt];
     float Mr[kCpt], Lr[kCpt];
     int crow[kCpt], cd[kCpt];
 #pragma unroll
     for (int j = 0; j < kCpt; ++j) {
-        const int c = ctid + j * kConsumerWarps * 32;
-        crow[j] = c < rows * kC ? c / kC : -1;
+        const int c = ctid / tpc + j * ngrp;
+        crow[j] = c < nchunk ? c / kC : -1;
         cd[j] = (c - (c / kC) * kC) * 4;
         acc[j] = make_float4(0.f, 0.f, 0.f, 0.f);
         Mr[j] = -INFINITY;
@@ -661,21 +676,18 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
     bool fail = false;
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");  // earlier generic use of the ring
     consumer_bar_sync();
-    for (int b0 = 0, batch = 0; b0 < splits; b0 += nbmax, ++batch) {
-        const int nbt = min(nbmax, splits - b0);
-        if (warp == 0) {
-            const uint32_t ml_bytes = (uint32_t)(nbt * kRows * 2 * 4), o_bytes = (uint32_t)(o_floats * 4);
-            if (lane == 0) mbar_arrive_expect_tx(merge_bar, ml_bytes + (uint32_t)nbt * o_bytes);
-            __syncwarp();
+    for (int b0 = 0, batch = 0; b0 < nparts; b0 += nbmax, ++batch) {
+        const int nbt = min(nbmax, nparts - b0);
+        if (ctid == 0) {
+            // the (m, l) block rounded up to 16 bytes (the slack stays inside the unit's region)
+            const uint32_t ml_bytes = ((uint32_t)(nbt * ml_split * 4) + 15u) & ~15u;
+            const uint32_t o_bytes = (uint32_t)(nbt * o_split * 4);
             asm volatile("fence.proxy.async.global;" ::: "memory");  // the acquired partials, to the copies
-            for (int i = lane; i <= nbt; i += 32) {
-                if (i == nbt)
-                    bulk_load_1d(ml_st, &p.ws_ml[(slot0 + b0) * kRows * 2], ml_bytes, merge_bar);
-                else
-                    bulk_load_1d(o_st + i * o_floats, &p.ws_part[(slot0 + b0 + i) * kRows * D], o_bytes, merge_bar);
-            }
+            mbar_arrive_expect_tx(bar, ml_bytes + o_bytes);
+            bulk_load_1d(ml_st, ml_g + (int64_t)b0 * ml_split, ml_bytes, bar);
+            bulk_load_1d(o_st, o_g + (int64_t)b0 * o_split, o_bytes, bar);
         }
-        const bool got = mbar_wait_warp(merge_bar, batch & 1);
+        const bool got = mbar_wait_warp(bar, batch & 1);
         if (!got && lane == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
         if (got) {
             // per row of the batch: maximum, normaliser and weights (warp w: rows w, w + 4, ...)
@@ -683,7 +695,7 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
                 float M = -INFINITY;
                 bool f = false;
                 for (int i = lane; i < nbt; i += 32) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + row) * 2]);
+                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * rows + row) * 2]);
                     f |= ml.y < 0.f;
                     if (ml.y > 0.f) M = fmaxf(M, ml.x);
                 }
@@ -691,9 +703,9 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
                 for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
                 float Ls = 0.f;
                 for (int i = lane; i < nbt; i += 32) {
-                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * kRows + row) * 2]);
+                    const float2 ml = *reinterpret_cast<const float2 *>(&ml_st[(i * rows + row) * 2]);
                     const float wgt = ml.y > 0.f ? fast_exp2(ml.x - M) : 0.f;
-                    w_st[i * kRows + row] = wgt;
+                    w_st[i * rows + row] = wgt;
                     Ls += ml.y > 0.f ? ml.y * wgt : 0.f;
                 }
 #pragma unroll
@@ -712,20 +724,28 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
         }
 #pragma unroll
         for (int j = 0; j < kCpt; ++j) {
-            if (crow[j] < 0) continue;
-            const float Lb = lb_st[crow[j]];
+            const int row = crow[j];
+            const float Lb = row >= 0 ? lb_st[row] : 0.f;
             fail |= Lb < 0.f;
-            if (Lb <= 0.f) continue;
             float4 ab = make_float4(0.f, 0.f, 0.f, 0.f);
-            for (int i = 0; i < nbt; ++i) {
-                const float wgt = w_st[i * kRows + crow[j]];
-                const float4 o = *reinterpret_cast<const float4 *>(&o_st[i * o_floats + crow[j] * D + cd[j]]);
-                ab.x += o.x * wgt;
-                ab.y += o.y * wgt;
-                ab.z += o.z * wgt;
-                ab.w += o.w * wgt;
+            if (Lb > 0.f) {
+                for (int i = member; i < nbt; i += tpc) {
+                    const float wgt = w_st[i * rows + row];
+                    const float4 o = *reinterpret_cast<const float4 *>(&o_st[(i * rows + row) * D + cd[j]]);
+                    ab.x += o.x * wgt;
+                    ab.y += o.y * wgt;
+                    ab.z += o.z * wgt;
+                    ab.w += o.w * wgt;
+                }
             }
-            const float Mb = mb_st[crow[j]];
+            for (int off = 1; off < tpc; off <<= 1) {  // the group's sum, in every member
+                ab.x += __shfl_xor_sync(0xffffffffu, ab.x, off);
+                ab.y += __shfl_xor_sync(0xffffffffu, ab.y, off);
+                ab.z += __shfl_xor_sync(0xffffffffu, ab.z, off);
+                ab.w += __shfl_xor_sync(0xffffffffu, ab.w, off);
+            }
+            if (Lb <= 0.f) continue;
+            const float Mb = mb_st[row];
             const float Mn = fmaxf(Mr[j], Mb);
             const float a = Lr[j] > 0.f ? fast_exp2(Mr[j] - Mn) : 0.f;
             const float bb = fast_exp2(Mb - Mn);
@@ -742,8 +762,7 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
         consumer_bar_sync();
     }
     // A failed split fails every row of the unit; make the decision CTA-wide.
-    fail = consumer_bar_or(fail);
-    if (fail) return;
+    if (consumer_bar_or(fail) || member != 0) return;
 #pragma unroll
     for (int j = 0; j < kCpt; ++j) {
         if (crow[j] < 0) continue;
@@ -910,6 +929,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                        const AttnParams p) {
     using T = AttnTile<D>;
     constexpr int kRows = MQ ? kMaxRows : kMaxGroup;  // query rows per unit in the merge buffers
+    // bytes of the receive region open to the cluster push (the rest holds the query tile)
+    constexpr int kPushBytes = MQ ? T::kRecvBytes - T::kQBytes : T::kRecvBytes;
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     __shared__ __align__(8) uint64_t full_bar[T::kStages];
@@ -988,7 +1009,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     const int sb_begin = split * per;
     const int sb_end = min(u.nb, sb_begin + per);
     const int n_my = max(0, sb_end - sb_begin);
-    const int n_stages = (n_my + kConsumerWarps - 1) / kConsumerWarps;
+    // Stage st holds sub-blocks sb0 + 4 st + [0, 4) that lie in [sb_begin, sb_end). When
+    // the split's count is not a multiple of 4 the partial stage comes first, where the
+    // warps wait for the pipeline to fill anyway, so all four finish the last stage
+    // together.
+    const int pad = (kConsumerWarps - n_my % kConsumerWarps) % kConsumerWarps;
+    const int sb0 = sb_begin - pad;
+    const int n_stages = (n_my + pad) / kConsumerWarps;
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < T::kStages; ++i) {
@@ -999,7 +1026,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         // workspace merge: the last CTA's bulk copies of the unit's partials
         if (CLUSTER)
             mbar_init(&merge_bar, split != 0 ? 1u
-                                  : cluster_push_fits<D>(splits, MQ ? p.rows : p.group)
+                                  : cluster_push_fits<D>(splits, MQ ? p.rows : p.group, kPushBytes)
                                       ? (uint32_t)(splits - 1) * kConsumerWarps * 32
                                       : (uint32_t)(splits - 1));
         else
@@ -1020,11 +1047,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
         // Page id of sub-block sb (-1 for compact sub-blocks and past the end).
         auto page_of = [&](int sb) -> int {
-            if (sb >= sb_end || sb < u.nb1) return -1;
+            if (sb >= sb_end || sb < sb_begin || sb < u.nb1) return -1;
             return ptab[u.page0 + (sb - u.nb1)];
         };
-        int cur = page_of(sb_begin + lane);
-        int nxt = page_of(sb_begin + 32 + lane);
+        int cur = page_of(sb0 + lane);
+        int nxt = page_of(sb0 + 32 + lane);
         // L2 prefetch of stage pst's sub-blocks (page ids of its chunk of 32 in page_src;
         // warp-collective). Dense units prefetch the rest of their first chunk right after
         // the ring's first fill, so the first refills read L2 without delaying the ring's
@@ -1033,8 +1060,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         // most one CTA per SM made them slower: batch-1 dense at 16K, 21.2 -> 23.7 us.)
         auto prefetch_stage = [&](int pst, int page_src) {
             const int page = __shfl_sync(0xffffffffu, page_src, ((pst & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1)));
-            const int sb = sb_begin + pst * kConsumerWarps + lane;
-            if (lane < kConsumerWarps && sb < sb_end) {
+            const int sb = sb0 + pst * kConsumerWarps + lane;
+            if (lane < kConsumerWarps && sb >= sb_begin && sb < sb_end) {
                 if (sb < u.nb1) {  // compact rows
                     const int32_t y = static_cast<int32_t>(u.crow0 + (int64_t)sb * kSubTokens);
 #pragma unroll
@@ -1055,7 +1082,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         for (int st = 0; st < n_stages; ++st) {
             if (st > 0 && (st & 7) == 0) {  // 8 stages x 4 sub-blocks = 32 page ids per chunk
                 cur = nxt;
-                nxt = page_of(sb_begin + (st / 8 + 1) * 32 + lane);
+                nxt = page_of(sb0 + (st / 8 + 1) * 32 + lane);
             }
             const int slot = st % T::kStages;
             if (st >= T::kStages) {
@@ -1067,16 +1094,16 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             if (p.withhold == st + 1) continue;  // diagnostic: this stage's copies never come
             // A stage of compact sub-blocks needs no page id; skipping the shuffle there keeps
             // the page-table loads off the path of the first TMA copies.
-            const bool paged = sb_begin + (st + 1) * kConsumerWarps > u.nb1;  // warp-uniform
+            const bool paged = sb0 + (st + 1) * kConsumerWarps > u.nb1;  // warp-uniform
             const int page =
                 paged ? __shfl_sync(0xffffffffu, cur, ((st & 7) * kConsumerWarps) + (lane & (kConsumerWarps - 1))) : -1;
             if (lane < kConsumerWarps) {
-                const int sb = sb_begin + st * kConsumerWarps + lane;
+                const int sb = sb0 + st * kConsumerWarps + lane;
                 int lo = 0, hi = 0, pos0 = 0;
                 const CUtensorMap *mk = &tm_pool_k;
                 const CUtensorMap *mv = &tm_pool_v;
                 int32_t y = 0;
-                if (sb < sb_end) {
+                if (sb >= sb_begin && sb < sb_end) {
                     if (sb < u.nb1) {  // compact segment (fast mode only)
                         mk = &tm_comp_k;
                         mv = &tm_comp_v;
@@ -1123,27 +1150,26 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     }
     const int g = lane >> 2, t = lane & 3;
     const int G = p.group;
-    uint32_t qa[D / 16][MQ ? 4 : 2];
+    uint32_t qa[D / 16][2];
+    const uint32_t qtile = smem_u32(smem + T::kRecvOffset + T::kRecvBytes - T::kQBytes);
     if constexpr (MQ) {
-        // rows g (A-fragment registers 0, 2) and g + 8 (registers 1, 3); row rho is
-        // query token rho / G, head rho % G of this KV head's group
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {
-            const int rho = g + 8 * half;
-            const int tok = rho / G;
-            const __nv_bfloat16 *qrow =
-                p.q + (((int64_t)r * p.tokens + tok) * p.hq + (int64_t)kvh * G + (rho - tok * G)) * D;
-#pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks) {
-                if (rho < p.rows) {
-                    qa[ks][half] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 2 * t);
-                    qa[ks][2 + half] = *reinterpret_cast<const uint32_t *>(qrow + ks * 16 + 8 + 2 * t);
-                } else {
-                    qa[ks][half] = 0u;
-                    qa[ks][2 + half] = 0u;
-                }
+        // The 16-row query tile goes to shared memory (row rho is query token rho / G,
+        // head rho % G of this KV head's group; rows past p.rows are zero), 16-byte
+        // chunk c of row rho at chunk c ^ (rho & 7): the A fragments are read with
+        // ldmatrix in each sub-block, which keeps 32 registers free.
+        constexpr int kChunks = D / 8;
+        uint8_t *qt = smem + T::kRecvOffset + T::kRecvBytes - T::kQBytes;
+        for (int e = threadIdx.x; e < kMaxRows * kChunks; e += kConsumerWarps * 32) {
+            const int rho = e / kChunks, c = e - rho * kChunks;
+            int4 v = make_int4(0, 0, 0, 0);
+            if (rho < p.rows) {
+                const int tok = rho / G;
+                v = *reinterpret_cast<const int4 *>(
+                    p.q + (((int64_t)r * p.tokens + tok) * p.hq + (int64_t)kvh * G + (rho - tok * G)) * D + c * 8);
             }
+            *reinterpret_cast<int4 *>(qt + rho * (D * 2) + ((c ^ (rho & 7)) << 4)) = v;
         }
+        consumer_bar_sync();
     } else {
         const __nv_bfloat16 *qrow = p.q + ((int64_t)r * p.hq + (int64_t)kvh * G + g) * D;
 #pragma unroll
@@ -1188,7 +1214,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     }
 
     if (!MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end &&
-        (u.sb_app - sb_begin) % kConsumerWarps == warp)
+        (u.sb_app - sb0) % kConsumerWarps == warp)
         stage_current_token<D>(p, r, kvh, u, lane, s_app_val, &s_app_page);
     bool timed_out = false;
     for (int st = 0; st < n_stages; ++st) {
@@ -1199,7 +1225,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
         const int2 in = s_info[slot][warp];
         const int lo = in.x & 0xffff, hi = in.x >> 16;
-        if (!MQ && p.k_new != nullptr && u.sb_app < sb_end && sb_begin + st * kConsumerWarps + warp == u.sb_app) {
+        const int sb_me = sb0 + st * kConsumerWarps + warp;  // this warp's sub-block in the stage
+        if (!MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end && sb_me == u.sb_app) {
             // Fused append: the current token's K/V replace row L - 1 of this tile (the
             // attention sees the cache after the append) and are written to the pages.
             // Only the split that owns that sub-block does it (a stage's padding slots
@@ -1207,7 +1234,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane,
                                   s_app_val, &s_app_page, &s_bad);
         }
-        if (MQ && p.k_new != nullptr && in.y >= 0 && sb_begin + st * kConsumerWarps + warp < sb_end &&
+        if (MQ && p.k_new != nullptr && in.y >= 0 && sb_me >= sb_begin && sb_me < sb_end &&
             in.y + kSubTokens > u.L0 - 1 && in.y < u.L) {
             // Fused append of the query tokens (positions [L - T, L)) in this paged sub-block.
             fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane,
@@ -1221,14 +1248,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     ra = RowSpan{max(lo, row_lo[0] - in.y), min(hi, row_len[0] - in.y)};
                     rb = RowSpan{max(lo, row_lo[1] - in.y), min(hi, row_len[1] - in.y)};
                 } else {  // compact rows: without a selection they are the sink positions
-                    const int c0 = (sb_begin + st * kConsumerWarps + warp) * kSubTokens;
+                    const int c0 = sb_me * kSubTokens;
                     ra = RowSpan{lo, u.cnt > 0 ? hi : min(hi, row_len[0] - c0)};
                     rb = RowSpan{lo, u.cnt > 0 ? hi : min(hi, row_len[1] - c0)};
                 }
                 const bool full = __all_sync(0xffffffffu, ra.lo == 0 && ra.hi == kSubTokens && rb.lo == 0 &&
                                                               rb.hi == kSubTokens);
-                consume_sub_block_mq<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, full, ra, rb, in.y, qa, o,
-                                                m_run, l_run, p, score_row, u.L, lane);
+                consume_sub_block_mq<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, full, ra, rb, in.y, qtile,
+                                                o, m_run, l_run, p, score_row, u.L, lane);
             } else {
                 consume_sub_block<D, SCORES>(kaddr, kaddr + T::kSubBytes, lo, hi, in.y, qa, o, m_run[0], l_run[0],
                                              p, score_row, u.L, lane);
@@ -1321,7 +1348,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                     cp_l[row] = lsum;
                 }
             } else {
-                const int64_t slot = (slot0 + split) * kRows + row;
+                const int64_t slot = slot0 * kRows + (int64_t)split * rows + row;  // packed per unit
                 p.ws_part[slot * D + d] = acc;
                 if (d == 0) {
                     p.ws_ml[slot * 2 + 0] = M;
@@ -1335,14 +1362,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 cp_m[row] = -INFINITY;
                 cp_l[row] = -1.f;
             } else {
-                const int64_t slot = (slot0 + split) * kRows + row;
+                const int64_t slot = slot0 * kRows + (int64_t)split * rows + row;
                 p.ws_ml[slot * 2 + 0] = -INFINITY;
                 p.ws_ml[slot * 2 + 1] = -1.f;
             }
         }
     }
     if (splits == 1) return;
-    merge_splits<D, kRows, CLUSTER>(p, reinterpret_cast<float *>(smem + T::kRecvOffset), T::kRecvBytes, &merge_bar,
+    merge_splits<D, kRows, CLUSTER>(p, reinterpret_cast<float *>(smem + T::kRecvOffset), kPushBytes, &merge_bar,
                                      &s_last, cp_o, cp_m, cp_l, rows, splits, split, unit, slot0,
                                      reinterpret_cast<float *>(smem), T::kRingBytes, out_row);
 }
