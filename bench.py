@@ -73,8 +73,10 @@ def parse_args():
     ap.add_argument("--sections", default=",".join(SECTIONS),
                     help="comma list of the sections after the headline: " + ", ".join(SECTIONS))
     ap.add_argument("--ragged-requests", type=int, default=64, help="requests of the ragged mixed-step section")
+    ap.add_argument("--spec-tokens", default="1,2,4,8", help="comma list of draft/verify token counts (speculative)")
     args = ap.parse_args()
     args.sections = [x for x in args.sections.split(",") if x]
+    args.spec_tokens = [int(x) for x in args.spec_tokens.split(",") if x]
     unknown = set(args.sections) - set(SECTIONS)
     if unknown:
         ap.error(f"unknown sections {sorted(unknown)}")
@@ -515,7 +517,8 @@ def run_gpu(args, ranks: Ranks):
         result["retention_sweep"] = retention_sweep(cy, dev, peak)
     if "speculative" in sections:
         result["speculative_sweep"] = speculative_sweep(dec, cy.layers, cy.batch, cy.shape, cy.q_all, cy.seq_steps,
-                                                        NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak, seed0)
+                                                        NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak, seed0,
+                                                        tokens=args.spec_tokens)
     cy.free()
     del cy, dec, g_cycle
     torch.cuda.empty_cache()
@@ -832,7 +835,7 @@ def retention_sweep(cy, dev, peak):
 
 
 def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak,
-                      seed0):
+                      seed0, tokens=(1, 2, 4, 8)):
     """Self-speculative decoding's two passes over all layers ("A Sparse Glimpse of the
     Whole", abstract): verification of T tokens (T-token append + causal dense
     attention + the recycled statistic) and a T-token draft pass over the sparse state
@@ -872,7 +875,7 @@ def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hk
         sfi.sfi_compact_gather(shape, kv, Lb.idx, Lb.compact.count, S, Lb.compact, stream=dec.main)
     torch.cuda.synchronize()
     rows = []
-    for T in (1, 2, 4, 8):
+    for T in tokens:
         L = L0 + T
         seq = torch.full((B,), L, dtype=torch.int32, device=dev)
         q = torch.empty((NL, B, T, Hq, D), dtype=torch.bfloat16, device=dev)
