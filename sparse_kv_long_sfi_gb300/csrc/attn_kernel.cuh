@@ -87,22 +87,38 @@ __device__ __forceinline__ bool consumer_bar_or(bool v) {
     return r != 0;
 }
 
-// Whether any page id of positions [0, L) of request r lies outside the pool. Called by
+// Whether any page id of positions [0, L) of request r lies outside the pool, checked by
 // every consumer thread before the first score write of a unit, so a unit with a bad
 // page writes none of its scores (the pages are checked again as they are streamed).
-__device__ __forceinline__ bool request_pages_bad(const AttnParams &p, int r, int L) {
+// In two parts: pages_first issues this thread's first eight loads (the first 1024
+// pages), which can happen before the grid dependency wait; pages_bad finishes the
+// check (the rest of the pages, then a barrier reduction over the consumer threads).
+constexpr int kPageCheckLoads = 8;
+__device__ __forceinline__ void pages_first(const AttnParams &p, int r, int L, int (&pg)[kPageCheckLoads]) {
+    const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+    const int npg = (L + kSubTokens - 1) / kSubTokens;
+#pragma unroll
+    for (int j = 0; j < kPageCheckLoads; ++j) {
+        const int i = threadIdx.x + j * kConsumerWarps * 32;
+        pg[j] = i < npg ? __ldg(ptab + i) : 0;
+    }
+}
+__device__ __forceinline__ bool pages_bad(const AttnParams &p, int r, int L, const int (&first)[kPageCheckLoads]) {
     const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
     const int npg = (L + kSubTokens - 1) / kSubTokens;
     bool bad = false;
-    for (int i0 = threadIdx.x; i0 < npg; i0 += 8 * kConsumerWarps * 32) {
-        int pg[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {  // eight independent loads in flight
+    for (int j = 0; j < kPageCheckLoads; ++j) bad |= first[j] < 0 || first[j] >= p.num_pages;
+    for (int i0 = threadIdx.x + kPageCheckLoads * kConsumerWarps * 32; i0 < npg;
+         i0 += kPageCheckLoads * kConsumerWarps * 32) {
+        int pg[kPageCheckLoads];
+#pragma unroll
+        for (int j = 0; j < kPageCheckLoads; ++j) {  // eight independent loads in flight
             const int i = i0 + j * kConsumerWarps * 32;
             pg[j] = i < npg ? __ldg(ptab + i) : 0;
         }
 #pragma unroll
-        for (int j = 0; j < 8; ++j) bad |= pg[j] < 0 || pg[j] >= p.num_pages;
+        for (int j = 0; j < kPageCheckLoads; ++j) bad |= pg[j] < 0 || pg[j] >= p.num_pages;
     }
     return consumer_bar_or(bad);
 }
@@ -1156,10 +1172,17 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     }
 
     // ---------------- consumer warps ----------------
+    // Units that write scores first check every page id of the request; with
+    // early_prefetch the page table is not written by the preceding kernel, so the first
+    // loads of that check go out before the dependency wait.
+    const bool check_pages = SCORES && p.scores && !fast && u.L <= p.score_stride;
+    int pg_first[kPageCheckLoads];
+    if (check_pages && p.early_prefetch) pages_first(p, r, u.L, pg_first);
     if (p.early_prefetch) {
         grid_dependency_wait();
         grid_launch_dependents();
     }
+    if (check_pages && !p.early_prefetch) pages_first(p, r, u.L, pg_first);
     const int g = lane >> 2, t = lane & 3;
     const int G = p.group;
     uint32_t qa[D / 16][2];
@@ -1212,10 +1235,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};  // rows g and g + 8 (MQ)
     float *score_row = nullptr;
     if (SCORES && p.scores && !fast) {
-        if (u.L <= p.score_stride) {
+        if (check_pages) {
             // Scores are written as the stream goes; a unit with a bad page id anywhere in
             // [0, L) writes none of them (nor its output: the flag reaches the merge).
-            if (!request_pages_bad(p, r, u.L)) {
+            if (!pages_bad(p, r, u.L, pg_first)) {
                 score_row = p.scores + ((int64_t)r * p.hkv + kvh) * p.score_stride;
             } else if (threadIdx.x == 0) {
                 s_bad = 1;
