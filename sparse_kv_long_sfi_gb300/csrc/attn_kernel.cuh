@@ -332,13 +332,23 @@ __device__ __forceinline__ void fuse_tokens(uint8_t *tile, const AttnParams &p, 
         const __nv_bfloat16 *src0 = (is_v ? p.v_new : p.k_new) + (int64_t)kvh * D + c * 8;
         __nv_bfloat16 *dst0 = (is_v ? p.v_pool_w : p.k_pool_w) + ((int64_t)page * p.hkv + kvh) * kSubTokens * D + c * 8;
         uint8_t *base0 = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128);
-#pragma unroll 4
-        for (int pos = first; pos < last; ++pos) {
-            const int tok = pos - (L - ntok);
-            const int4 val = *reinterpret_cast<const int4 *>(src0 + ((int64_t)r * ntok + tok) * p.hkv * D);
-            const int row = pos - pos0;
-            *reinterpret_cast<int4 *>(base0 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val;
-            if (page_ok) *reinterpret_cast<int4 *>(dst0 + (int64_t)row * D) = val;
+        // up to 8 tokens per round, every load of a round issued before its stores
+        for (int pos8 = first; pos8 < last; pos8 += 8) {
+            int4 val[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int tok = pos8 + j - (L - ntok);
+                if (pos8 + j < last)
+                    val[j] = *reinterpret_cast<const int4 *>(src0 + ((int64_t)r * ntok + tok) * p.hkv * D);
+            }
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const int row = pos8 + j - pos0;
+                if (pos8 + j < last) {
+                    *reinterpret_cast<int4 *>(base0 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) = val[j];
+                    if (page_ok) *reinterpret_cast<int4 *>(dst0 + (int64_t)row * D) = val[j];
+                }
+            }
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
@@ -553,13 +563,11 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
     }
 }
 
-// Write the current token's K/V (k_new/v_new of this KV head) into row u.row_app of
-// the swizzled K and V tiles at `tile` and into the paged cache at position L - 1.
-// One 16-byte chunk per lane; the writing lanes then order their generic-proxy
-// shared-memory writes before later TMA (async-proxy) writes into the same stage.
-// Start the loads fuse_current_token needs (the current token's K/V chunks and its page
-// id) as asynchronous copies into shared memory, so their latency overlaps the stages
-// before the one holding position L - 1.
+// Fused append of the current token (k_new/v_new of this KV head, position L - 1), in
+// three steps by the warp that owns its sub-block: stage_current_token starts
+// asynchronous copies of the token's K/V chunks and its page id into shared memory
+// before the stream; store_current_token writes them to the page early in the stream;
+// fuse_current_token puts them into the sub-block's tile when it arrives.
 template <int D>
 __device__ __forceinline__ void stage_current_token(const AttnParams &p, int r, int kvh, const UnitStream &u,
                                                     int lane, int4 *s_val, int *s_page) {
@@ -577,37 +585,134 @@ __device__ __forceinline__ void stage_current_token(const AttnParams &p, int r, 
     }
 }
 
+// Write the staged current token's K/V into the paged cache at position L - 1: done by
+// the warp that owns the token's sub-block early in the stream, so the writes drain
+// during the stream instead of at its end. A bad page id is reported and makes the
+// unit write no output.
 template <int D>
-__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const AttnParams &p, int r, int kvh,
-                                                   const UnitStream &u, int lane, const int4 *s_val,
-                                                   const int *s_page, int *s_bad) {
-    using T = AttnTile<D>;
+__device__ __forceinline__ void store_current_token(const AttnParams &p, int kvh, const UnitStream &u, int lane,
+                                                    const int4 *s_val, const int *s_page, int *s_bad) {
     constexpr int kChunks = D / 8;
     // the copies issued by stage_current_token have landed (each lane waits for its own)
     asm volatile("cp.async.wait_all;" ::: "memory");
     __syncwarp();
+    const int page = *s_page;
+    if (page < 0 || page >= p.num_pages) {
+        if (lane == 0) {
+            report(p.dev_status, SFI_DEV_BAD_PAGE);
+            *s_bad = 1;  // the unit writes no output
+        }
+    } else if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const int pos = u.L - 1;
+        __nv_bfloat16 *dst = (is_v ? p.v_pool_w : p.k_pool_w) +
+                             (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D + c * 8;
+        *reinterpret_cast<int4 *>(dst) = s_val[lane];
+    }
+}
+
+// The staged current token's K/V replace row u.row_app of the swizzled K and V tiles at
+// `tile` (the attention sees the cache after the append). One 16-byte chunk per lane;
+// the writing lanes then order their generic-proxy shared-memory writes before later
+// TMA (async-proxy) writes into the same stage.
+template <int D>
+__device__ __forceinline__ void fuse_current_token(uint8_t *tile, const UnitStream &u, int lane, const int4 *s_val) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
     if (lane < 2 * kChunks) {
         const bool is_v = lane >= kChunks;
         const int c = is_v ? lane - kChunks : lane;
-        const int4 val = s_val[lane];
         const int row = u.row_app;
         uint8_t *base = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128) + row * 128;
-        *reinterpret_cast<int4 *>(base + (((c & 7) ^ (row & 7)) << 4)) = val;
-        const int pos = u.L - 1;
-        const int page = *s_page;
-        if (page < 0 || page >= p.num_pages) {
-            if (lane == 0) {
-                report(p.dev_status, SFI_DEV_BAD_PAGE);
-                *s_bad = 1;  // the unit writes no output
-            }
-        } else {
-            __nv_bfloat16 *dst = (is_v ? p.v_pool_w : p.k_pool_w) +
-                                 (((int64_t)page * p.hkv + kvh) * kSubTokens + pos % kSubTokens) * D + c * 8;
-            *reinterpret_cast<int4 *>(dst) = val;
+        *reinterpret_cast<int4 *>(base + (((c & 7) ^ (row & 7)) << 4)) = s_val[lane];
+        asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+    }
+    __syncwarp();
+}
+
+// Multi-token form of stage_current_token: the K/V rows of the query tokens that fall in
+// the paged sub-block starting at position pos0 (k_new/v_new: [request][T][Hkv][D]) are
+// copied asynchronously into `stage` (token i = position L - T + i at i * 4D bytes: its
+// K row, then its V row), and the page id into *s_page.
+template <int D>
+__device__ __forceinline__ void stage_tokens(const AttnParams &p, int r, int kvh, int L, int pos0, int lane,
+                                             uint8_t *stage, int *s_page) {
+    constexpr int kChunks = D / 8;
+    const int ntok = p.tokens;
+    const int first = max(L - ntok, pos0), last = min(L, pos0 + kSubTokens);
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        const __nv_bfloat16 *src0 = (is_v ? p.v_new : p.k_new) + (int64_t)kvh * D + c * 8;
+        for (int pos = first; pos < last; ++pos) {
+            const int tok = pos - (L - ntok);
+            const __nv_bfloat16 *src = src0 + ((int64_t)r * ntok + tok) * p.hkv * D;
+            uint8_t *dst = stage + tok * (4 * D) + (is_v ? 2 * D : 0) + c * 16;
+            asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+        }
+    }
+    if (lane == 0) {
+        const int32_t *src = p.page_table + (int64_t)r * p.max_pages + pos0 / kSubTokens;
+        asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(s_page)), "l"(src) : "memory");
+    }
+}
+
+// Write the staged query tokens of the sub-block at pos0 into the paged cache (early in
+// the stream, like store_current_token).
+template <int D>
+__device__ __forceinline__ void store_tokens(const AttnParams &p, int kvh, int L, int pos0, int lane,
+                                             const uint8_t *stage, const int *s_page, int *s_bad) {
+    constexpr int kChunks = D / 8;
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    __syncwarp();
+    const int ntok = p.tokens;
+    const int first = max(L - ntok, pos0), last = min(L, pos0 + kSubTokens);
+    const int page = *s_page;
+    if (page < 0 || page >= p.num_pages) {
+        if (lane == 0) {
+            report(p.dev_status, SFI_DEV_BAD_PAGE);
+            *s_bad = 1;  // the unit writes no output
+        }
+    } else if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        __nv_bfloat16 *dst0 = (is_v ? p.v_pool_w : p.k_pool_w) + ((int64_t)page * p.hkv + kvh) * kSubTokens * D + c * 8;
+        for (int pos = first; pos < last; ++pos) {
+            const int tok = pos - (L - ntok);
+            *reinterpret_cast<int4 *>(dst0 + (int64_t)(pos - pos0) * D) =
+                *reinterpret_cast<const int4 *>(stage + tok * (4 * D) + (is_v ? 2 * D : 0) + c * 16);
+        }
+    }
+}
+
+// The staged query tokens replace their rows of the swizzled K and V tiles at `tile`.
+template <int D>
+__device__ __forceinline__ void fuse_staged_tokens(uint8_t *tile, const AttnParams &p, int L, int pos0, int lane,
+                                                   const uint8_t *stage) {
+    using T = AttnTile<D>;
+    constexpr int kChunks = D / 8;
+    const int ntok = p.tokens;
+    const int first = max(L - ntok, pos0), last = min(L, pos0 + kSubTokens);
+    if (lane < 2 * kChunks) {
+        const bool is_v = lane >= kChunks;
+        const int c = is_v ? lane - kChunks : lane;
+        uint8_t *base0 = tile + (is_v ? T::kSubBytes : 0) + (c >> 3) * (kSubTokens * 128);
+        for (int pos = first; pos < last; ++pos) {
+            const int tok = pos - (L - ntok), row = pos - pos0;
+            *reinterpret_cast<int4 *>(base0 + row * 128 + (((c & 7) ^ (row & 7)) << 4)) =
+                *reinterpret_cast<const int4 *>(stage + tok * (4 * D) + (is_v ? 2 * D : 0) + c * 16);
         }
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
     }
     __syncwarp();
+}
+
+// Four consecutive output floats; the output is only 8-byte aligned (by contract), so two
+// 8-byte stores.
+__device__ __forceinline__ void store_out4(float *dst, float4 v) {
+    *reinterpret_cast<float2 *>(dst) = make_float2(v.x, v.y);
+    *reinterpret_cast<float2 *>(dst + 2) = make_float2(v.z, v.w);
 }
 
 // Floats of one pushed partial in the receive region: o [rows][D], m [rows], l [rows],
@@ -792,152 +897,139 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
 
 // Split merge of one unit's partial states (m, l, unnormalised o per query row), run by
 // the consumer threads (threadIdx.x < 128) of each of the unit's CTAs once this CTA's
-// partial is complete: in cp_o [rows][D], cp_m, cp_l (shared memory) when the unit's
-// splits form a thread-block cluster, in workspace slot (slot0 + split) otherwise.
-// Inside the cluster the other CTAs push their partials into rank 0's receive region
-// `recv` (recv_bytes) with distributed shared-memory stores, or rank 0 pulls them when
-// they do not fit. A partial with l < 0 comes from a split that must not write (a bad
-// page id or a timed-out wait): the merge then writes nothing for the unit. (Clusters
-// of 8 whose partials then merge through the workspace were measured and dropped:
-// batch-1 dense at 16K, 32 splits, 15.9 -> 22.9 us per layer against merging the 32
-// splits one by one.)
+// partial is written. Without a cluster the partials are in the workspace (slots from
+// slot0) and workspace_merge combines them. When the unit's splits form a thread-block
+// cluster, the other CTAs either have pushed their partials into rank 0's receive region
+// `recv` with distributed shared-memory stores (`push`; each slot holds o [rows][D],
+// m [rows], l [rows]) or keep them in their own cp_o [rows][D], cp_m, cp_l for rank 0 to
+// pull, when they do not fit. Rank 0 merges in two passes: one thread per row derives
+// the row's maximum, normaliser and the splits' weights (into `wsc`: [kMaxClusterSplits]
+// [kRows] weights, then [kRows] output scales 1 / l and [kRows] natural-log LSEs), then
+// each thread sums 4-float chunks of the output rows with those weights. A partial with
+// l < 0 comes from a split that must not write (a bad page id or a timed-out wait): the
+// merge then writes nothing for the unit. (Clusters of 8 whose partials then merge
+// through the workspace were measured and dropped: batch-1 dense at 16K, 32 splits,
+// 15.9 -> 22.9 us per layer against merging the 32 splits one by one.)
 template <int D, int kRows, bool CLUSTER, typename OutRow>
-__device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, int recv_bytes, uint64_t *merge_bar,
-                                             int *s_last, float *cp_o, float *cp_m, float *cp_l, int rows, int splits,
-                                             int split, int64_t unit, int64_t slot0, float *stage, int stage_bytes,
-                                             OutRow out_row) {
+__device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, bool push, uint64_t *merge_bar,
+                                             int *s_last, float *cp_o, float *cp_m, float *cp_l, float *wsc,
+                                             int rows, int splits, int split, int64_t unit, int64_t slot0,
+                                             float *stage, int stage_bytes, OutRow out_row) {
     const int ctid = threadIdx.x;  // 0 .. 127
     if (!CLUSTER) {
         workspace_merge<D, kRows>(p, merge_bar, s_last, rows, splits, unit, slot0, stage, stage_bytes, recv, out_row);
         return;
     }
-    const int crank = split, csize = splits;
-    // the merged values of one output pair
-    auto emit = [&](int row, int d, float M, float ax, float ay, float lsum, bool fail) {
-        if (fail) return;
-        *reinterpret_cast<float2 *>(&p.out[out_row(row) * D + d]) = make_float2(ax / lsum, ay / lsum);
-        if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-    };
-    if (cluster_push_fits<D>(csize, rows, recv_bytes)) {
-        // ---- push: the other CTAs store their partials into rank 0's receive region ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        const int slot_f = cluster_slot_floats<D>(rows);
-        if (crank != 0) {
-            const uint32_t dst = cluster_map(smem_u32(recv), 0) + (uint32_t)((crank - 1) * slot_f) * 4u;
-            for (int e4 = ctid; e4 < rows * D / 4; e4 += kConsumerWarps * 32)
-                st_cluster_f32x4(dst + e4 * 16, *reinterpret_cast<const float4 *>(&cp_o[4 * e4]));
-            for (int e = ctid; e < rows; e += kConsumerWarps * 32) {
-                st_cluster_f32(dst + (rows * D + e) * 4, cp_m[e]);
-                st_cluster_f32(dst + (rows * D + rows + e) * 4, cp_l[e]);
-            }
-            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // release: my stores above
+    const int csize = splits;
+    if (split != 0) {
+        if (push) {
+            // release: this thread's stores into rank 0's receive region
+            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));
             // Rank 0 signals once every push has landed; only then may this CTA exit.
             if (ctid == 0 && !mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
-            return;
-        }
-        const bool got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
-        if (got && ctid >= 1 && ctid < csize) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
-        if (!got) {
-            if (ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
         } else {
-            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-                float2 os[kMaxClusterSplits];
-                ms[0] = cp_m[row];
-                ls[0] = cp_l[row];
-                os[0] = *reinterpret_cast<const float2 *>(&cp_o[row * D + d]);
-#pragma unroll
-                for (int s = 1; s < kMaxClusterSplits; ++s) {
-                    if (s < csize) {
-                        const float *src = recv + (s - 1) * slot_f;
-                        ms[s] = src[rows * D + row];
-                        ls[s] = src[rows * D + rows + row];
-                        os[s] = *reinterpret_cast<const float2 *>(&src[row * D + d]);
-                    }
-                }
-                float M = -INFINITY;
-                bool fail = false;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < csize) {
-                        if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
-                        fail |= ls[s] < 0.f;
-                    }
-                }
-                float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < csize && ls[s] > 0.f) {
-                        const float f = fast_exp2(ms[s] - M);
-                        ax += os[s].x * f;
-                        ay += os[s].y * f;
-                        lsum += ls[s] * f;
-                    }
-                }
-                emit(row, d, M, ax, ay, lsum, fail);
-            }
-        }
-    } else {
-        // ---- pull: rank 0 reads the other CTAs' partials from their shared memory
-        // (when they do not fit its receive region) ----
-        consumer_bar_sync();  // this CTA's partial is complete in its shared memory
-        if (crank != 0) {
+            consumer_bar_sync();  // this CTA's partial is complete in its shared memory
             if (ctid == 0) {
                 mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));  // "my partial is ready"
                 // Stay alive (shared memory readable) until rank 0 has read it.
                 if (!mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
             }
-            return;
         }
+        return;
+    }
+    bool got;
+    if (push) {
+        got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
+        // The pushed partials are in this CTA's memory now: the peers may exit. The signal
+        // orders nothing (a release here stalled the merge by about 1 us).
+        if (got && ctid >= 1 && ctid < csize) mbar_arrive_remote_relaxed(cluster_map(smem_u32(merge_bar), ctid));
+    } else {
         if (ctid == 0) *s_last = mbar_wait_cluster_bounded(merge_bar, 0) ? 1 : 0;
         consumer_bar_sync();
-        const bool got = *s_last != 0;
-        if (got) {
-            // Each thread merges pairs of outputs. All loads from the peers' shared
-            // memory are issued before any is used, so their latencies overlap.
-            for (int e2 = ctid; e2 < rows * D / 2; e2 += kConsumerWarps * 32) {
-                const int row = (2 * e2) / D, d = 2 * e2 - row * D;
-                float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
-                float2 os[kMaxClusterSplits];
+        got = *s_last != 0;
+    }
+    const int slot_f = cluster_slot_floats<D>(rows);
+    float *w_row = wsc;                                   // [kMaxClusterSplits][kRows]
+    float *scale_row = wsc + kMaxClusterSplits * kRows;   // [kRows]
+    float *lse_row = scale_row + kRows;                   // [kRows]
+    bool bad = !got;
+    if (got && ctid < rows) {
+        const int row = ctid;
+        float ms[kMaxClusterSplits], ls[kMaxClusterSplits];
 #pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < csize) {
-                        ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
-                        ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
-                        os[s] = ld_cluster_f32x2(cluster_map(smem_u32(&cp_o[row * D + d]), s));
-                    }
-                }
-                float M = -INFINITY;
-                bool fail = false;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < csize) {
-                        if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
-                        fail |= ls[s] < 0.f;
-                    }
-                }
-                float ax = 0.f, ay = 0.f, lsum = 0.f;
-#pragma unroll
-                for (int s = 0; s < kMaxClusterSplits; ++s) {
-                    if (s < csize && ls[s] > 0.f) {
-                        const float f = fast_exp2(ms[s] - M);
-                        ax += os[s].x * f;
-                        ay += os[s].y * f;
-                        lsum += ls[s] * f;
-                    }
-                }
-                emit(row, d, M, ax, ay, lsum, fail);
+        for (int s = 0; s < kMaxClusterSplits; ++s) {
+            if (s >= csize) break;
+            if (s == 0) {
+                ms[s] = cp_m[row];
+                ls[s] = cp_l[row];
+            } else if (push) {
+                const float *src = recv + (s - 1) * slot_f + rows * D;
+                ms[s] = src[row];
+                ls[s] = src[rows + row];
+            } else {
+                ms[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_m[row]), s));
+                ls[s] = ld_cluster_f32(cluster_map(smem_u32(&cp_l[row]), s));
             }
-        } else if (ctid == 0) {
-            report(p.dev_status, SFI_DEV_TIMEOUT);
         }
+        float M = -INFINITY;
+#pragma unroll
+        for (int s = 0; s < kMaxClusterSplits; ++s) {
+            if (s >= csize) break;
+            if (ls[s] > 0.f) M = fmaxf(M, ms[s]);
+            bad |= ls[s] < 0.f;
+        }
+        float lsum = 0.f;
+#pragma unroll
+        for (int s = 0; s < kMaxClusterSplits; ++s) {
+            if (s >= csize) break;
+            const float w = ls[s] > 0.f ? fast_exp2(ms[s] - M) : 0.f;
+            w_row[s * kRows + row] = w;
+            lsum += ls[s] > 0.f ? ls[s] * w : 0.f;
+        }
+        scale_row[row] = 1.f / lsum;
+        lse_row[row] = (M + log2f(lsum)) * kLn2;
+    }
+    // A failed split fails every row of the unit; make the decision CTA-wide.
+    const bool fail = consumer_bar_or(bad);
+    if (!got && ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+    if (!fail) {
+        constexpr int kC = D / 4;  // 4-float chunks per row
+        for (int c = ctid; c < rows * kC; c += kConsumerWarps * 32) {
+            const int row = c / kC, d = (c - row * kC) * 4;
+            float4 o[kMaxClusterSplits];
+            // every load first, so the distributed shared-memory latencies overlap
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s >= csize) break;
+                if (s == 0)
+                    o[s] = *reinterpret_cast<const float4 *>(&cp_o[row * D + d]);
+                else if (push)
+                    o[s] = *reinterpret_cast<const float4 *>(&recv[(s - 1) * slot_f + row * D + d]);
+                else
+                    o[s] = ld_cluster_f32x4(cluster_map(smem_u32(&cp_o[row * D + d]), s));
+            }
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int s = 0; s < kMaxClusterSplits; ++s) {
+                if (s >= csize) break;
+                const float w = w_row[s * kRows + row];
+                acc.x += o[s].x * w;
+                acc.y += o[s].y * w;
+                acc.z += o[s].z * w;
+                acc.w += o[s].w * w;
+            }
+            const float sc = scale_row[row];
+            store_out4(&p.out[out_row(row) * D + d], make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+            if (d == 0 && p.lse) p.lse[out_row(row)] = lse_row[row];
+        }
+    }
+    if (!push) {
         consumer_bar_sync();  // every read of the peers' shared memory is done
         if (got && ctid > 0 && ctid < csize) mbar_arrive_remote(cluster_map(smem_u32(merge_bar), ctid));
     }
 }
 
-// MQ: p.tokens query tokens per request (rows = tokens x G <= 16), no fused append.
+// MQ: p.tokens query tokens per request (rows = tokens x G <= 16).
 template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>
 __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     attn_decode_kernel(const __grid_constant__ CUtensorMap tm_pool_k, const __grid_constant__ CUtensorMap tm_pool_v,
@@ -958,6 +1050,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     __shared__ int s_bad;  // a page id of this unit is out of range: the unit writes no output
     __shared__ __align__(16) int4 s_app_val[32];  // the current token's K/V chunks (fused append)
     __shared__ int s_app_page;
+    __shared__ int s_tok_page[kConsumerWarps];  // page ids of the staged query tokens (multi-token append)
 
     // ---- this CTA's work item: (request, KV head, split) and the unit's mode ----
     int split, kvh, b, splits;
@@ -1183,6 +1276,21 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         grid_launch_dependents();
     }
     if (check_pages && !p.early_prefetch) pages_first(p, r, u.L, pg_first);
+    if (MQ && p.k_new != nullptr) {
+        // The CTA that appends the query tokens' K/V (positions [L - T, L), in the last
+        // one or two sub-blocks) brings their rows into L2 now; the append reads them
+        // at the end of the stream.
+        const int sb_first = u.sb_app - ((u.L - 1) / kSubTokens - (u.L0 - 1) / kSubTokens);
+        if (sb_begin <= u.sb_app && sb_end > sb_first) {
+            constexpr int kLines = D * 2 / 128;  // 128-byte lines per K (or V) row
+            for (int i = threadIdx.x; i < p.tokens * 2 * kLines; i += kConsumerWarps * 32) {
+                const int tok = i / (2 * kLines), rem = i - tok * 2 * kLines;
+                const __nv_bfloat16 *src = (rem < kLines ? p.k_new : p.v_new) +
+                                           (((int64_t)r * p.tokens + tok) * p.hkv + kvh) * D + (rem % kLines) * 64;
+                asm volatile("prefetch.global.L2 [%0];" ::"l"(src));
+            }
+        }
+    }
     const int g = lane >> 2, t = lane & 3;
     const int G = p.group;
     uint32_t qa[D / 16][2];
@@ -1248,10 +1356,28 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         }
     }
 
-    if (!MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end &&
-        (u.sb_app - sb0) % kConsumerWarps == warp)
-        stage_current_token<D>(p, r, kvh, u, lane, s_app_val, &s_app_page);
+    // the warp that owns the sub-block with the current token (single-token append)
+    const bool app_mine = !MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end &&
+                          (u.sb_app - sb0) % kConsumerWarps == warp;
+    if (app_mine) stage_current_token<D>(p, r, kvh, u, lane, s_app_val, &s_app_page);
+    // Multi-token append: the first position of the paged sub-block with query tokens
+    // that this warp owns (-1 if none). Their K/V are staged at the start of the receive
+    // region, which nothing else uses during the stream unless this CTA is rank 0 of a
+    // cluster (the push target): that CTA appends from global memory instead.
+    int tok_pos0 = -1;
+    uint8_t *tok_stage = smem + T::kRecvOffset;
+    if (MQ && p.k_new != nullptr && !(CLUSTER && split == 0)) {
+        const int pos_last = ((u.L - 1) / kSubTokens) * kSubTokens;
+        for (int k = 0; k < 2; ++k) {  // T <= 16 tokens lie in at most two sub-blocks
+            const int pos0 = pos_last - k * kSubTokens, sb = u.sb_app - k;
+            // stop below the query tokens or outside the paged segment
+            if (pos0 + kSubTokens <= u.L0 - 1 || u.lo_pos >= u.L || pos0 / kSubTokens < u.page0) break;
+            if (sb >= sb_begin && sb < sb_end && (sb - sb0) % kConsumerWarps == warp) tok_pos0 = pos0;
+        }
+        if (tok_pos0 >= 0) stage_tokens<D>(p, r, kvh, u.L, tok_pos0, lane, tok_stage, &s_tok_page[warp]);
+    }
     bool timed_out = false;
+    const int store_st = min(2, n_stages - 1);
     for (int st = 0; st < n_stages; ++st) {
         const int slot = st % T::kStages;
         if (!mbar_wait_warp(&full_bar[slot], (st / T::kStages) & 1)) {
@@ -1261,19 +1387,28 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         const int2 in = s_info[slot][warp];
         const int lo = in.x & 0xffff, hi = in.x >> 16;
         const int sb_me = sb0 + st * kConsumerWarps + warp;  // this warp's sub-block in the stage
-        if (!MQ && p.k_new != nullptr && u.sb_app >= sb_begin && u.sb_app < sb_end && sb_me == u.sb_app) {
+        // The appended tokens go to the pages at the third stage (the first ones wait on
+        // the staged copies more often; at T = 8 drafts this was 0.3 us per launch faster
+        // than the first stage).
+        if (st == store_st && app_mine) store_current_token<D>(p, kvh, u, lane, s_app_val, &s_app_page, &s_bad);
+        if (st == store_st && tok_pos0 >= 0)
+            store_tokens<D>(p, kvh, u.L, tok_pos0, lane, tok_stage, &s_tok_page[warp], &s_bad);
+        if (app_mine && sb_me == u.sb_app) {
             // Fused append: the current token's K/V replace row L - 1 of this tile (the
-            // attention sees the cache after the append) and are written to the pages.
-            // Only the split that owns that sub-block does it (a stage's padding slots
-            // past sb_end may carry the same index).
-            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u, lane,
-                                  s_app_val, &s_app_page, &s_bad);
+            // attention sees the cache after the append). Only the split that owns that
+            // sub-block does it (a stage's padding slots past sb_end may carry the same
+            // index).
+            fuse_current_token<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, u, lane, s_app_val);
         }
         if (MQ && p.k_new != nullptr && in.y >= 0 && sb_me >= sb_begin && sb_me < sb_end &&
             in.y + kSubTokens > u.L0 - 1 && in.y < u.L) {
             // Fused append of the query tokens (positions [L - T, L)) in this paged sub-block.
-            fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane,
-                           &s_bad);
+            if (in.y == tok_pos0)
+                fuse_staged_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, u.L, in.y, lane,
+                                      tok_stage);
+            else
+                fuse_tokens<D>(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes, p, r, kvh, u.L, in.y, lane,
+                               &s_bad);
         }
         if (hi > lo) {
             const uint32_t kaddr = smem_u32(smem + slot * T::kStageBytes + warp * 2 * T::kSubBytes);
@@ -1299,6 +1434,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         __syncwarp();
         if (lane == 0) mbar_arrive(&empty_bar[slot]);
     }
+    // staged copies still in flight after a timed-out wait land before shared memory is reused
+    if (app_mine || tok_pos0 >= 0) asm volatile("cp.async.wait_all;" ::: "memory");
     if (timed_out && lane == 0) {
         report(p.dev_status, SFI_DEV_TIMEOUT);
         s_timeout = 1;
@@ -1313,12 +1450,14 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     consumer_bar_sync();
     const bool ok = s_timeout == 0;
     constexpr int MS = T::kMergeStride;
+    constexpr int kC = D / 4;                                       // 4-float chunks per row
     float *sm_o = reinterpret_cast<float *>(smem);                  // [warps][kRows][MS]
-    float *sm_m = sm_o + kConsumerWarps * kRows * MS;               // [warps][kRows]
+    float *sm_m = sm_o + kConsumerWarps * kRows * MS;               // [warps][kRows] maxima, then weights
     float *sm_l = sm_m + kConsumerWarps * kRows;                    // [warps][kRows]
     float *cp_o = sm_l + kConsumerWarps * kRows;                    // [kRows][D]  this CTA's partial (cluster merge)
     float *cp_m = cp_o + kRows * D;                                 // [kRows]
     float *cp_l = cp_m + kRows;                                     // [kRows]
+    float *wsc = cp_l + kRows;                                      // [kMaxClusterSplits + 2][kRows] merge scratch
     // up to 8 query rows: rows g + 8 hold the P_lo V half of row g
     const bool packed = !MQ || p.rows <= kMaxGroup;
     if (ok) {
@@ -1354,59 +1493,79 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     // A partial that must not reach the output (a bad page id in the unit, or a timed-out
     // wait) carries l = -1: every merge that sees it skips the unit's writes.
     const bool skip = !ok || s_bad != 0;
-    if (ok) {
-        for (int e = ctid; e < rows * D; e += kConsumerWarps * 32) {
-            const int row = e / D, d = e - (e / D) * D;
-            float M = -INFINITY;
+    // Where this CTA's partial goes: the output (one split), rank 0's receive region
+    // (cluster push from another rank), cp_* (cluster rank 0, or pull), or the workspace.
+    float *recv = reinterpret_cast<float *>(smem + T::kRecvOffset);
+    const bool push = CLUSTER && cluster_push_fits<D>(splits, rows, kPushBytes);
+    const bool remote = push && split != 0;
+    const uint32_t rdst =
+        remote ? cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * cluster_slot_floats<D>(rows)) * 4u : 0u;
+    const int64_t wslot = slot0 * kRows + (int64_t)split * rows;  // workspace slot of row 0 (packed per unit)
+    // Two passes: one thread per row takes the row's maximum over the warps, turns each
+    // warp's maximum into its weight 2^(m_w - M) and sums the normaliser; then each
+    // thread sums 4-float chunks of the rows with those weights.
+    if (ctid < rows) {
+        const int row = ctid;
+        float M = -INFINITY, lsum = -1.f;
+        if (ok) {
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) M = fmaxf(M, sm_m[w * kRows + row]);
-            float acc = 0.f, lsum = 0.f;
+            lsum = 0.f;
 #pragma unroll
             for (int w = 0; w < kConsumerWarps; ++w) {
                 const float mw = sm_m[w * kRows + row];
-                if (mw != -INFINITY) {
-                    const float f = fast_exp2(mw - M);
-                    acc += sm_o[(w * kRows + row) * MS + d] * f;
-                    lsum += sm_l[w * kRows + row] * f;
-                }
+                const float f = mw != -INFINITY ? fast_exp2(mw - M) : 0.f;
+                sm_m[w * kRows + row] = f;
+                lsum += sm_l[w * kRows + row] * f;
             }
             if (skip) lsum = -1.f;
-            if (splits == 1) {
-                if (!skip) {
-                    p.out[out_row(row) * D + d] = acc / lsum;
-                    if (d == 0 && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
-                }
-            } else if (CLUSTER) {
-                cp_o[row * D + d] = acc;
-                if (d == 0) {
-                    cp_m[row] = M;
-                    cp_l[row] = lsum;
-                }
-            } else {
-                const int64_t slot = slot0 * kRows + (int64_t)split * rows + row;  // packed per unit
-                p.ws_part[slot * D + d] = acc;
-                if (d == 0) {
-                    p.ws_ml[slot * 2 + 0] = M;
-                    p.ws_ml[slot * 2 + 1] = lsum;
-                }
-            }
         }
-    } else if (splits > 1) {
-        for (int row = ctid; row < rows; row += kConsumerWarps * 32) {
-            if (CLUSTER) {
-                cp_m[row] = -INFINITY;
-                cp_l[row] = -1.f;
+        if (splits == 1) {
+            wsc[row] = 1.f / lsum;
+            if (!skip && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+        } else if (remote) {
+            st_cluster_f32(rdst + (rows * D + row) * 4, M);
+            st_cluster_f32(rdst + (rows * D + rows + row) * 4, lsum);
+        } else if (CLUSTER) {
+            cp_m[row] = M;
+            cp_l[row] = lsum;
+        } else {
+            p.ws_ml[(wslot + row) * 2 + 0] = M;
+            p.ws_ml[(wslot + row) * 2 + 1] = lsum;
+        }
+    }
+    if (ok && !(splits == 1 && skip)) {
+        consumer_bar_sync();
+        for (int c = ctid; c < rows * kC; c += kConsumerWarps * 32) {
+            const int row = c / kC, d = (c - row * kC) * 4;
+            float4 ow[kConsumerWarps];
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w)
+                ow[w] = *reinterpret_cast<const float4 *>(&sm_o[(w * kRows + row) * MS + d]);
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = sm_m[w * kRows + row];  // 0 for a warp that saw no token (its o is 0)
+                acc.x += ow[w].x * f;
+                acc.y += ow[w].y * f;
+                acc.z += ow[w].z * f;
+                acc.w += ow[w].w * f;
+            }
+            if (splits == 1) {
+                const float sc = wsc[row];
+                store_out4(&p.out[out_row(row) * D + d], make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+            } else if (remote) {
+                st_cluster_f32x4(rdst + (row * D + d) * 4, acc);
+            } else if (CLUSTER) {
+                *reinterpret_cast<float4 *>(&cp_o[row * D + d]) = acc;
             } else {
-                const int64_t slot = slot0 * kRows + (int64_t)split * rows + row;
-                p.ws_ml[slot * 2 + 0] = -INFINITY;
-                p.ws_ml[slot * 2 + 1] = -1.f;
+                *reinterpret_cast<float4 *>(&p.ws_part[(wslot + row) * D + d]) = acc;
             }
         }
     }
     if (splits == 1) return;
-    merge_splits<D, kRows, CLUSTER>(p, reinterpret_cast<float *>(smem + T::kRecvOffset), kPushBytes, &merge_bar,
-                                     &s_last, cp_o, cp_m, cp_l, rows, splits, split, unit, slot0,
-                                     reinterpret_cast<float *>(smem), T::kRingBytes, out_row);
+    merge_splits<D, kRows, CLUSTER>(p, recv, push, &merge_bar, &s_last, cp_o, cp_m, cp_l, wsc, rows, splits, split,
+                                     unit, slot0, reinterpret_cast<float *>(smem), T::kRingBytes, out_row);
 }
 
 template <int D, int MODE, bool SCORES, bool CLUSTER, bool MQ>

@@ -102,9 +102,12 @@ __device__ __forceinline__ float ld_cluster_f32(uint32_t caddr) {
     return v;
 }
 
-__device__ __forceinline__ float2 ld_cluster_f32x2(uint32_t caddr) {
-    float2 v;
-    asm volatile("ld.shared::cluster.v2.f32 {%0, %1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(caddr) : "memory");
+__device__ __forceinline__ float4 ld_cluster_f32x4(uint32_t caddr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(caddr)
+                 : "memory");
     return v;
 }
 
@@ -121,6 +124,12 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t caddr, float4 v) {
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+// Arrive on an mbarrier of another CTA of the cluster with no memory ordering (a bare
+// signal: nothing written before it needs to be visible to the waiter).
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t caddr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
 }
 
 // Bounded wait (one thread) for a phase completed by arrivals from other CTAs.

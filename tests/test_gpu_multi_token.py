@@ -230,9 +230,21 @@ def test_draft_g8_two_tokens():
 def test_verify_with_fused_append_matches_oracle(T, splits, flags):
     """k_new/v_new given to the verification: it equals the T-token append followed by the
     verification, pages included, with and without early KV prefetch."""
+    _verify_fused_case(T, splits, flags, [300, 1023, 17, 40])
+
+
+@pytest.mark.parametrize("T,splits", [(8, 2), (8, 3), (16, 2)])
+def test_verify_fused_append_across_splits(T, splits):
+    """Query tokens that straddle a page boundary and a split boundary of a short request:
+    the first split of a cluster appends its part straight from global memory (its receive
+    region takes the other splits' partials), the later ones from shared-memory staging."""
+    _verify_fused_case(T, splits, 1, [10, 13, 5, 2])
+
+
+def _verify_fused_case(T, splits, flags, lens0):
     sfi = _sfi()
     Hq, Hkv = (8, 8) if T == 16 else (16, 8)
-    prob = Problem(seed=800 + T, lens=[300, 1023, 17, 40], Hq=Hq, Hkv=Hkv, D=128, S=4, W=32,
+    prob = Problem(seed=800 + T, lens=lens0, Hq=Hq, Hkv=Hkv, D=128, S=4, W=32,
                    extra_tokens=T).to_device()
     g = syn.rng(403, T)
     kn, vn = syn.normal_bf16(g, (prob.B, T, Hkv, 128)), syn.normal_bf16(g, (prob.B, T, Hkv, 128))
