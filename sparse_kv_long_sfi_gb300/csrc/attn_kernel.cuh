@@ -751,7 +751,6 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
         int prev;
         asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], 1;" : "=r"(prev) : "l"(&p.ws_count[unit]) : "memory");
         *s_last = (prev == nparts - 1);
-        if (*s_last) p.ws_count[unit] = 0;
     }
     consumer_bar_sync();
     if (!*s_last) return;
@@ -882,6 +881,9 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
         asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
         consumer_bar_sync();
     }
+    // The counter goes back to zero for the next launch (after the last shared-memory
+    // read: a global store would hold those up).
+    if (ctid == 0) p.ws_count[unit] = 0;
     // A failed split fails every row of the unit; make the decision CTA-wide.
     if (consumer_bar_or(fail) || member != 0) return;
 #pragma unroll
@@ -994,33 +996,48 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, b
     if (!got && ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
     if (!fail) {
         constexpr int kC = D / 4;  // 4-float chunks per row
-        for (int c = ctid; c < rows * kC; c += kConsumerWarps * 32) {
+        // Every chunk of this thread is summed (the loads of all splits issued together, so
+        // distributed shared-memory latencies overlap) before any of the stores is issued:
+        // a shared-memory load after a global store waits for the store path.
+        constexpr int kIt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+        float4 acc[kIt];
+        float lse_v[kIt];
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+            const int c = ctid + i * kConsumerWarps * 32;
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            lse_v[i] = 0.f;
+            if (c < rows * kC) {
+                const int row = c / kC, d = (c - row * kC) * 4;
+#pragma unroll
+                for (int s = 0; s < kMaxClusterSplits; ++s) {
+                    if (s < csize) {
+                        float4 o;
+                        if (s == 0)
+                            o = *reinterpret_cast<const float4 *>(&cp_o[row * D + d]);
+                        else if (push)
+                            o = *reinterpret_cast<const float4 *>(&recv[(s - 1) * slot_f + row * D + d]);
+                        else
+                            o = ld_cluster_f32x4(cluster_map(smem_u32(&cp_o[row * D + d]), s));
+                        const float w = w_row[s * kRows + row];
+                        acc[i].x += o.x * w;
+                        acc[i].y += o.y * w;
+                        acc[i].z += o.z * w;
+                        acc[i].w += o.w * w;
+                    }
+                }
+                const float sc = scale_row[row];
+                acc[i] = make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc);
+                lse_v[i] = lse_row[row];
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+            const int c = ctid + i * kConsumerWarps * 32;
+            if (c >= rows * kC) break;
             const int row = c / kC, d = (c - row * kC) * 4;
-            float4 o[kMaxClusterSplits];
-            // every load first, so the distributed shared-memory latencies overlap
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-                if (s >= csize) break;
-                if (s == 0)
-                    o[s] = *reinterpret_cast<const float4 *>(&cp_o[row * D + d]);
-                else if (push)
-                    o[s] = *reinterpret_cast<const float4 *>(&recv[(s - 1) * slot_f + row * D + d]);
-                else
-                    o[s] = ld_cluster_f32x4(cluster_map(smem_u32(&cp_o[row * D + d]), s));
-            }
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-            for (int s = 0; s < kMaxClusterSplits; ++s) {
-                if (s >= csize) break;
-                const float w = w_row[s * kRows + row];
-                acc.x += o[s].x * w;
-                acc.y += o[s].y * w;
-                acc.z += o[s].z * w;
-                acc.w += o[s].w * w;
-            }
-            const float sc = scale_row[row];
-            store_out4(&p.out[out_row(row) * D + d], make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
-            if (d == 0 && p.lse) p.lse[out_row(row)] = lse_row[row];
+            store_out4(&p.out[out_row(row) * D + d], acc[i]);
+            if (d == 0 && p.lse) p.lse[out_row(row)] = lse_v[i];
         }
     }
     if (!push) {
@@ -1040,7 +1057,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     // bytes of the receive region open to the cluster push (the rest holds the query tile)
     constexpr int kPushBytes = MQ ? T::kRecvBytes - T::kQBytes : T::kRecvBytes;
     extern __shared__ uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    // 1024-byte aligned (the 128-byte swizzle pattern repeats every 1 KB). Offsetting the
+    // array itself, rather than rounding an integer address, keeps every pointer derived
+    // from it a shared-memory pointer to the compiler (shared loads and stores, and no
+    // assumed aliasing with global stores in the merges).
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
     __shared__ __align__(8) uint64_t full_bar[T::kStages];
     __shared__ __align__(8) uint64_t empty_bar[T::kStages];
     __shared__ __align__(8) uint64_t merge_bar;  // cluster merge handshake, or the workspace merge's copies
@@ -1520,46 +1541,70 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             }
             if (skip) lsum = -1.f;
         }
+        // Row results for the second pass go to shared memory: global stores here would
+        // hold up this thread's shared-memory loads behind them (the store path is long
+        // while the other CTAs stream).
         if (splits == 1) {
             wsc[row] = 1.f / lsum;
-            if (!skip && p.lse) p.lse[out_row(row)] = (M + log2f(lsum)) * kLn2;
+            wsc[kRows + row] = (M + log2f(lsum)) * kLn2;
         } else if (remote) {
             st_cluster_f32(rdst + (rows * D + row) * 4, M);
             st_cluster_f32(rdst + (rows * D + rows + row) * 4, lsum);
         } else if (CLUSTER) {
             cp_m[row] = M;
             cp_l[row] = lsum;
-        } else {
+        } else if (ok) {
+            wsc[row] = M;
+            wsc[kRows + row] = lsum;
+        } else {  // no second pass
             p.ws_ml[(wslot + row) * 2 + 0] = M;
             p.ws_ml[(wslot + row) * 2 + 1] = lsum;
         }
     }
     if (ok && !(splits == 1 && skip)) {
         consumer_bar_sync();
-        for (int c = ctid; c < rows * kC; c += kConsumerWarps * 32) {
-            const int row = c / kC, d = (c - row * kC) * 4;
-            float4 ow[kConsumerWarps];
+        // Every chunk of this thread is summed (all shared-memory reads) before any of the
+        // stores is issued.
+        constexpr int kIt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+        float4 acc[kIt];
+        float2 rowv[kIt];  // the row's (scale, lse) or (m, l), read by its first chunk's thread
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w)
-                ow[w] = *reinterpret_cast<const float4 *>(&sm_o[(w * kRows + row) * MS + d]);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        for (int i = 0; i < kIt; ++i) {
+            const int c = ctid + i * kConsumerWarps * 32;
+            acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+            rowv[i] = make_float2(0.f, 0.f);
+            if (c < rows * kC) {
+                const int row = c / kC;
+                const int d = (c - row * kC) * 4;
 #pragma unroll
-            for (int w = 0; w < kConsumerWarps; ++w) {
-                const float f = sm_m[w * kRows + row];  // 0 for a warp that saw no token (its o is 0)
-                acc.x += ow[w].x * f;
-                acc.y += ow[w].y * f;
-                acc.z += ow[w].z * f;
-                acc.w += ow[w].w * f;
+                for (int w = 0; w < kConsumerWarps; ++w) {
+                    const float f = sm_m[w * kRows + row];  // 0 for a warp that saw no token (its o is 0)
+                    const float4 ow = *reinterpret_cast<const float4 *>(&sm_o[(w * kRows + row) * MS + d]);
+                    acc[i].x += ow.x * f;
+                    acc[i].y += ow.y * f;
+                    acc[i].z += ow.z * f;
+                    acc[i].w += ow.w * f;
+                }
+                if (splits == 1 || d == 0) rowv[i] = make_float2(wsc[row], wsc[kRows + row]);
             }
+        }
+#pragma unroll
+        for (int i = 0; i < kIt; ++i) {
+            const int c = ctid + i * kConsumerWarps * 32;
+            if (c >= rows * kC) break;
+            const int row = c / kC, d = (c - row * kC) * 4;
             if (splits == 1) {
-                const float sc = wsc[row];
-                store_out4(&p.out[out_row(row) * D + d], make_float4(acc.x * sc, acc.y * sc, acc.z * sc, acc.w * sc));
+                const float sc = rowv[i].x;
+                store_out4(&p.out[out_row(row) * D + d],
+                           make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc));
+                if (d == 0 && p.lse) p.lse[out_row(row)] = rowv[i].y;
             } else if (remote) {
-                st_cluster_f32x4(rdst + (row * D + d) * 4, acc);
+                st_cluster_f32x4(rdst + (row * D + d) * 4, acc[i]);
             } else if (CLUSTER) {
-                *reinterpret_cast<float4 *>(&cp_o[row * D + d]) = acc;
+                *reinterpret_cast<float4 *>(&cp_o[row * D + d]) = acc[i];
             } else {
-                *reinterpret_cast<float4 *>(&p.ws_part[(wslot + row) * D + d]) = acc;
+                *reinterpret_cast<float4 *>(&p.ws_part[(wslot + row) * D + d]) = acc[i];
+                if (d == 0) *reinterpret_cast<float2 *>(&p.ws_ml[(wslot + row) * 2]) = rowv[i];
             }
         }
     }
