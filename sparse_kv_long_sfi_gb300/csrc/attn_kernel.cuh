@@ -234,15 +234,13 @@ __device__ __forceinline__ void consume_sub_block(uint32_t kaddr, uint32_t vaddr
             v2 += __shfl_xor_sync(0xffffffffu, v2, off);
             v3 += __shfl_xor_sync(0xffffffffu, v3, off);
         }
-        if (g == 0 && score_row != nullptr) {
+        // Every lane of a column group holds the sums now; lanes g < 4 store one token each,
+        // so the sub-block's 16 scores leave in one coalesced 64-byte store.
+        if (g < 4 && score_row != nullptr) {
             const int c_lo = p.sink, c_hi = L - p.recent;
-            const float vv[4] = {v0, v1, v2, v3};
-            const int tk[4] = {tk0, tk1, tk2, tk3};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int pos = pos0 + tk[i];
-                if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? vv[i] * p.scale : -INFINITY;
-            }
+            const float vg = (g & 2) ? ((g & 1) ? v3 : v2) : ((g & 1) ? v1 : v0);
+            const int pos = pos0 + (g >> 1) * 8 + 2 * t + (g & 1);  // tk0 .. tk3
+            if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? vg * p.scale : -INFINITY;
         }
     }
 
@@ -418,13 +416,12 @@ __device__ __forceinline__ void consume_sub_block_mq(uint32_t kaddr, uint32_t va
 #pragma unroll
             for (int i = 0; i < 4; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], off);
         }
-        if (g == 0 && score_row != nullptr) {
+        // one token per lane g < 4 (every lane of a column group holds the sums)
+        if (g < 4 && score_row != nullptr) {
             const int c_lo = p.sink, c_hi = L - p.recent;
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const int pos = pos0 + tk[i];
-                if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? v[i] * p.scale : -INFINITY;
-            }
+            const float vg = (g & 2) ? ((g & 1) ? v[3] : v[2]) : ((g & 1) ? v[1] : v[0]);
+            const int pos = pos0 + (g >> 1) * 8 + 2 * t + (g & 1);  // tk[g]
+            if (pos < L) score_row[pos] = (pos >= c_lo && pos < c_hi) ? vg * p.scale : -INFINITY;
         }
     }
 
