@@ -250,7 +250,9 @@ SFI_API sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_
                                          size_t workspace_bytes, int32_t *dev_status, void *stream);
 
 /* Workspace bytes sfi_mixed_decode_attn needs for these arguments on the current
- * device (0 when it needs none). */
+ * device (0 when it needs none). With one of n_fast, n_slow zero (the SFI_ATTN_RAGGED
+ * plans of the single-mode calls) the size is valid for every batch size up to the
+ * other, as for sfi_workspace_size. */
 SFI_API size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_fast, int32_t n_slow,
                                         int32_t max_fast_tokens, int32_t max_dense_tokens);
 
@@ -325,8 +327,9 @@ SFI_API sfi_status sfi_sparse_draft_attn(const sfi_attn_shape *shape, const sfi_
                                          int32_t batch, int32_t max_tokens, int32_t num_splits, uint32_t flags,
                                          void *workspace, size_t workspace_bytes, int32_t *dev_status, void *stream);
 
-/* Workspace bytes the two multi-token attention calls need on the current device
- * (0 when none; 0 also on invalid input). */
+/* Workspace bytes the two multi-token attention calls need on the current device,
+ * valid for every batch size 1..batch as for sfi_workspace_size (0 when none; 0 also
+ * on invalid input). */
 SFI_API size_t sfi_multi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t num_tokens,
                                         int32_t max_tokens, int32_t num_splits);
 
@@ -423,10 +426,14 @@ SFI_API sfi_status sfi_fast_decode_attn_noalloc(const sfi_attn_shape *shape, con
 
 /*
  * sfi_workspace_size - bytes of workspace the attention entry points need for this
- * batch, token bound and split request on the current device (split-KV partial
- * states plus one counter per (request, KV head)). Returns 0 when the plan needs none
- * (at most 8 splits: the splits of a unit merge inside a thread-block cluster) and on
- * invalid input.
+ * batch, token bound and split request on the current device, valid for every batch
+ * size 1..batch (calls on a subset of the requests plan their splits for the subset):
+ * one split counter per (request, KV head) at the start of the buffer, and the largest
+ * block of split-KV partial states of those plans, which each call places at the end
+ * of the buffer it is given. So calls with different batch sizes may share one buffer
+ * (one at a time) when it holds the size for the largest of them. Returns 0 when no
+ * plan needs any (at most 8 splits: the splits of a unit merge inside a thread-block
+ * cluster) and on invalid input.
  */
 SFI_API size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
 

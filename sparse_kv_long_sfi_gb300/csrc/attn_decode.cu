@@ -5,18 +5,26 @@
 
 namespace sfi {
 
-WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows) {
+WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows, size_t bytes) {
     WorkspaceLayout w;
     auto up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t cnt = up(sizeof(int32_t) * (size_t)units);  // one split counter per unit
+    const size_t ml = up(sizeof(float) * 2 * (size_t)rows * (size_t)slots);
+    const size_t part = up(sizeof(float) * (size_t)head_dim * (size_t)rows * (size_t)slots);
     w.count_off = 0;
-    w.ml_off = up(sizeof(int32_t) * (size_t)units);
-    w.part_off = w.ml_off + up(sizeof(float) * 2 * (size_t)rows * (size_t)slots);
-    w.total = w.part_off + up(sizeof(float) * (size_t)head_dim * (size_t)rows * (size_t)slots);
+    w.data_bytes = ml + part;
+    w.total = cnt + w.data_bytes;
+    // The partial states sit at the end of the caller's buffer (right after the counters
+    // when it is exactly `total` bytes), so the counters of every call sharing a buffer
+    // stay clear of every other call's partial states, whatever their batch sizes.
+    const size_t end = bytes >= w.total ? (bytes & ~size_t(255)) : w.total;
+    w.part_off = end - part;
+    w.ml_off = w.part_off - ml;
     return w;
 }
 
-WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int rows) {
-    return workspace_layout_slots(units, units * splits, head_dim, rows);
+WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int rows, size_t bytes) {
+    return workspace_layout_slots(units, units * splits, head_dim, rows, bytes);
 }
 
 template <int D, bool CLUSTER>

@@ -188,7 +188,7 @@ sfi_status bind_workspace(AttnParams &p, int64_t units, int head_dim, void *ws, 
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
     if (!needs_workspace(p.splits)) return SFI_OK;
-    const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim, rows);
+    const sfi::WorkspaceLayout l = sfi::workspace_layout(units, p.splits, head_dim, rows, ws_bytes);
     if (!ws || ws_bytes < l.total || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0) return SFI_ERR_WORKSPACE;
     char *base = static_cast<char *>(ws);
     p.ws_count = reinterpret_cast<int32_t *>(base + l.count_off);
@@ -218,7 +218,8 @@ sfi_status launch_chunked(AttnParams &p, bool fast, const int32_t *req_ids, int3
     p.ws_ml = nullptr;
     p.ws_part = nullptr;
     if (p.splits > 1) {
-        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, head_dim);
+        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, head_dim, sfi::kMaxGroup,
+                                                                   workspace_bytes);
         if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return SFI_ERR_WORKSPACE;
         char *base = static_cast<char *>(workspace);
@@ -279,10 +280,27 @@ int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_
     return plan_splits((int64_t)batch * shape->num_kv_heads, max_tokens, num_splits, sm_count_current_device());
 }
 
+// Bytes for the split plans of every batch size 1..batch sharing one buffer: the counters
+// of `batch` requests plus the largest partial-state block of any of those plans (each
+// call puts its partial states at the end of the buffer); 0 when no plan needs any.
+size_t subset_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits,
+                             int rows) {
+    if (check_shape(shape) != SFI_OK || batch < 0 || num_splits < 0) return 0;
+    size_t data = 0;
+    bool any = false;
+    for (int32_t b = 1; b <= batch; ++b) {
+        const int32_t s = sfi_plan_splits(shape, b, max_tokens, num_splits);
+        if (!needs_workspace(s)) continue;
+        any = true;
+        data = std::max(data, sfi::workspace_layout((int64_t)b * shape->num_kv_heads, s, shape->head_dim, rows)
+                                  .data_bytes);
+    }
+    if (!any) return 0;
+    return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, 0, shape->head_dim, rows).total + data;
+}
+
 size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits) {
-    const int32_t s = sfi_plan_splits(shape, batch, max_tokens, num_splits);
-    if (!needs_workspace(s)) return 0;
-    return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, s, shape->head_dim).total;
+    return subset_workspace_size(shape, batch, max_tokens, num_splits, sfi::kMaxGroup);
 }
 
 sfi_status sfi_paged_kv_append(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const void *k_new,
@@ -390,10 +408,23 @@ sfi_status sfi_slow_dense_attn_with_scores(const sfi_attn_shape *shape, const sf
 size_t sfi_mixed_workspace_size(const sfi_attn_shape *shape, int32_t n_fast, int32_t n_slow, int32_t max_fast_tokens,
                                 int32_t max_dense_tokens) {
     if (check_shape(shape) != SFI_OK || n_fast < 0 || n_slow < 0) return 0;
-    const MixedPlan m = plan_mixed((int64_t)n_fast * shape->num_kv_heads, (int64_t)n_slow * shape->num_kv_heads,
-                                   max_fast_tokens, max_dense_tokens, sm_count_current_device());
-    if (m.fast_splits == 1 && m.slow_splits == 1) return 0;
-    return sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim).total;
+    const int hkv = shape->num_kv_heads;
+    const int sms = sm_count_current_device();
+    // One mode only (the chunked plans of SFI_ATTN_RAGGED): valid for every batch size up
+    // to n, like sfi_workspace_size. Both modes: this split of the requests.
+    const int32_t n = n_fast + n_slow;
+    const int32_t b_lo = (n_fast == 0 || n_slow == 0) ? 1 : n;
+    size_t data = 0;
+    bool any = false;
+    for (int32_t b = std::max(1, b_lo); b <= n; ++b) {
+        const int64_t f = n_slow == 0 ? b : n_fast, sl = n_fast == 0 ? b : n_slow;
+        const MixedPlan m = plan_mixed(f * hkv, sl * hkv, max_fast_tokens, max_dense_tokens, sms);
+        if (m.fast_splits == 1 && m.slow_splits == 1) continue;
+        any = true;
+        data = std::max(data, sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim).data_bytes);
+    }
+    if (!any) return 0;
+    return sfi::workspace_layout_slots((int64_t)n * hkv, 0, shape->head_dim).total + data;
 }
 
 sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, const sfi_compact_kv *compact,
@@ -443,7 +474,8 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
     p.slow_chunk_sb = m.slow_chunk_sb;
     p.splits = std::max(m.fast_splits, m.slow_splits);  // > 1: partial states go through the workspace
     if (p.splits > 1) {
-        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim);
+        const sfi::WorkspaceLayout l = sfi::workspace_layout_slots(m.units, m.slots, shape->head_dim,
+                                                                   sfi::kMaxGroup, workspace_bytes);
         if (!workspace || workspace_bytes < l.total || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0)
             return SFI_ERR_WORKSPACE;
         char *base = static_cast<char *>(workspace);
@@ -473,9 +505,7 @@ sfi_status sfi_mixed_decode_attn(const sfi_attn_shape *shape, const sfi_paged_kv
 size_t sfi_multi_workspace_size(const sfi_attn_shape *shape, int32_t batch, int32_t num_tokens, int32_t max_tokens,
                                 int32_t num_splits) {
     if (num_tokens < 1 || num_tokens > SFI_MAX_QUERY_TOKENS) return 0;
-    const int32_t s = sfi_plan_splits(shape, batch, max_tokens, num_splits);
-    if (!needs_workspace(s)) return 0;
-    return sfi::workspace_layout((int64_t)batch * shape->num_kv_heads, s, shape->head_dim, sfi::kMaxRows).total;
+    return subset_workspace_size(shape, batch, max_tokens, num_splits, sfi::kMaxRows);
 }
 
 sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_paged_kv *kv, int32_t sink, int32_t recent,

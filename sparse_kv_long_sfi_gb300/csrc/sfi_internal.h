@@ -76,13 +76,16 @@ struct AttnMaps {
     CUtensorMap comp_k, comp_v;  // rows = compact buffer rows (dummy copies of pool maps in dense mode)
 };
 
-// Workspace layout for `units` (request, KV head) pairs and `splits` splits.
+// Workspace layout for `units` (request, KV head) pairs and `splits` splits: the split
+// counters at the start, the partial states (data_bytes) at the end of a buffer of
+// `bytes` bytes (0: exactly `total`).
 struct WorkspaceLayout {
-    size_t count_off, ml_off, part_off, total;
+    size_t count_off, ml_off, part_off, data_bytes, total;
 };
 // Single-token launches keep kMaxGroup rows per partial slot, multi-token ones kMaxRows.
-WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int rows = kMaxGroup);
-WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows = kMaxGroup);
+WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int rows = kMaxGroup, size_t bytes = 0);
+WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows = kMaxGroup,
+                                       size_t bytes = 0);
 
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream);

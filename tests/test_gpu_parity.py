@@ -65,19 +65,55 @@ def _dense(prob, num_splits=0, scores=None, req_ids=None, ragged=False, max_toke
 def test_automatic_split_plans():
     """The automatic plans on this GPU: about 85% of one wave of two CTAs per SM (8 when
     that lands between 8 and 16), never fewer than four stages (16 sub-blocks) per split;
-    the workspace follows the plan (none inside a cluster)."""
+    the workspace follows the plans of every batch size up to the given one (none when
+    all of them merge inside a cluster)."""
     sfi = _sfi()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shape = sfi.AttnShape(16, 8, 128)
+
+    def plan(batch, L):
+        units, nb = batch * 8, (L + 15) // 16 + 1
+        s = max(1, sms * 2 * 17 // 20 // units)
+        if 8 < s < 16:
+            s = 8
+        return max(1, min(s, nb // 16, 256))
+
     for batch in (1, 2, 3, 4, 16, 64):
         for L in (1040, 16400, 65600):
-            units, nb = batch * 8, (L + 15) // 16 + 1
-            s = max(1, sms * 2 * 17 // 20 // units)
-            if 8 < s < 16:
-                s = 8
-            s = max(1, min(s, nb // 16, 256))
-            assert sfi.sfi_plan_splits(shape, batch, L, 0) == s, (batch, L)
-            assert (sfi.sfi_workspace_size(shape, batch, L, 0) == 0) == (s <= 8), (batch, L)
+            assert sfi.sfi_plan_splits(shape, batch, L, 0) == plan(batch, L), (batch, L)
+            needs = any(plan(b, L) > 8 for b in range(1, batch + 1))
+            assert (sfi.sfi_workspace_size(shape, batch, L, 0) > 0) == needs, (batch, L)
+
+
+@pytest.mark.parametrize("ragged", [False, True])
+def test_workspace_shared_by_calls_of_different_batch_sizes(ragged):
+    """One workspace, sized for 12 requests, serves calls on subsets of 3, 12, 5 and 12
+    requests in turn: each call's partial states stay clear of the split counters of
+    every other call (counters at the start, partial states at the end of the buffer),
+    so every output matches the oracle and the counters end zeroed."""
+    sfi = _sfi()
+    lens = [9000, 300, 5000, 40, 7000, 2500, 1200, 8100, 60, 3300, 6400, 900]
+    prob = Problem(seed=71, lens=lens, Hq=16, Hkv=8, D=128, S=4, W=32).to_device()
+    maxL = int(prob.lens.max()) + 16
+    splits = 0 if ragged else 12
+    ws = (sfi.alloc_ragged_workspace(prob.shape, prob.B, maxL, dense=True) if ragged
+          else sfi.alloc_workspace(prob.shape, prob.B, maxL, splits))
+    st = _status()
+    refs = [prob.oracle_dense(r) for r in range(prob.B)]
+    for subset in ([0, 4, 7], list(range(12)), [11, 2, 9, 0, 5], list(range(11, -1, -1))):
+        out = torch.full((prob.B, prob.Hq, prob.D), float("nan"), device="cuda")
+        lse = torch.full((prob.B, prob.Hq), float("nan"), device="cuda")
+        sfi.sfi_slow_dense_attn_with_scores(prob.shape, prob.d_kv, prob.S, prob.W, prob.d_q, out, lse, None,
+                                            req_ids=dev_i32(subset), max_tokens=maxL, num_splits=splits,
+                                            workspace=ws, dev_status=st,
+                                            flags=sfi.SFI_ATTN_RAGGED if ragged else 0)
+        torch.cuda.synchronize()
+        assert st.item() == 0
+        assert counters_zero(ws, prob.B * prob.Hkv), subset
+        o, l = out.cpu().numpy(), lse.cpu().numpy()
+        for r in subset:
+            assert_close(o[r], refs[r][0], f"out r={r} subset={subset}")
+            assert_close(l[r], refs[r][1], f"lse r={r} subset={subset}")
 
 
 @pytest.mark.parametrize("D,Hq,Hkv", [(128, 16, 8), (128, 32, 8), (128, 64, 8), (64, 8, 2), (128, 8, 8)])
