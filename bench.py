@@ -207,7 +207,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "ca4127d6d3c66598", "fast": 68_272_640 + 568_064, "slow": 1_073_944_832 + 6_990_080}
+PROFILED_TRAFFIC = {"sha256_16": "ea17a2e610913927", "fast": 68_272_640 + 568_064, "slow": 1_073_944_832 + 6_990_080}
 
 
 def profiled_traffic(kind):

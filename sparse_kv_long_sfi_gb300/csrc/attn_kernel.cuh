@@ -29,13 +29,16 @@
 //    with its own causal / window bounds, at the same number of mma instructions.
 //  * The slow step sums the C fragments over the group's rows with warp shuffles and
 //    writes the fp32 masked scores.
-//  * With k_new/v_new the consumer warp owning position L - 1 writes the current token
-//    into its tile and into the page (the append fused into the attention).
-//  * Warps merge through shared memory. Splits of a unit merge in-kernel: with up to
-//    8 splits the unit's CTAs form one thread-block cluster and rank 0 reads the
-//    others' partial (m, l, o) states through distributed shared memory; with more,
-//    the last CTA of the unit (atomic counter, self-resetting) merges them from a
-//    global workspace.
+//  * With k_new/v_new the consumer warp owning position L - 1 (the positions of the T
+//    query tokens, multi-token form) stages the new K/V in shared memory before the
+//    stream, writes it to the page early in the stream and into its tile when the
+//    sub-block arrives (the append fused into the attention).
+//  * Warps merge through shared memory in two passes (per-row weights, then 4-float
+//    chunks). Splits of a unit merge in-kernel: with up to 8 splits the unit's CTAs
+//    form one thread-block cluster and the other ranks store their partial (m, l, o)
+//    states into rank 0's shared memory (or rank 0 reads them through distributed
+//    shared memory when they do not fit); with more, the last CTA of the unit (atomic
+//    counter, self-resetting) merges them from a global workspace.
 //  * Every wait on the pipeline or on a peer CTA is bounded and reports
 //    SFI_DEV_TIMEOUT instead of hanging.
 #pragma once
