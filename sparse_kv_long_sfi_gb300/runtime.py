@@ -205,20 +205,24 @@ class SFIDecoder:
                                    dev_status=self.dev_status, stream=self.main)
         return None, None
 
-    def _enter(self):
+    def _enter(self, name: str):
         """Order the main stream after the caller's stream (inputs such as seq_lens, q or
         k_new may have just been written there; torch streams do not synchronise with
-        each other implicitly)."""
+        each other implicitly), and open the step's NVTX range ("sfi.<name>") so that a
+        profiler's timeline groups its launches."""
+        torch.cuda.nvtx.range_push("sfi." + name)
         cur = torch.cuda.current_stream(self.main.device)
         if cur != self.main:
             self.main.wait_stream(cur)
 
-    def _leave(self):
+    def _leave(self, close_range: bool = True):
         """Order the caller's stream after the main stream (outputs, and reuse of the
-        input tensors' memory by the caching allocator)."""
+        input tensors' memory by the caching allocator); close the step's NVTX range."""
         cur = torch.cuda.current_stream(self.main.device)
         if cur != self.main:
             cur.wait_stream(self.main)
+        if close_range:
+            torch.cuda.nvtx.range_pop()
 
     def _refresh(self, i: int, L: LayerBuffers, kv: PagedKV, seq_lens: torch.Tensor,
                  req_ids: Optional[torch.Tensor], n: Optional[int]):
@@ -253,7 +257,7 @@ class SFIDecoder:
     def slow_step(self, io: StepIO, seq_lens: torch.Tensor, req_ids: Optional[torch.Tensor] = None,
                   append: bool = True):
         n = None if req_ids is None else req_ids.numel()
-        self._enter()
+        self._enter("slow_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
@@ -268,7 +272,7 @@ class SFIDecoder:
         refresh layer, which keeps one layer's sparse state current at every step."""
         n = None if req_ids is None else req_ids.numel()
         refresh = set(int(x) for x in refresh_layers)
-        self._enter()
+        self._enter("fast_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
@@ -288,7 +292,7 @@ class SFIDecoder:
         """One step where each request is slow or fast (ASPIRE-style mixed batch): one
         attention launch per layer for both kinds (or two with single_launch_mixed off)."""
         ns, nf = slow_ids.numel(), fast_ids.numel()
-        self._enter()
+        self._enter("mixed_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
@@ -337,7 +341,7 @@ class SFIDecoder:
         refresh_selection."""
         T, n = int(num_tokens), None if req_ids is None else req_ids.numel()
         ws_v, _ = self._multi_workspaces()
-        self._enter()
+        self._enter("verify_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
@@ -355,7 +359,7 @@ class SFIDecoder:
         verify_step, at the accepted lengths seq_lens (at most the verified ones), on
         the aux stream; the next use of each layer's compact buffer waits for it."""
         n = None if req_ids is None else req_ids.numel()
-        self._enter()
+        self._enter("refresh_selection")
         self.aux.wait_stream(self.main)
         for i, L in enumerate(self.layers):
             self._refresh(i, L, self.kv(i, seq_lens), seq_lens, req_ids, n)
@@ -368,7 +372,7 @@ class SFIDecoder:
         go into the pages first. seq_lens count the T tokens."""
         T, n = int(num_tokens), None if req_ids is None else req_ids.numel()
         _, ws_d = self._multi_workspaces()
-        self._enter()
+        self._enter("draft_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             self._wait_aux(i)
@@ -383,7 +387,7 @@ class SFIDecoder:
 
     def dense_step(self, io: StepIO, seq_lens: torch.Tensor, append: bool = True):
         """Full-KV decode step (the baseline of the paper's Table 1)."""
-        self._enter()
+        self._enter("dense_step")
         for i, L in enumerate(self.layers):
             kv = self.kv(i, seq_lens)
             kn, vn = self._append(i, kv, io, append, None, None)
@@ -399,4 +403,4 @@ class SFIDecoder:
         """Make the main stream (and the caller's stream) wait for all outstanding aux work."""
         for i in range(len(self.layers)):
             self._wait_aux(i)
-        self._leave()
+        self._leave(close_range=False)
