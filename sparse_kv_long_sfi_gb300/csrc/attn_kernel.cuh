@@ -1169,8 +1169,10 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     // before it depends on the unit's metadata, which all of them read alike): after
     // it, each CTA's merge barrier is initialised for remote arrivals. (Letting the
     // producer warp issue the ring's first fill before this barrier was measured
-    // slower: fast step at batch 16, 13.6 -> 14.3 us per launch.)
-    if (CLUSTER) cluster_sync_all();
+    // slower: fast step at batch 16, 13.6 -> 14.3 us per launch. A relaxed cluster
+    // arrive instead of a release one: drafts at batch 16, T = 1 / 4 / 8, 14.7 / 15.3 /
+    // 17.9 -> 14.5 / 15.2 / 17.3 us per launch.)
+    if (CLUSTER) cluster_sync_after_init();
     else __syncthreads();
 
     if (warp == kConsumerWarps) {
