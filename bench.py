@@ -207,7 +207,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "ea17a2e610913927", "fast": 68_272_640 + 568_064, "slow": 1_073_944_832 + 6_990_080}
+PROFILED_TRAFFIC = {"sha256_16": "2162431949b7fa8d", "fast": 68_272_384 + 711_680, "slow": 1_073_961_216 + 6_628_352}
 
 
 def profiled_traffic(kind):
