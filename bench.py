@@ -825,13 +825,46 @@ def retention_sweep(cy, dev, peak):
                      "us_per_step": round(us, 2), "GBps": round(by / (us * 1e-6) / 1e9, 1),
                      "frac_of_peak": round(by / (us * 1e-6) / 1e9 / peak, 3),
                      "speedup_vs_dense": round(us_dense / us, 3), "table1_speedup_context": TABLE1[n]})
+    # Latency floor of a fast launch: the same graph over the smallest state (16 sink rows,
+    # no selected rows, one recent page: 32 tokens per (request, KV head)), where the
+    # bytes are negligible and the launch costs its fixed start-up and merge.
+    Sf, Wf = 16, 16
+    k0 = torch.zeros((B,), dtype=torch.int32, device=dev)
+    for i, Lb in enumerate(layers):
+        kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq_steps[0])
+        sfi.sfi_slow_dense_attn_with_scores(shape, kv, Sf, Wf, q_all[0, i], out[i], None, Lb.scores,
+                                            max_tokens=L0 + P, workspace=ws_dense, stream=dec.main)
+        sfi.sfi_select_topk(Lb.scores, Hkv, seq_steps[0], Sf, Wf, k0, Lb.idx, Lb.compact.count, stream=dec.main)
+        sfi.sfi_compact_gather(shape, kv, Lb.idx, Lb.compact.count, Sf, Lb.compact, stream=dec.main)
+    max_tok_f = Sf + Wf + 2 * P
+    ws_floor = sfi.alloc_workspace(shape, B, max_tok_f, device=dev)
+
+    def floor_step():
+        for i, Lb in enumerate(layers):
+            kv = sfi.PagedKV(Lb.k_pool, Lb.v_pool, batch.page_table, seq)
+            sfi.sfi_fast_decode_attn(shape, kv, Lb.compact, Sf, Wf, q_all[1, i], out[i], None,
+                                     k_new=kn_all[1, i], v_new=vn_all[1, i], max_tokens=max_tok_f,
+                                     workspace=ws_floor, stream=dec.main, flags=dec.attn_flags)
+
+    floor_us = time_graph(floor_step) / NL
+    for r in rows:
+        per = r["us_per_step"] / NL
+        by_launch = r["GBps"] * 1e9 * per * 1e-6
+        r["us_per_launch"] = round(per, 3)
+        r["bytes_at_peak_us_per_launch"] = round(by_launch / (peak * 1e3), 3)
+        r["over_latency_floor_us_per_launch"] = round(per - floor_us, 3)
     # restore the main cycle's selection state
     dec.pending = [False] * len(layers)
     return {"batch": B, "dense_us_per_step": round(us_dense, 2),
             "dense_GBps": round(NL * by_dense / (us_dense * 1e-6) / 1e9, 1),
             "dense_frac_of_peak": round(NL * by_dense / (us_dense * 1e-6) / 1e9 / peak, 3),
+            "latency_floor_us_per_launch": round(floor_us, 3),
+            "latency_floor_state": f"sink {Sf}, k 0, recent {Wf}: {Sf + Wf} tokens per (request, KV head)",
             "points": rows, "note": f"fast and dense steps include the (fused) paged append; {NL} layers per step; "
-                                    "Table 1 speedups are the paper's (hardware unstated), context only"}
+                                    "Table 1 speedups are the paper's (hardware unstated), context only; "
+                                    "latency_floor_us_per_launch is a fast launch over the smallest state (its fixed "
+                                    "start-up and merge cost), bytes_at_peak the point's bytes at the measured copy "
+                                    "bandwidth: a point is latency-bound where its time sits near the floor plus that"}
 
 
 def speculative_sweep(dec, layers, batch, shape, q_all, seq_steps, NL, B, Hq, Hkv, D, P, L0, S, W, k_main, dev, peak,
