@@ -233,27 +233,28 @@ def test_verify_with_fused_append_matches_oracle(T, splits, flags):
     _verify_fused_case(T, splits, flags, [300, 1023, 17, 40])
 
 
-@pytest.mark.parametrize("T,splits", [(8, 2), (8, 3), (16, 2)])
-def test_verify_fused_append_across_splits(T, splits):
+@pytest.mark.parametrize("T,splits,D", [(8, 2, 128), (8, 3, 128), (16, 2, 128), (8, 2, 64), (4, 12, 64)])
+def test_verify_fused_append_across_splits(T, splits, D):
     """Query tokens that straddle a page boundary and a split boundary of a short request:
     the first split of a cluster appends its part straight from global memory (its receive
-    region takes the other splits' partials), the later ones from shared-memory staging."""
-    _verify_fused_case(T, splits, 1, [10, 13, 5, 2])
+    region takes the other splits' partials), the later ones from shared-memory staging;
+    at D = 64 too, and with the workspace merge (12 splits)."""
+    _verify_fused_case(T, splits, 1, [10, 13, 5, 2] if splits <= 3 else [300, 1023, 17, 40], D=D)
 
 
-def _verify_fused_case(T, splits, flags, lens0):
+def _verify_fused_case(T, splits, flags, lens0, D=128):
     sfi = _sfi()
     Hq, Hkv = (8, 8) if T == 16 else (16, 8)
-    prob = Problem(seed=800 + T, lens=lens0, Hq=Hq, Hkv=Hkv, D=128, S=4, W=32,
+    prob = Problem(seed=800 + T, lens=lens0, Hq=Hq, Hkv=Hkv, D=D, S=4, W=32,
                    extra_tokens=T).to_device()
     g = syn.rng(403, T)
-    kn, vn = syn.normal_bf16(g, (prob.B, T, Hkv, 128)), syn.normal_bf16(g, (prob.B, T, Hkv, 128))
+    kn, vn = syn.normal_bf16(g, (prob.B, T, Hkv, D)), syn.normal_bf16(g, (prob.B, T, Hkv, D))
     lens = prob.lens + T
     prob.set_lens(lens)
-    q = _queries(810 + T, prob.B, T, Hq, 128)
+    q = _queries(810 + T, prob.B, T, Hq, D)
     stride = int(lens.max())
     scores = torch.full((prob.B, Hkv, stride), float("nan"), device="cuda")
-    out = torch.full((prob.B, T, Hq, 128), float("nan"), device="cuda")
+    out = torch.full((prob.B, T, Hq, D), float("nan"), device="cuda")
     maxL = stride + 16
     ws = sfi.alloc_multi_workspace(prob.shape, prob.B, T, maxL, splits)
     st = _status()
@@ -264,16 +265,16 @@ def _verify_fused_case(T, splits, flags, lens0):
     assert st.item() == 0
     for r in range(prob.B):
         oracle.paged_append_tokens(prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], lens[r], T, kn[r], vn[r],
-                                   Hkv, 128, 16)
+                                   Hkv, D, 16)
     np.testing.assert_array_equal(host_bf16(prob.d_kv.k_pool), prob.kv.k_pool)
     np.testing.assert_array_equal(host_bf16(prob.d_kv.v_pool), prob.kv.v_pool)
     o, sc = out.cpu().numpy(), scores.cpu().numpy()
     for r in range(prob.B):
         o_ref, _ = oracle.verify_attn(q[r], prob.kv.k_pool, prob.kv.v_pool, prob.kv.page_table[r], lens[r], T, Hq, Hkv,
-                                      128, 16)
+                                      D, 16)
         assert_close(o[r], o_ref, f"out r={r}")
         ref = oracle.verify_scores(q[r], prob.kv.k_pool, prob.kv.page_table[r], lens[r], T, prob.S, prob.W, Hq, Hkv,
-                                   128, 16, stride=stride)
+                                   D, 16, stride=stride)
         L = lens[r]
         assert np.array_equal(np.isneginf(sc[r, :, :L]), np.isneginf(ref[:, :L]))
 
