@@ -440,12 +440,24 @@ SFI_API size_t sfi_workspace_size(const sfi_attn_shape *shape, int32_t batch, in
 /*
  * sfi_plan_splits - the split count the attention entry points will use for these
  * arguments on the current device (for reports and tests). 0 on invalid input.
- * Automatic plans (num_splits = 0) fill one wave of two CTAs per SM over the
- * (request, KV head) units; above 8 splits they take one CTA per SM when that still
- * gives at least 16 splits, else 8; every split keeps at least four stages of 64
- * tokens. An explicit num_splits is honoured down to two stages per split.
+ * Automatic plans (num_splits = 0) give the (request, KV head) units about 85% of one
+ * wave of two CTAs per SM; a count between 8 and 16 becomes 8. Every split keeps at
+ * least four stages of 64 tokens, or three while the plan stays at most 8 splits (the
+ * splits of a unit then merge inside a thread-block cluster). A plan of 2..8 splits
+ * also leaves a ninth of the SM slots free in whole clusters, by the count of
+ * sfi_attn_cluster_capacity, one split fewer at a time until it does. An explicit
+ * num_splits is honoured down to two stages per split.
  */
 SFI_API int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_tokens, int32_t num_splits);
+
+/*
+ * sfi_attn_cluster_capacity - how many thread-block clusters of cluster_size attention
+ * CTAs (1..8) the current device holds at once (its occupancy query for the attention
+ * kernel, cached per device). A cluster is placed whole on one GPC, so this can be
+ * below the SM slots divided by cluster_size. 0 on invalid input, when there is no
+ * device, or when the query fails.
+ */
+SFI_API int32_t sfi_attn_cluster_capacity(int32_t cluster_size);
 
 /* Human-readable name of a status code (static string). */
 SFI_API const char *sfi_status_string(sfi_status status);

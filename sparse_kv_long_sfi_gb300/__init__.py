@@ -11,8 +11,9 @@ from .api import (SFI_ATTN_EARLY_KV_PREFETCH, SFI_ATTN_RAGGED, SFI_ATTN_TEST_WIT
                   alloc_ragged_workspace, alloc_workspace, sfi_compact_gather, sfi_dense_verify_attn,
                   sfi_fast_decode_attn, sfi_fast_decode_attn_noalloc, sfi_mixed_decode_attn,
                   sfi_mixed_workspace_size, sfi_multi_workspace_size, sfi_paged_kv_append,
-                  sfi_paged_kv_append_tokens, sfi_plan_splits, sfi_select_compact, sfi_select_topk,
-                  sfi_slow_dense_attn_with_scores, sfi_sparse_draft_attn, sfi_version, sfi_workspace_size)
+                  sfi_paged_kv_append_tokens, sfi_plan_splits, sfi_attn_cluster_capacity, sfi_select_compact,
+                  sfi_select_topk, sfi_slow_dense_attn_with_scores, sfi_sparse_draft_attn, sfi_version,
+                  sfi_workspace_size)
 from .runtime import (DecodeBatch, LayerBuffers, SFIDecoder, SlowFastSchedule, StepIO, allocate_layers,
                       compact_layout)
 
@@ -22,6 +23,7 @@ __all__ = [
     "alloc_workspace", "sfi_compact_gather", "sfi_dense_verify_attn", "sfi_fast_decode_attn",
     "sfi_fast_decode_attn_noalloc", "sfi_mixed_decode_attn", "sfi_mixed_workspace_size",
     "sfi_multi_workspace_size", "sfi_paged_kv_append", "sfi_paged_kv_append_tokens", "sfi_plan_splits",
+    "sfi_attn_cluster_capacity",
     "sfi_select_compact", "sfi_select_topk", "sfi_slow_dense_attn_with_scores", "sfi_sparse_draft_attn",
     "sfi_version", "sfi_workspace_size", "DecodeBatch", "LayerBuffers", "SFIDecoder", "SlowFastSchedule",
     "StepIO", "allocate_layers", "compact_layout",

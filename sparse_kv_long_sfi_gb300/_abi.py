@@ -69,6 +69,7 @@ PROTOTYPES = {
                                              c_vp, c_vp, c_i32, c_i32, c_i32, c_u32, c_vp, c_vp]),
     "sfi_workspace_size": (c_sz, [P_SHAPE, c_i32, c_i32, c_i32]),
     "sfi_plan_splits": (c_i32, [P_SHAPE, c_i32, c_i32, c_i32]),
+    "sfi_attn_cluster_capacity": (c_i32, [c_i32]),
     "sfi_status_string": (ctypes.c_char_p, [c_i32]),
     "sfi_version": (c_i32, []),
 }

@@ -341,6 +341,10 @@ def sfi_plan_splits(shape: AttnShape, batch: int, max_tokens: int, num_splits: i
     return int(_abi.lib().sfi_plan_splits(ctypes.byref(shape.c()), int(batch), int(max_tokens), int(num_splits)))
 
 
+def sfi_attn_cluster_capacity(cluster_size: int) -> int:
+    return int(_abi.lib().sfi_attn_cluster_capacity(int(cluster_size)))
+
+
 def sfi_version() -> int:
     return int(_abi.lib().sfi_version())
 

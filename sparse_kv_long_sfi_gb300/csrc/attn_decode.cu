@@ -27,6 +27,41 @@ WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int ro
     return workspace_layout_slots(units, units * splits, head_dim, rows, bytes);
 }
 
+int attn_cluster_capacity(int size) {
+    static std::atomic<int> cache[64][kMaxClusterSplits + 1];
+    int dev = 0;
+    if (size < 1 || size > kMaxClusterSplits || cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const bool cacheable = dev >= 0 && dev < 64;
+    if (cacheable) {
+        const int v = cache[dev][size].load(std::memory_order_relaxed);
+        if (v > 0) return v;
+    }
+    using T = AttnTile<128>;
+    auto kern = attn_decode_kernel<128, kModeFast, false, true, false>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, T::kSmemBytes) != cudaSuccess) {
+        cudaGetLastError();
+        return 0;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)size);
+    cfg.blockDim = dim3(kAttnThreads);
+    cfg.dynamicSmemBytes = T::kSmemBytes;
+    cudaLaunchAttribute attr;
+    attr.id = cudaLaunchAttributeClusterDimension;
+    attr.val.clusterDim.x = (unsigned)size;
+    attr.val.clusterDim.y = 1;
+    attr.val.clusterDim.z = 1;
+    cfg.attrs = &attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess) {
+        cudaGetLastError();  // leave no error behind for the next launch's check
+        return 0;
+    }
+    if (cacheable && n > 0) cache[dev][size].store(n, std::memory_order_relaxed);
+    return n;
+}
+
 template <int D, bool CLUSTER>
 static cudaError_t launch_mode(int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p, int batch,
                                cudaStream_t stream) {

@@ -84,13 +84,23 @@ sfi_status check_paged(const sfi_attn_shape *s, const sfi_paged_kv *kv) {
 }
 
 // Split-KV plan of one attention launch. Automatic plans fill about 85% of one wave of
-// resident CTAs (two per SM) and keep at least four full stages of sub-blocks per split;
-// an explicit request is honoured down to two stages per split. Leaving a sixth of the
-// slots free lets the next launch's CTAs become resident and start streaming while this
-// one drains (batch 1 at 16K, dense: 32 splits, 256 CTAs, 15.9 us per layer against 20.6
-// us for 38 splits, 304 CTAs). Plans of up to kMaxClusterSplits merge inside a
-// thread-block cluster (no workspace); between 8 and 16 splits the plan stays at 8;
-// from 16 on the last CTA of a unit merges the splits from the workspace.
+// resident CTAs (two per SM); an explicit request is honoured down to two stages per
+// split. Leaving a sixth of the slots free lets the next launch's CTAs become resident
+// and start streaming while this one drains (batch 1 at 16K, dense: 32 splits, 256 CTAs,
+// 15.9 us per layer against 20.6 us for 38 splits, 304 CTAs). Plans of up to
+// kMaxClusterSplits merge inside a thread-block cluster (no workspace); between 8 and 16
+// splits the plan stays at 8; from 16 on the last CTA of a unit merges the splits from
+// the workspace. How short a split may get depends on its merge: inside a cluster three
+// stages (12 sub-blocks) per split pay for the CTA's start-up (batch 1, a bound of 1056
+// tokens: 6 splits of 11 sub-blocks, 5.05 us per layer against 6.22 us for 4 splits of
+// 16); a workspace merge publishes through a global release and wants four stages per
+// split.
+// The free slots are counted in whole clusters (one cluster of 8 needs 8 free slots of
+// one GPC). On a GPU that holds 36 clusters of 8, 38 of 7, 46 of 6 and 58 of 5 (two
+// CTAs per SM, 152 SMs): batch 4 at a bound of 2080 tokens, 32 clusters of 8 (32 slots
+// free) take 10.3 us per layer against 8.1 us for 32 clusters of 7 (42 free), and at 16K
+// dense 53.0 against 47.1 us; batch 5 at 1056 tokens, 40 clusters of 6 (36 free) take
+// 5.1 us against 5.5 us for 40 clusters of 5.
 int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_count) {
     constexpr int kMaxSplits = 256;
     if (units <= 0) return 1;
@@ -104,7 +114,16 @@ int plan_splits(int64_t units, int32_t max_tokens, int32_t requested, int sm_cou
     } else {
         s = (int)std::max<int64_t>(1, (int64_t)sm_count * sfi::kAttnCtasPerSm * 17 / 20 / units);
         if (s > sfi::kMaxClusterSplits && s < 2 * sfi::kMaxClusterSplits) s = sfi::kMaxClusterSplits;
-        s = std::min(s, std::max(1, nb / (4 * sfi::kConsumerWarps)));
+        const int in_cluster = std::min(sfi::kMaxClusterSplits, (nb + 3 * sfi::kConsumerWarps - 1) / (3 * sfi::kConsumerWarps));
+        s = std::min(s, std::max({1, nb / (4 * sfi::kConsumerWarps), in_cluster}));
+        // A cluster is placed whole, so the slots the next launch's early start finds free
+        // count in whole clusters: keep a ninth of the SM slots free in those terms.
+        const int64_t reserve = (int64_t)sm_count * sfi::kAttnCtasPerSm / 9;
+        while (s > 1 && s <= sfi::kMaxClusterSplits) {
+            const int cap = sfi::attn_cluster_capacity(s);
+            if (cap <= 0 || ((int64_t)cap - units) * s >= reserve) break;
+            --s;
+        }
     }
     return std::max(1, std::min(s, kMaxSplits));
 }
@@ -279,6 +298,8 @@ int32_t sfi_plan_splits(const sfi_attn_shape *shape, int32_t batch, int32_t max_
     if (check_shape(shape) != SFI_OK || batch < 0 || num_splits < 0) return 0;
     return plan_splits((int64_t)batch * shape->num_kv_heads, max_tokens, num_splits, sm_count_current_device());
 }
+
+int32_t sfi_attn_cluster_capacity(int32_t cluster_size) { return sfi::attn_cluster_capacity(cluster_size); }
 
 // Bytes for the split plans of every batch size 1..batch sharing one buffer: the counters
 // of `batch` requests plus the largest partial-state block of any of those plans (each

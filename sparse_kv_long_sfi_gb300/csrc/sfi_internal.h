@@ -87,6 +87,11 @@ WorkspaceLayout workspace_layout(int64_t units, int splits, int head_dim, int ro
 WorkspaceLayout workspace_layout_slots(int64_t units, int64_t slots, int head_dim, int rows = kMaxGroup,
                                        size_t bytes = 0);
 
+// Clusters of `size` attention CTAs (1..kMaxClusterSplits) the current device holds at
+// once (the occupancy query of the head-dim-128 kernel, cached per device); 0 when the
+// query fails or there is no device.
+int attn_cluster_capacity(int size);
+
 cudaError_t launch_attention(int head_dim, int mode, bool with_scores, const AttnMaps &maps, const AttnParams &p,
                              int batch, cudaStream_t stream);
 // Multi-token launch: mode kModeFast (draft over the sparse state) or kModeDense

@@ -114,6 +114,8 @@ def test_workspace_size_rejects_bad_shapes(libsfi):
     assert libsfi.sfi_plan_splits(ctypes.byref(sh), 4, 1024, 0) == 0
     assert libsfi.sfi_plan_splits(ctypes.byref(_shape()), 4, 0, 0) == 1  # no token bound: one split
     assert libsfi.sfi_plan_splits(ctypes.byref(_shape()), 4, 4096, 3) == 3  # explicit request honoured
+    for bad in (0, -1, 9, 16):
+        assert libsfi.sfi_attn_cluster_capacity(bad) == 0
 
 
 def test_multi_token_calls_validate_on_the_host(libsfi):

@@ -64,22 +64,32 @@ def _dense(prob, num_splits=0, scores=None, req_ids=None, ragged=False, max_toke
 # ---------------------------------------------------------------------------
 def test_automatic_split_plans():
     """The automatic plans on this GPU: about 85% of one wave of two CTAs per SM (8 when
-    that lands between 8 and 16), never fewer than four stages (16 sub-blocks) per split;
-    the workspace follows the plans of every batch size up to the given one (none when
-    all of them merge inside a cluster)."""
+    that lands between 8 and 16), never fewer than three stages (12 sub-blocks) per split
+    while the splits merge inside a cluster and four (16 sub-blocks) beyond it, and a
+    cluster plan leaves a ninth of the SM slots free in whole clusters; the workspace
+    follows the plans of every batch size up to the given one (none when all of them
+    merge inside a cluster)."""
     sfi = _sfi()
     sms = torch.cuda.get_device_properties(0).multi_processor_count
     shape = sfi.AttnShape(16, 8, 128)
+    cap = {c: sfi.sfi_attn_cluster_capacity(c) for c in range(1, 9)}
+    assert cap[1] == 2 * sms  # two CTAs per SM
+    for c in range(2, 9):  # whole clusters never hold more CTAs than the SM slots
+        assert 0 < cap[c] * c <= 2 * sms, (c, cap[c])
 
     def plan(batch, L):
         units, nb = batch * 8, (L + 15) // 16 + 1
         s = max(1, sms * 2 * 17 // 20 // units)
         if 8 < s < 16:
             s = 8
-        return max(1, min(s, nb // 16, 256))
+        s = max(1, min(s, max(nb // 16, min(8, -(-nb // 12))), 256))
+        while 1 < s <= 8 and (cap[s] - units) * s < sms * 2 // 9:
+            s -= 1
+        return s
 
-    for batch in (1, 2, 3, 4, 16, 64):
-        for L in (1040, 16400, 65600):
+    assert plan(1, 1056) == 6 and plan(16, 16400) == 2  # the two workloads of the decode step
+    for batch in (1, 2, 3, 4, 5, 8, 16, 64):
+        for L in (150, 1040, 1500, 2100, 16400, 65600):
             assert sfi.sfi_plan_splits(shape, batch, L, 0) == plan(batch, L), (batch, L)
             needs = any(plan(b, L) > 8 for b in range(1, batch + 1))
             assert (sfi.sfi_workspace_size(shape, batch, L, 0) > 0) == needs, (batch, L)
