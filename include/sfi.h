@@ -315,7 +315,9 @@ SFI_API sfi_status sfi_dense_verify_attn(const sfi_attn_shape *shape, const sfi_
  * sees exactly what sfi_fast_decode_attn at length L_t sees, compact rows
  * [0, min(S, L_t) + count[r]) and the recent window [max(S, L_t - W), L_t); so the
  * result equals T single-token fast steps. A non-empty selection (count[r] > 0)
- * needs L - T + 1 >= S (else SFI_DEV_K_OVERFLOW).
+ * needs L - T + 1 >= S (else SFI_DEV_K_OVERFLOW). With T = 1 the call is
+ * sfi_fast_decode_attn (same kernel; flags other than SFI_ATTN_EARLY_KV_PREFETCH are
+ * ignored, and the token may also lie in the sink).
  *   max_tokens : an upper bound on S + max count + W + T + P (split planning only)
  *   num_splits, flags, workspace : as for sfi_dense_verify_attn
  * Device errors: those of sfi_fast_decode_attn.

@@ -279,9 +279,10 @@ def _verify_fused_case(T, splits, flags, lens0, D=128):
         assert np.array_equal(np.isneginf(sc[r, :, :L]), np.isneginf(ref[:, :L]))
 
 
-@pytest.mark.parametrize("T,flags", [(4, 1), (8, 0)])
+@pytest.mark.parametrize("T,flags", [(4, 1), (8, 0), (1, 1)])
 def test_draft_with_fused_append_matches_oracle(T, flags):
-    """k_new/v_new given to the draft pass: equals the T-token append followed by the draft."""
+    """k_new/v_new given to the draft pass: equals the T-token append followed by the draft
+    (T = 1 runs the single-token fast-step kernel)."""
     sfi = _sfi()
     S, W, Hq, Hkv, D = 4, 32, 16, 8, 128
     lens_slow = [1024, 530, 36]
