@@ -36,8 +36,9 @@
 //  * Warps merge through shared memory in two passes (per-row weights, then 4-float
 //    chunks). Splits of a unit merge in-kernel: with up to 8 splits the unit's CTAs
 //    form one thread-block cluster and the other ranks store their partial (m, l, o)
-//    states into rank 0's shared memory (or rank 0 reads them through distributed
-//    shared memory when they do not fit); with more, the last CTA of the unit (atomic
+//    states into rank 0's shared memory with asynchronous stores that complete on rank
+//    0's mbarrier (or rank 0 reads them through distributed shared memory when they do
+//    not fit); with more, the last CTA of the unit (atomic
 //    counter, self-resetting) merges them from a global workspace.
 //  * Every wait on the pipeline or on a peer CTA is bounded and reports
 //    SFI_DEV_TIMEOUT instead of hanging.
@@ -902,8 +903,9 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
 // partial is written. Without a cluster the partials are in the workspace (slots from
 // slot0) and workspace_merge combines them. When the unit's splits form a thread-block
 // cluster, the other CTAs either have pushed their partials into rank 0's receive region
-// `recv` with distributed shared-memory stores (`push`; each slot holds o [rows][D],
-// m [rows], l [rows]) or keep them in their own cp_o [rows][D], cp_m, cp_l for rank 0 to
+// `recv` with asynchronous distributed shared-memory stores that complete their bytes on
+// rank 0's `merge_bar` (`push`; each slot holds o [rows][D], m [rows], l [rows]) or keep
+// them in their own cp_o [rows][D], cp_m, cp_l for rank 0 to
 // pull, when they do not fit. Rank 0 merges in two passes: one thread per row derives
 // the row's maximum, normaliser and the splits' weights (into `wsc`: [kMaxClusterSplits]
 // [kRows] weights, then [kRows] output scales 1 / l and [kRows] natural-log LSEs), then
@@ -925,9 +927,8 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, b
     const int csize = splits;
     if (split != 0) {
         if (push) {
-            // release: this thread's stores into rank 0's receive region
-            mbar_arrive_remote(cluster_map(smem_u32(merge_bar), 0));
-            // Rank 0 signals once every push has landed; only then may this CTA exit.
+            // This CTA's asynchronous stores complete on rank 0's barrier by themselves. Rank 0
+            // signals once every push has landed; only then may this CTA exit.
             if (ctid == 0 && !mbar_wait_cluster_bounded(merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
         } else {
             consumer_bar_sync();  // this CTA's partial is complete in its shared memory
@@ -941,7 +942,7 @@ __device__ __forceinline__ void merge_splits(const AttnParams &p, float *recv, b
     }
     bool got;
     if (push) {
-        got = mbar_wait_cluster_bounded(merge_bar, 0);  // acquire: the peers' pushes
+        got = mbar_wait_cluster_bounded(merge_bar, 0);  // every pushed byte has landed
         // The pushed partials are in this CTA's memory now: the peers may exit. The signal
         // orders nothing (a release here stalled the merge by about 1 us).
         if (got && ctid >= 1 && ctid < csize) mbar_arrive_remote_relaxed(cluster_map(smem_u32(merge_bar), ctid));
@@ -1152,15 +1153,16 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             mbar_init(&full_bar[i], kConsumerWarps);
             mbar_init(&empty_bar[i], kConsumerWarps);
         }
-        // push merge: every consumer thread of every other CTA arrives once at rank 0;
+        // push merge: rank 0's barrier expects the bytes of the other CTAs' partials (their
+        // asynchronous stores complete them); pull merge: one arrival per other CTA;
         // workspace merge: the last CTA's bulk copies of the unit's partials
+        const int mrows = MQ ? p.rows : p.group;
+        const bool push0 = CLUSTER && split == 0 && cluster_push_fits<D>(splits, mrows, kPushBytes);
         if (CLUSTER)
-            mbar_init(&merge_bar, split != 0 ? 1u
-                                  : cluster_push_fits<D>(splits, MQ ? p.rows : p.group, kPushBytes)
-                                      ? (uint32_t)(splits - 1) * kConsumerWarps * 32
-                                      : (uint32_t)(splits - 1));
+            mbar_init(&merge_bar, split != 0 || push0 ? 1u : (uint32_t)(splits - 1));
         else
             mbar_init(&merge_bar, 1u);
+        if (push0) mbar_arrive_expect_tx(&merge_bar, (uint32_t)((splits - 1) * mrows * (D + 2) * 4));
         s_timeout = 0;
         s_bad = 0;
         fence_barrier_init();
@@ -1523,6 +1525,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     const bool remote = push && split != 0;
     const uint32_t rdst =
         remote ? cluster_map(smem_u32(recv), 0) + (uint32_t)((split - 1) * cluster_slot_floats<D>(rows)) * 4u : 0u;
+    const uint32_t rbar = remote ? cluster_map(smem_u32(&merge_bar), 0) : 0u;  // completes the pushed bytes
     const int64_t wslot = slot0 * kRows + (int64_t)split * rows;  // workspace slot of row 0 (packed per unit)
     // Two passes: one thread per row takes the row's maximum over the warps, turns each
     // warp's maximum into its weight 2^(m_w - M) and sums the normaliser; then each
@@ -1550,8 +1553,8 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             wsc[row] = 1.f / lsum;
             wsc[kRows + row] = (M + log2f(lsum)) * kLn2;
         } else if (remote) {
-            st_cluster_f32(rdst + (rows * D + row) * 4, M);
-            st_cluster_f32(rdst + (rows * D + rows + row) * 4, lsum);
+            st_async_f32(rdst + (rows * D + row) * 4, M, rbar);
+            st_async_f32(rdst + (rows * D + rows + row) * 4, lsum, rbar);
         } else if (CLUSTER) {
             cp_m[row] = M;
             cp_l[row] = lsum;
@@ -1601,7 +1604,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                            make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc));
                 if (d == 0 && p.lse) p.lse[out_row(row)] = rowv[i].y;
             } else if (remote) {
-                st_cluster_f32x4(rdst + (row * D + d) * 4, acc[i]);
+                st_async_f32x4(rdst + (row * D + d) * 4, acc[i], rbar);
             } else if (CLUSTER) {
                 *reinterpret_cast<float4 *>(&cp_o[row * D + d]) = acc[i];
             } else {
@@ -1609,6 +1612,11 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
                 if (d == 0) *reinterpret_cast<float2 *>(&p.ws_ml[(wslot + row) * 2]) = rowv[i];
             }
         }
+    }
+    if (remote && !ok) {
+        // a failed split still delivers every byte rank 0 expects (its l = -1 marks it)
+        for (int c = ctid; c < rows * kC; c += kConsumerWarps * 32)
+            st_async_f32x4(rdst + (uint32_t)c * 16u, make_float4(0.f, 0.f, 0.f, 0.f), rbar);
     }
     if (splits == 1) return;
     merge_splits<D, kRows, CLUSTER>(p, recv, push, &merge_bar, &s_last, cp_o, cp_m, cp_l, wsc, rows, splits, split,

@@ -126,6 +126,23 @@ __device__ __forceinline__ void st_cluster_f32x4(uint32_t caddr, float4 v) {
                  : "memory");
 }
 
+// Asynchronous stores into another CTA's shared memory (cluster addresses) that
+// complete their bytes on an mbarrier of that CTA (`cbar`, a cluster address): the
+// receiver arms the barrier with the bytes it expects, and its wait ends once every
+// store has landed, with the data visible; the sender issues no release.
+__device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(caddr),
+                 "r"(__float_as_uint(v)), "r"(cbar)
+                 : "memory");
+}
+__device__ __forceinline__ void st_async_f32x4(uint32_t caddr, float4 v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                     caddr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(__float_as_uint(v.z)),
+                 "r"(__float_as_uint(v.w)), "r"(cbar)
+                 : "memory");
+}
+
 // Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t caddr) {
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
