@@ -729,6 +729,13 @@ __host__ __device__ constexpr bool cluster_push_fits(int splits, int rows, int r
     return (splits - 1) * cluster_slot_floats<D>(rows) * 4 <= recv_bytes;
 }
 
+// Whether the other CTAs' per-warp partials (one slot per consumer warp) fit rank 0's
+// receive region: then those CTAs skip their own warp merge.
+template <int D>
+__host__ __device__ constexpr bool warp_push_fits(int splits, int rows, int recv_bytes = AttnTile<D>::kRecvBytes) {
+    return (splits - 1) * kConsumerWarps * cluster_slot_floats<D>(rows) * 4 <= recv_bytes;
+}
+
 // Workspace merge of one unit's `nparts` partial states (this CTA's own already
 // written): the CTA that arrives last merges them. A unit's partials are packed
 // densely from the start of its region: (m, l) of split s, row `row` at float pair
@@ -895,6 +902,107 @@ __device__ __forceinline__ void workspace_merge(const AttnParams &p, uint64_t *b
         *reinterpret_cast<float2 *>(dst) = make_float2(acc[j].x / lsum, acc[j].y / lsum);
         *reinterpret_cast<float2 *>(dst + 2) = make_float2(acc[j].z / lsum, acc[j].w / lsum);
         if (cd[j] == 0 && p.lse) p.lse[out_row(crow[j])] = (Mr[j] + log2f(lsum)) * kLn2;
+    }
+}
+
+// Cluster merge from per-warp partials (rank 0, when warp_push_fits): this CTA's warps
+// have written theirs to sm_o [warps][kRows][MS], sm_m, sm_l; every warp of the other
+// CTAs has pushed its (o [rows][D], m [rows], l [rows]) into slot (rank - 1) * warps +
+// warp of `recv`, completing its bytes on `merge_bar`. One pass merges them all: one
+// thread per row derives the maximum, normaliser and every partial's weight (own warps'
+// weights over sm_m, the others' into `wrem` [partials][kRows]), then each thread sums
+// 4-float chunks of the output rows. A partial with l < 0 (a failed split), `skip`
+// (this CTA failed) or a wait that ran out writes nothing for the unit.
+template <int D, int kRows, typename OutRow>
+__device__ __forceinline__ void merge_cluster_warps(const AttnParams &p, uint64_t *merge_bar, const float *sm_o,
+                                                    float *sm_m, const float *sm_l, const float *recv, float *wrem,
+                                                    float *wsc, int rows, int splits, bool skip, OutRow out_row) {
+    constexpr int MS = AttnTile<D>::kMergeStride;
+    constexpr int kC = D / 4;  // 4-float chunks per row
+    const int ctid = threadIdx.x;
+    const int slot_f = cluster_slot_floats<D>(rows);
+    const int nrem = (splits - 1) * kConsumerWarps;
+    const bool got = mbar_wait_cluster_bounded(merge_bar, 0);  // every pushed byte has landed
+    // The pushed partials are in this CTA's memory now: the other CTAs may exit.
+    if (got && ctid >= 1 && ctid < splits) mbar_arrive_remote_relaxed(cluster_map(smem_u32(merge_bar), ctid));
+    float *scale_row = wsc;        // [kRows]
+    float *lse_row = wsc + kRows;  // [kRows]
+    bool bad = skip || !got;
+    if (!bad && ctid < rows) {
+        const int row = ctid;
+        float M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w)
+            if (sm_l[w * kRows + row] > 0.f) M = fmaxf(M, sm_m[w * kRows + row]);
+        for (int q = 0; q < nrem; ++q) {
+            const float *ml = recv + q * slot_f + rows * D;
+            const float l = ml[rows + row];
+            bad |= l < 0.f;
+            if (l > 0.f) M = fmaxf(M, ml[row]);
+        }
+        float lsum = 0.f;
+#pragma unroll
+        for (int w = 0; w < kConsumerWarps; ++w) {
+            const float l = sm_l[w * kRows + row];
+            const float f = l > 0.f ? fast_exp2(sm_m[w * kRows + row] - M) : 0.f;
+            sm_m[w * kRows + row] = f;
+            lsum += l > 0.f ? l * f : 0.f;
+        }
+        for (int q = 0; q < nrem; ++q) {
+            const float *ml = recv + q * slot_f + rows * D;
+            const float l = ml[rows + row];
+            const float f = l > 0.f ? fast_exp2(ml[row] - M) : 0.f;
+            wrem[q * kRows + row] = f;
+            lsum += l > 0.f ? l * f : 0.f;
+        }
+        scale_row[row] = 1.f / lsum;
+        lse_row[row] = (M + log2f(lsum)) * kLn2;
+    }
+    // A failed split fails every row of the unit; make the decision CTA-wide.
+    const bool fail = consumer_bar_or(bad);
+    if (!got && ctid == 0) report(p.dev_status, SFI_DEV_TIMEOUT);
+    if (fail) return;
+    // Every chunk of this thread is summed (all shared-memory reads) before any of the
+    // stores is issued.
+    constexpr int kIt = (kRows * kC + kConsumerWarps * 32 - 1) / (kConsumerWarps * 32);
+    float4 acc[kIt];
+    float lse_v[kIt];
+#pragma unroll
+    for (int i = 0; i < kIt; ++i) {
+        const int c = ctid + i * kConsumerWarps * 32;
+        acc[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+        lse_v[i] = 0.f;
+        if (c < rows * kC) {
+            const int row = c / kC, d = (c - row * kC) * 4;
+#pragma unroll
+            for (int w = 0; w < kConsumerWarps; ++w) {
+                const float f = sm_m[w * kRows + row];
+                const float4 ow = *reinterpret_cast<const float4 *>(&sm_o[(w * kRows + row) * MS + d]);
+                acc[i].x += ow.x * f;
+                acc[i].y += ow.y * f;
+                acc[i].z += ow.z * f;
+                acc[i].w += ow.w * f;
+            }
+            for (int q = 0; q < nrem; ++q) {
+                const float f = wrem[q * kRows + row];
+                const float4 oq = *reinterpret_cast<const float4 *>(&recv[q * slot_f + row * D + d]);
+                acc[i].x += oq.x * f;
+                acc[i].y += oq.y * f;
+                acc[i].z += oq.z * f;
+                acc[i].w += oq.w * f;
+            }
+            const float sc = scale_row[row];
+            acc[i] = make_float4(acc[i].x * sc, acc[i].y * sc, acc[i].z * sc, acc[i].w * sc);
+            lse_v[i] = lse_row[row];
+        }
+    }
+#pragma unroll
+    for (int i = 0; i < kIt; ++i) {
+        const int c = ctid + i * kConsumerWarps * 32;
+        if (c >= rows * kC) break;
+        const int row = c / kC, d = (c - row * kC) * 4;
+        store_out4(&p.out[out_row(row) * D + d], acc[i]);
+        if (d == 0 && p.lse) p.lse[out_row(row)] = lse_v[i];
     }
 }
 
@@ -1157,12 +1265,15 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         // asynchronous stores complete them); pull merge: one arrival per other CTA;
         // workspace merge: the last CTA's bulk copies of the unit's partials
         const int mrows = MQ ? p.rows : p.group;
+        const bool wpush0 = CLUSTER && !MQ && warp_push_fits<D>(splits, mrows, kPushBytes);
         const bool push0 = CLUSTER && split == 0 && cluster_push_fits<D>(splits, mrows, kPushBytes);
         if (CLUSTER)
             mbar_init(&merge_bar, split != 0 || push0 ? 1u : (uint32_t)(splits - 1));
         else
             mbar_init(&merge_bar, 1u);
-        if (push0) mbar_arrive_expect_tx(&merge_bar, (uint32_t)((splits - 1) * mrows * (D + 2) * 4));
+        if (push0)
+            mbar_arrive_expect_tx(&merge_bar,
+                                  (uint32_t)((splits - 1) * (wpush0 ? kConsumerWarps : 1) * mrows * (D + 2) * 4));
         s_timeout = 0;
         s_bad = 0;
         fence_barrier_init();
@@ -1470,6 +1581,41 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 1);
         l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 2);
     }
+    // up to 8 query rows: rows g + 8 hold the P_lo V half of row g
+    const bool packed = !MQ || p.rows <= kMaxGroup;
+    const int rows = MQ ? p.rows : G;
+    float *recv = reinterpret_cast<float *>(smem + T::kRecvOffset);
+    // Small partials: every warp of a CTA other than cluster rank 0 sends its own partial
+    // straight into its slot of rank 0's receive region as soon as its stream ends, and
+    // rank 0 merges all the cluster's warps in one pass (no warp merge in those CTAs).
+    // Single-token kernels only: in the multi-token one the partials rarely fit, and the
+    // extra path alone cost its drafts 0.2 us per launch.
+    const bool wpush = CLUSTER && !MQ && splits > 1 && warp_push_fits<D>(splits, rows, kPushBytes);
+    if (wpush && split != 0) {
+        const bool bad_w = timed_out || s_bad != 0;  // l = -1: rank 0 writes nothing for the unit
+        const uint32_t cbar = cluster_map(smem_u32(&merge_bar), 0);
+        const uint32_t slot = cluster_map(smem_u32(recv), 0) +
+                              (uint32_t)(((split - 1) * kConsumerWarps + warp) * cluster_slot_floats<D>(rows)) * 4u;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int row = g + 8 * half;
+            if ((half == 1 && packed) || row >= rows) continue;
+#pragma unroll
+            for (int nt = 0; nt < D / 8; ++nt) {
+                float2 v = packed ? make_float2(o[nt][0] + o[nt][2], o[nt][1] + o[nt][3])
+                                  : make_float2(o[nt][2 * half], o[nt][2 * half + 1]);
+                if (bad_w) v = make_float2(0.f, 0.f);
+                st_async_f32x2(slot + (uint32_t)(row * D + nt * 8 + 2 * t) * 4u, v, cbar);
+            }
+            if (t == 0) {
+                st_async_f32(slot + (uint32_t)(rows * D + row) * 4u, m_run[half], cbar);
+                st_async_f32(slot + (uint32_t)(rows * D + rows + row) * 4u, bad_w ? -1.f : l_run[half], cbar);
+            }
+        }
+        // Rank 0 signals once every push has landed; only then may this CTA exit.
+        if (threadIdx.x == 0 && !mbar_wait_cluster_bounded(&merge_bar, 0)) report(p.dev_status, SFI_DEV_TIMEOUT);
+        return;
+    }
 
     // ---- merge the consumer warps through shared memory (stage buffers are free now) ----
     consumer_bar_sync();
@@ -1483,8 +1629,6 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     float *cp_m = cp_o + kRows * D;                                 // [kRows]
     float *cp_l = cp_m + kRows;                                     // [kRows]
     float *wsc = cp_l + kRows;                                      // [kMaxClusterSplits + 2][kRows] merge scratch
-    // up to 8 query rows: rows g + 8 hold the P_lo V half of row g
-    const bool packed = !MQ || p.rows <= kMaxGroup;
     if (ok) {
 #pragma unroll
         for (int nt = 0; nt < D / 8; ++nt) {
@@ -1507,7 +1651,6 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     consumer_bar_sync();
 
     const int ctid = threadIdx.x;  // 0 .. 127
-    const int rows = MQ ? p.rows : G;
     // output row of tile row `row`: (request, token row / G, head kvh * G + row % G)
     const int64_t head0 = (int64_t)r * p.hq + (int64_t)kvh * G;
     auto out_row = [&](int row) -> int64_t {
@@ -1518,9 +1661,12 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     // A partial that must not reach the output (a bad page id in the unit, or a timed-out
     // wait) carries l = -1: every merge that sees it skips the unit's writes.
     const bool skip = !ok || s_bad != 0;
+    if (wpush) {  // cluster rank 0 with per-warp partials from the other CTAs
+        merge_cluster_warps<D, kRows>(p, &merge_bar, sm_o, sm_m, sm_l, recv, cp_o, wsc, rows, splits, skip, out_row);
+        return;
+    }
     // Where this CTA's partial goes: the output (one split), rank 0's receive region
     // (cluster push from another rank), cp_* (cluster rank 0, or pull), or the workspace.
-    float *recv = reinterpret_cast<float *>(smem + T::kRecvOffset);
     const bool push = CLUSTER && cluster_push_fits<D>(splits, rows, kPushBytes);
     const bool remote = push && split != 0;
     const uint32_t rdst =

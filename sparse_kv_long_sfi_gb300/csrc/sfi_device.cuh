@@ -135,6 +135,11 @@ __device__ __forceinline__ void st_async_f32(uint32_t caddr, float v, uint32_t c
                  "r"(__float_as_uint(v)), "r"(cbar)
                  : "memory");
 }
+__device__ __forceinline__ void st_async_f32x2(uint32_t caddr, float2 v, uint32_t cbar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v2.b32 [%0], {%1, %2}, [%3];" ::"r"(caddr),
+                 "r"(__float_as_uint(v.x)), "r"(__float_as_uint(v.y)), "r"(cbar)
+                 : "memory");
+}
 __device__ __forceinline__ void st_async_f32x4(uint32_t caddr, float4 v, uint32_t cbar) {
     asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.b32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
                      caddr),
