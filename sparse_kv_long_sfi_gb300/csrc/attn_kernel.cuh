@@ -1279,13 +1279,13 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         fence_barrier_init();
     }
     // Every CTA of a cluster reaches this point unconditionally (the only branch
-    // before it depends on the unit's metadata, which all of them read alike): after
-    // it, each CTA's merge barrier is initialised for remote arrivals. (Letting the
-    // producer warp issue the ring's first fill before this barrier was measured
-    // slower: fast step at batch 16, 13.6 -> 14.3 us per launch. A relaxed cluster
-    // arrive instead of a release one: drafts at batch 16, T = 1 / 4 / 8, 14.7 / 15.3 /
-    // 17.9 -> 14.5 / 15.2 / 17.3 us per launch.)
-    if (CLUSTER) cluster_sync_after_init();
+    // before it depends on the unit's metadata, which all of them read alike) and
+    // arrives on the cluster barrier; a thread waits on it only before its first access
+    // to another CTA (after its stream), by when each CTA's merge barrier is
+    // initialised for remote arrivals. (A relaxed cluster arrive instead of a release
+    // one: drafts at batch 16, T = 1 / 4 / 8, 14.7 / 15.3 / 17.9 -> 14.5 / 15.2 / 17.3 us
+    // per launch.)
+    if (CLUSTER) cluster_arrive_after_init();
     else __syncthreads();
 
     if (warp == kConsumerWarps) {
@@ -1397,6 +1397,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
             if (!fast && st == T::kStages - 1)
                 for (int pst = T::kStages; pst < 8 && pst < n_stages; ++pst) prefetch_stage(pst, cur);
         }
+        if (CLUSTER) cluster_wait();
         return;  // the producer takes no part in the merges
     }
 
@@ -1581,6 +1582,7 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
         l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 1);
         l_run[half] += __shfl_xor_sync(0xffffffffu, l_run[half], 2);
     }
+    if (CLUSTER) cluster_wait();  // the other CTAs' mbarriers are initialised
     // up to 8 query rows: rows g + 8 hold the P_lo V half of row g
     const bool packed = !MQ || p.rows <= kMaxGroup;
     const int rows = MQ ? p.rows : G;

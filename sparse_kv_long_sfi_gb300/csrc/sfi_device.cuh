@@ -88,11 +88,16 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 // CTA initialised the CTA's mbarriers and ran fence_barrier_init: the CTA barrier
 // orders that thread's other shared-memory writes for its own CTA, the init fence
 // publishes the mbarrier initialisation to the cluster, so the cluster arrive can be
-// relaxed (a release arrive cost 0.3 us of every CTA's start-up).
-__device__ __forceinline__ void cluster_sync_after_init() {
+// relaxed (a release arrive cost 0.3 us of every CTA's start-up). It is split in two:
+// every thread arrives right after the initialisation and waits (acquire) only before
+// its first access to another CTA's shared memory or mbarriers, so the streams start
+// without waiting for the rest of the cluster. Every arriving thread waits once before
+// it exits.
+__device__ __forceinline__ void cluster_arrive_after_init() {
     __syncthreads();
-    asm volatile("barrier.cluster.arrive.relaxed.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
 }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // shared::cluster address of the variable at local shared address `saddr` in CTA `rank`.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
