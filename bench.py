@@ -207,7 +207,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "2162431949b7fa8d", "fast": 68_272_384 + 711_680, "slow": 1_073_961_216 + 6_628_352}
+PROFILED_TRAFFIC = {"sha256_16": "7bb7a7e6c5655776", "fast": 68_289_280 + 576_000, "slow": 1_074_048_768 + 6_731_264}
 
 
 def profiled_traffic(kind):
