@@ -1255,6 +1255,21 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     const int pad = (kConsumerWarps - n_my % kConsumerWarps) % kConsumerWarps;
     const int sb0 = sb_begin - pad;
     const int n_stages = (n_my + pad) / kConsumerWarps;
+    // Page id of sub-block sb (-1 for compact sub-blocks and past the split's range).
+    const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
+    auto page_of = [&](int sb) -> int {
+        if (sb >= sb_end || sb < sb_begin || sb < u.nb1) return -1;
+        return ptab[u.page0 + (sb - u.nb1)];
+    };
+    // When the first stage holds paged sub-blocks (dense units), the producer warp issues
+    // the loads of its first two chunks of page ids now: they travel while the barriers
+    // are initialised.
+    const bool ids_first = warp == kConsumerWarps && sb0 + kConsumerWarps > u.nb1;
+    int ids_cur = -1, ids_nxt = -1;
+    if (ids_first) {
+        ids_cur = page_of(sb0 + lane);
+        ids_nxt = page_of(sb0 + 32 + lane);
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < T::kStages; ++i) {
@@ -1291,23 +1306,16 @@ __global__ void __launch_bounds__(kAttnThreads, kAttnCtasPerSm)
     if (warp == kConsumerWarps) {
         // ---------------- producer warp ----------------
         const uint64_t policy = l2_policy_evict_first();
-        const int32_t *ptab = p.page_table + (int64_t)r * p.max_pages;
-        // Page id of sub-block sb (-1 for compact sub-blocks and past the end).
-        auto page_of = [&](int sb) -> int {
-            if (sb >= sb_end || sb < sb_begin || sb < u.nb1) return -1;
-            return ptab[u.page0 + (sb - u.nb1)];
-        };
         // Page ids of the current and the next chunk of 32 sub-blocks. When the first stage
         // is all compact rows they are loaded only after its copies are issued, so those
         // copies do not wait for the page table.
-        int cur = -1, nxt = -1;
-        bool ids_loaded = false;
+        int cur = ids_cur, nxt = ids_nxt;
+        bool ids_loaded = ids_first;
         auto load_ids = [&]() {
             cur = page_of(sb0 + lane);
             nxt = page_of(sb0 + 32 + lane);
             ids_loaded = true;
         };
-        if (sb0 + kConsumerWarps > u.nb1) load_ids();  // the first stage holds paged sub-blocks
         // L2 prefetch of stage pst's sub-blocks (page ids of its chunk of 32 in page_src;
         // warp-collective). Dense units prefetch the rest of their first chunk right after
         // the ring's first fill, so the first refills read L2 without delaying the ring's
