@@ -369,8 +369,10 @@ def _fast_case(seed, lens, Hq, Hkv, D, S, W, k_per_req, k_cap, splits=0, req_ids
     return prob
 
 
-@pytest.mark.parametrize("splits", [1, 2, 5, 0])
+@pytest.mark.parametrize("splits", [1, 2, 3, 4, 5, 0])
 def test_fast_step_matches_oracle(splits):
+    """Split plans of one CTA, clusters whose other CTAs send per-warp partials (2-4
+    splits at G = 2), clusters that send one partial per CTA (5) and the automatic plan."""
     lens = [1024, 1031, 530, 36, 30, 3, 17]
     _fast_case(21 + splits, lens, 16, 8, 128, 4, 32, [64, 64, 100, 5, 5, 5, 5], 128, splits=splits)
 
