@@ -37,7 +37,8 @@
 //    chunks). Splits of a unit merge in-kernel: with up to 8 splits the unit's CTAs
 //    form one thread-block cluster and the other ranks store their partial (m, l, o)
 //    states into rank 0's shared memory with asynchronous stores that complete on rank
-//    0's mbarrier (or rank 0 reads them through distributed shared memory when they do
+//    0's mbarrier (one partial per warp, without their own warp merge, when those fit;
+//    rank 0 reads them through distributed shared memory when even one per CTA does
 //    not fit); with more, the last CTA of the unit (atomic
 //    counter, self-resetting) merges them from a global workspace.
 //  * Every wait on the pipeline or on a peer CTA is bounded and reports
