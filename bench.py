@@ -207,7 +207,7 @@ def append_bytes(B, Hkv, D):
 PROFILED_SOURCES = ("sparse_kv_long_sfi_gb300/csrc/attn_kernel.cuh", "sparse_kv_long_sfi_gb300/csrc/attn_decode.cu",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_device.cuh", "sparse_kv_long_sfi_gb300/csrc/sfi_internal.h",
                     "sparse_kv_long_sfi_gb300/csrc/sfi_api.cu")
-PROFILED_TRAFFIC = {"sha256_16": "66c9e6abe1db0be7", "fast": 68_289_280 + 590_592, "slow": 1_073_978_880 + 6_813_440}
+PROFILED_TRAFFIC = {"sha256_16": "b1a619051ccb121b", "fast": 68_289_280 + 574_208, "slow": 1_073_954_560 + 6_764_800}
 
 
 def profiled_traffic(kind):
