@@ -377,6 +377,17 @@ def test_fast_step_matches_oracle(splits):
     _fast_case(21 + splits, lens, 16, 8, 128, 4, 32, [64, 64, 100, 5, 5, 5, 5], 128, splits=splits)
 
 
+@pytest.mark.parametrize("D,splits", [(128, 7), (64, 8)])
+def test_fast_step_per_warp_partials_from_many_ctas(D, splits):
+    """One query row per KV head (G = 1): the other CTAs of a 7- or 8-CTA cluster each
+    send four per-warp partials (up to 28) into rank 0's receive region, merged in one pass."""
+    lens = [2000, 1500, 1800, 1200]
+    k_cap = 1024
+    shape = _sfi().AttnShape(8, 8, D)
+    assert _sfi().sfi_plan_splits(shape, len(lens), 4 + k_cap + 32 + 32, splits) == splits
+    _fast_case(61 + splits, lens, 8, 8, D, 4, 32, [900, 700, 1000, 500], k_cap, splits=splits)
+
+
 @pytest.mark.parametrize("bounds", ["tight", "underestimated"])
 def test_ragged_fast_step_matches_oracle(bounds):
     """SFI_ATTN_RAGGED: the fast step planned in fixed-size chunks over requests whose
