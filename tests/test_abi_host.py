@@ -118,6 +118,18 @@ def test_workspace_size_rejects_bad_shapes(libsfi):
         assert libsfi.sfi_attn_cluster_capacity(bad) == 0
 
 
+def test_cluster_capacity_needs_a_device(libsfi):
+    """The capacity query answers 0 for every valid size when there is no CUDA device
+    (so automatic plans keep the slot-count rule), and a positive count with one."""
+    import torch
+    caps = [libsfi.sfi_attn_cluster_capacity(c) for c in range(1, 9)]
+    if torch.cuda.is_available():
+        assert all(c > 0 for c in caps)
+    else:
+        assert caps == [0] * 8
+        assert libsfi.sfi_plan_splits(ctypes.byref(_shape()), 4, 4096, 3) == 3  # plans still answer
+
+
 def test_multi_token_calls_validate_on_the_host(libsfi):
     from sparse_kv_long_sfi_gb300 import _abi
     sh, kv = _shape(), _paged()  # G = 2: at most 8 tokens
